@@ -1,0 +1,225 @@
+"""CPU oracle for the MX block-scaled and FP16/BF16 matrix multiply.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers.  The product library never imports it,
+and it imports nothing from the product.
+
+The arithmetic lives in ``mx_oracle.c`` (float64 throughout, formats decoded
+from their bit fields, encoding by search over the representable values); this
+module compiles it with gcc on first use and marshals numpy arrays in and out.
+
+What each function follows:
+  * ``quantize`` -- the OCP MX conversion rule on blocks of 32 consecutive
+    K elements sharing one UE8M0 scale (WWDC26 session 330, "Multi-plane
+    tensors" and its 4:48 listing: block factors {32, 1} on the innermost
+    dimension; the MX scaling formats named in "Managing quantized data").
+  * ``gemm_mx`` / ``gemm_f16`` -- the float64 reference over exactly the same
+    quantized bytes (RIGEL technical summary, "Metodologia", checksum gate),
+    returning C and S = sum_k |a_ik * b_kj| for the per-element tolerance
+    |C_gpu - C| <= tol * S.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3 = 1
+E2M1 = 2
+F16 = 2
+BF16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mx_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mx_oracle.c`` into ``liboracle.so`` (gcc, OpenMP)."""
+    stale = (not os.path.exists(_LIB)
+             or os.path.getmtime(_LIB) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        u8, u16, i32, i64, dbl = (ctypes.c_uint8, ctypes.c_uint16,
+                                  ctypes.c_int, ctypes.c_int64,
+                                  ctypes.c_double)
+        p = ctypes.c_void_p
+        lib.mxo_decode_e4m3.restype = dbl
+        lib.mxo_decode_e4m3.argtypes = [u8]
+        lib.mxo_decode_e2m1.restype = dbl
+        lib.mxo_decode_e2m1.argtypes = [u8]
+        lib.mxo_decode_ue8m0.restype = dbl
+        lib.mxo_decode_ue8m0.argtypes = [u8]
+        lib.mxo_decode_f16.restype = dbl
+        lib.mxo_decode_f16.argtypes = [u16]
+        lib.mxo_decode_bf16.restype = dbl
+        lib.mxo_decode_bf16.argtypes = [u16]
+        lib.mxo_encode_e4m3.restype = u8
+        lib.mxo_encode_e4m3.argtypes = [dbl]
+        lib.mxo_encode_e2m1.restype = u8
+        lib.mxo_encode_e2m1.argtypes = [dbl]
+        lib.mxo_floor_log2_f32.restype = i32
+        lib.mxo_floor_log2_f32.argtypes = [ctypes.c_float]
+        lib.mxo_quantize.restype = None
+        lib.mxo_quantize.argtypes = [p, i64, i64, i64, i64, i32, p, p]
+        lib.mxo_gemm_mx.restype = None
+        lib.mxo_gemm_mx.argtypes = [p, p, p, p, i64, i64, i64, i32, p, i64,
+                                    p, p]
+        lib.mxo_gemm_f16.restype = None
+        lib.mxo_gemm_f16.argtypes = [p, p, i64, i64, i64, i32, p, i64, p, p]
+        lib.mxo_num_threads.restype = i32
+        lib.mxo_num_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+# --------------------------------------------------------------------------
+# scalar codecs
+# --------------------------------------------------------------------------
+
+def decode_e4m3(code: int) -> float:
+    return _load().mxo_decode_e4m3(int(code) & 0xFF)
+
+
+def decode_e2m1(code: int) -> float:
+    return _load().mxo_decode_e2m1(int(code) & 0xF)
+
+
+def decode_ue8m0(code: int) -> float:
+    return _load().mxo_decode_ue8m0(int(code) & 0xFF)
+
+
+def decode_f16(bits: int) -> float:
+    return _load().mxo_decode_f16(int(bits) & 0xFFFF)
+
+
+def decode_bf16(bits: int) -> float:
+    return _load().mxo_decode_bf16(int(bits) & 0xFFFF)
+
+
+def encode_e4m3(v: float) -> int:
+    return int(_load().mxo_encode_e4m3(float(v)))
+
+
+def encode_e2m1(v: float) -> int:
+    return int(_load().mxo_encode_e2m1(float(v)))
+
+
+def floor_log2_f32(a: float) -> int:
+    return int(_load().mxo_floor_log2_f32(float(a)))
+
+
+def decode_table(fmt: int) -> np.ndarray:
+    """float64 value of every code: 256 entries for E4M3, 16 for E2M1."""
+    if fmt == E4M3:
+        return np.array([decode_e4m3(c) for c in range(256)])
+    return np.array([decode_e2m1(c) for c in range(16)])
+
+
+def num_threads() -> int:
+    return int(_load().mxo_num_threads())
+
+
+# --------------------------------------------------------------------------
+# array operations
+# --------------------------------------------------------------------------
+
+def quantize(src: np.ndarray, fmt: int, k_axis: int = 1):
+    """OCP MX quantization of a 2-D float32 matrix.
+
+    ``k_axis=1``: src is outer x K (K contiguous; the A operand).
+    ``k_axis=0``: src is K x outer (the row-major K x N B operand); blocks of
+    32 still run along K, i.e. down the columns.
+
+    Returns ``(codes, scales)``: codes outer x K uint8, one code per byte
+    (E2M1 codes in the low nibble), and scales outer x K/32 UE8M0 codes.
+    """
+    lib = _load()
+    src = np.ascontiguousarray(src, dtype=np.float32)
+    if k_axis == 1:
+        outer, K = src.shape
+        s_row, s_k = K, 1
+    else:
+        K, outer = src.shape
+        s_row, s_k = 1, outer
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    codes = np.empty((outer, K), dtype=np.uint8)
+    scales = np.empty((outer, K // 32), dtype=np.uint8)
+    lib.mxo_quantize(_ptr(src), outer, K, s_row, s_k, fmt, _ptr(codes),
+                     _ptr(scales))
+    return codes, scales
+
+
+def _rows_arg(rows, M):
+    if rows is None:
+        return None, M
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if r.size and (r.min() < 0 or r.max() >= M):
+        raise IndexError("row index out of range")
+    return r, int(r.size)
+
+
+def gemm_mx(codesA, scalesA, codesB, scalesB, fmt: int, rows=None):
+    """float64 C = A_mx * B_mx^T and S = sum |products|.
+
+    codesA M x K, scalesA M x K/32, codesB N x K, scalesB N x K/32 (both
+    operands K-major, as returned by ``quantize``).  ``rows`` restricts the
+    evaluation to those rows of A (C and S then have len(rows) rows).
+    """
+    lib = _load()
+    cA = np.ascontiguousarray(codesA, dtype=np.uint8)
+    sA = np.ascontiguousarray(scalesA, dtype=np.uint8)
+    cB = np.ascontiguousarray(codesB, dtype=np.uint8)
+    sB = np.ascontiguousarray(scalesB, dtype=np.uint8)
+    M, K = cA.shape
+    N, K2 = cB.shape
+    if K != K2 or sA.shape != (M, K // 32) or sB.shape != (N, K // 32):
+        raise ValueError("shape mismatch")
+    r, nr = _rows_arg(rows, M)
+    C = np.empty((nr, N), dtype=np.float64)
+    S = np.empty((nr, N), dtype=np.float64)
+    lib.mxo_gemm_mx(_ptr(cA), _ptr(sA), _ptr(cB), _ptr(sB), M, N, K, fmt,
+                    None if r is None else _ptr(r), nr, _ptr(C), _ptr(S))
+    return C, S
+
+
+def gemm_f16(A_bits, B_bits, dtype: int, rows=None):
+    """float64 C = A * B for row-major fp16/bf16 bit patterns (uint16)
+    A (M x K) and B (K x N); also S = sum |products|."""
+    lib = _load()
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("shape mismatch")
+    r, nr = _rows_arg(rows, M)
+    C = np.empty((nr, N), dtype=np.float64)
+    S = np.empty((nr, N), dtype=np.float64)
+    lib.mxo_gemm_f16(_ptr(A), _ptr(B), M, N, K, dtype,
+                     None if r is None else _ptr(r), nr, _ptr(C), _ptr(S))
+    return C, S

@@ -1,0 +1,159 @@
+"""Seeded synthetic inputs for the MX / FP16 GEMM workloads.
+
+Shared by the tests, the smoke check and the benchmark, so that the oracle
+and the CUDA library always see identical bytes.  This module holds no part of
+the method's arithmetic (no quantization, no matmul): it only draws numbers.
+
+Every source is drawn on the CPU in float32 with ``torch.Generator`` seeded
+per matrix, so the values do not depend on the device or on its RNG.
+
+Workloads (sizes and value recipes):
+  mx256      MXFP8, M=N=K=256, N(0,1) sources, fp32 output
+  f16        FP16 / BF16 dense, M=N=K in {1024, 2048, 4096}, U[-1, 1]
+             sources rounded to the 16-bit type, fp32 output
+  mxfp8      MXFP8, M=N=K in {2048, 4096, 8192}, N(0,1) with 1 % of the
+             entries (Bernoulli(0.01), drawn from the same generator)
+             multiplied by 100, bf16 output
+  mxfp4      MXFP4, M=N=K in {4096, 8192}, N(0,1), bf16 output
+  proj       transformer projections of a 1B-parameter model at 32 x 512
+             tokens (M=16384), hidden 2048, FFN 8192: qkv (K=2048, N=6144),
+             out (K=2048, N=2048), up (K=2048, N=8192), down (K=8192,
+             N=2048); activations N(0,1) as A, weights N(0, 0.02) as B
+             (K x N), MXFP8, bf16 output
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class GemmCase:
+    name: str
+    kind: str          # "mxfp8" | "mxfp4" | "f16" | "bf16"
+    M: int
+    N: int
+    K: int
+    out: str           # "f32" | "bf16"
+    dist_a: str        # value recipe of A
+    dist_b: str        # value recipe of B
+    seed_a: int
+    seed_b: int
+
+
+def _seeds(group: int, tag: int):
+    base = 1000 * group + 10 * tag
+    return base + 1, base + 2
+
+
+def mx256() -> GemmCase:
+    sa, sb = _seeds(0, 8)
+    return GemmCase("mx256", "mxfp8", 256, 256, 256, "f32", "normal",
+                    "normal", sa, sb)
+
+
+def f16_cases():
+    out = []
+    for kind in ("f16", "bf16"):
+        for n in (1024, 2048, 4096):
+            sa, sb = _seeds(1, int(math.log2(n)))
+            out.append(GemmCase(f"{kind}_{n}", kind, n, n, n, "f32",
+                                "uniform", "uniform", sa, sb))
+    return out
+
+
+def mxfp8_cases():
+    out = []
+    for n in (2048, 4096, 8192):
+        sa, sb = _seeds(2, int(math.log2(n)))
+        out.append(GemmCase(f"mxfp8_{n}", "mxfp8", n, n, n, "bf16",
+                            "outlier", "outlier", sa, sb))
+    return out
+
+
+def mxfp4_cases():
+    out = []
+    for n in (4096, 8192):
+        sa, sb = _seeds(3, int(math.log2(n)))
+        out.append(GemmCase(f"mxfp4_{n}", "mxfp4", n, n, n, "bf16",
+                            "normal", "normal", sa, sb))
+    return out
+
+
+PROJ_SHAPES = (("qkv", 2048, 6144), ("out", 2048, 2048), ("up", 2048, 8192),
+               ("down", 8192, 2048))
+
+
+def proj_cases():
+    out = []
+    for i, (name, K, N) in enumerate(PROJ_SHAPES):
+        sa, sb = _seeds(4, i)
+        out.append(GemmCase(f"proj_{name}", "mxfp8", 16384, N, K, "bf16",
+                            "normal", "weight", sa, sb))
+    return out
+
+
+def all_cases():
+    return [mx256()] + f16_cases() + mxfp8_cases() + mxfp4_cases() + \
+        proj_cases()
+
+
+def case(name: str) -> GemmCase:
+    for c in all_cases():
+        if c.name == name:
+            return c
+    raise KeyError(name)
+
+
+def draw(shape, dist: str, seed: int) -> torch.Tensor:
+    """float32 CPU tensor of the given recipe, from its own seeded stream."""
+    g = torch.Generator().manual_seed(int(seed))
+    if dist == "normal":
+        return torch.randn(shape, generator=g, dtype=torch.float32)
+    if dist == "weight":
+        return torch.randn(shape, generator=g, dtype=torch.float32) * 0.02
+    if dist == "uniform":
+        return torch.rand(shape, generator=g, dtype=torch.float32) * 2 - 1
+    if dist == "outlier":
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        mask = torch.rand(shape, generator=g, dtype=torch.float32) < 0.01
+        return torch.where(mask, x * 100.0, x)
+    raise ValueError(dist)
+
+
+def sources(c: GemmCase, M: int | None = None, N: int | None = None,
+            K: int | None = None):
+    """(A, B) float32 sources: A is M x K row-major, B is K x N row-major.
+    Sizes may be overridden to draw a smaller problem of the same recipe."""
+    M = c.M if M is None else M
+    N = c.N if N is None else N
+    K = c.K if K is None else K
+    A = draw((M, K), c.dist_a, c.seed_a)
+    B = draw((K, N), c.dist_b, c.seed_b)
+    if c.kind in ("f16", "bf16"):
+        dt = torch.float16 if c.kind == "f16" else torch.bfloat16
+        A, B = A.to(dt), B.to(dt)
+    return A, B
+
+
+def random_codes(shape, fmt: int, seed: int, scale_lo: int = 112,
+                 scale_hi: int = 142):
+    """Random MX planes for GEMM-only tests: finite element codes (uint8,
+    one per byte, unpacked) and UE8M0 scale codes drawn uniformly from
+    [scale_lo, scale_hi].  Returns (codes outer x K, scales outer x K/32)."""
+    outer, K = shape
+    g = torch.Generator().manual_seed(int(seed))
+    if fmt == 1:
+        codes = torch.randint(0, 256, (outer, K), generator=g,
+                              dtype=torch.int32)
+        # 0x7F and 0xFF are NaN in E4M3: redraw them as zeros
+        codes = torch.where((codes & 0x7F) == 0x7F, torch.zeros_like(codes),
+                            codes)
+    else:
+        codes = torch.randint(0, 16, (outer, K), generator=g,
+                              dtype=torch.int32)
+    scales = torch.randint(scale_lo, scale_hi + 1, (outer, K // 32),
+                           generator=g, dtype=torch.int32)
+    return (codes.to(torch.uint8).numpy(), scales.to(torch.uint8).numpy())
