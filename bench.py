@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of the MX block-scaled GEMM hot path on one GB300 (or N, as
+independent replicas: weak scaling).
+
+One step = the whole path on one batch of synthetic input resident in HBM:
+  mx_quantize(A fp32 8192 x 8192 -> E4M3 + UE8M0)
+  mx_quantize(B fp32 8192 x 8192, row-major K x N -> E4M3 + UE8M0, K-major)
+  mx_gemm(A_mx, B_mx -> C bf16 8192 x 8192)
+value = 2*M*N*K / step time, in TFLOP/s.  The fp32 sources (268 MB each) are
+larger than L2 (129 MB), so no step finds its inputs in L2.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+                  [--workload mxfp8_8192|mxfp4_8192|bf16_4096|...]
+
+--impl reference times the CPU oracle (float64, OpenMP) on a bounded sample
+of the same workload (rows of C computed from the fp32 sources) on the host
+cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# nominal dense ratios to bf16: fp8 2x, fp4 6x (2.25 / 4.5 / 13.5 PFLOP/s)
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0}
+
+
+def peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "measured")
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2])
+                          if v.lower().startswith("active")})
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ our arm
+
+def flops_of(c):
+    return 2.0 * c.M * c.N * c.K
+
+
+def quant_bytes(fmt, rows, K):
+    """Algorithmic bytes of one mx_quantize: fp32 in, codes + scales out."""
+    code = rows * K if fmt == 1 else rows * K / 2
+    return 4.0 * rows * K + code + rows * K / 32
+
+
+def run_ours(args, rank, world, local_rank):
+    import block_scaled_quantized_mx_gb300 as mx
+    mx.build()
+    mx.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    c = workloads.case(args.workload)
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    stream = torch.cuda.current_stream()
+
+    A, B = workloads.sources(c)
+    is_mx = c.kind in ("mxfp8", "mxfp4")
+    fmt = {"mxfp8": mx.E4M3, "mxfp4": mx.E2M1}.get(c.kind)
+    out_dt = torch.bfloat16 if c.out == "bf16" else torch.float32
+    dA, dB = A.to(dev), B.to(dev)
+    C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
+    if is_mx:
+        qa = mx.empty_mx(fmt, c.M, c.K, dev)
+        qb = mx.empty_mx(fmt, c.N, c.K, dev)
+
+    # per-kernel events so every launch's duration is known
+    def step(ev=None):
+        if is_mx:
+            if ev is not None:
+                ev[0].record(stream)
+            mx.mx_quantize(dA, fmt, out=qa)
+            if ev is not None:
+                ev[1].record(stream)
+            mx.mx_quantize(dB, fmt, k_strided=True, out=qb)
+            if ev is not None:
+                ev[2].record(stream)
+            mx.mx_gemm(qa, qb, out_dtype=out_dt, out=C)
+            if ev is not None:
+                ev[3].record(stream)
+        else:
+            if ev is not None:
+                ev[0].record(stream)
+            mx.gemm_f16(dA, dB, out=C)
+            if ev is not None:
+                ev[1].record(stream)
+
+    launches_per_step = 3 if is_mx else 1
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mx.mx_last_error() == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    nev = 4 if is_mx else 2
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+           for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device()
+                          if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local_rank)
+    clocks.start()
+    barrier()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    assert mx.mx_last_error() == 0
+    ms = t0.elapsed_time(t1)
+    per_kernel = [[e[j].elapsed_time(e[j + 1]) for e in evs]
+                  for j in range(nev - 1)]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    tflops = flops_of(c) * world / (ms_step * 1e-3) / 1e12
+
+    gemm_ms = statistics.mean(per_kernel[-1])
+    gemm_tf = flops_of(c) / (gemm_ms * 1e-3) / 1e12
+    peak = bf16 * NOMINAL_RATIO[c.kind]
+    extra = {"gemm_ms": gemm_ms, "gemm_tflops": gemm_tf,
+             "gemm_frac_of_peak": gemm_tf / peak}
+    if is_mx:
+        qa_ms = statistics.mean(per_kernel[0])
+        qb_ms = statistics.mean(per_kernel[1])
+        extra["quantize_a_ms"] = qa_ms
+        extra["quantize_b_ms"] = qb_ms
+        extra["quantize_a_gbs"] = quant_bytes(fmt, c.M, c.K) / qa_ms / 1e6
+        extra["quantize_b_gbs"] = quant_bytes(fmt, c.N, c.K) / qb_ms / 1e6
+        extra["quantize_a_frac_hbm"] = extra["quantize_a_gbs"] / hbm
+        extra["quantize_b_frac_hbm"] = extra["quantize_b_gbs"] / hbm
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hA = A.pin_memory()
+        hB = B.pin_memory()
+        hC = torch.empty((c.M, c.N), dtype=out_dt).pin_memory()
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            step()
+            hC.copy_(C, non_blocking=True)
+
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, args.e2e_steps)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": flops_of(c) * world / (ems * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
+                                         hB.numel() * hB.element_size()),
+               "d2h_bytes_per_step": int(hC.numel() * hC.element_size())}
+
+    roofline = {"bound": "tensor", "kernel": "mx_gemm" if is_mx else "gemm_f16",
+                "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
+                "frac": gemm_tf / peak, "traffic": None,
+                "peak_source": "%s bf16 burst x nominal %s/bf16 ratio %g" %
+                (peak_src, c.kind, NOMINAL_RATIO[c.kind])}
+    line = {
+        "metric": "%s GEMM TFLOP/s (quantize A + quantize B + GEMM per step)"
+                  % c.kind if is_mx else "%s GEMM TFLOP/s" % c.kind,
+        "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"mxfp8": "e4m3", "mxfp4": "e2m1"}.get(c.kind, c.kind),
+        "data": "synthetic (seeded)",
+        "config": {"workload": c.name, "M": c.M, "N": c.N, "K": c.K,
+                   "out": c.out, "dist": c.dist_a,
+                   "l2": "inputs larger than L2 (fp32 sources %d MB each)"
+                         % (4 * c.M * c.K // 2 ** 20) if is_mx else
+                         "operands %d MB + %d MB; no flush" %
+                         (2 * c.M * c.K // 2 ** 20, 2 * c.K * c.N // 2 ** 20),
+                   "parallelism": "replicas%d" % world},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roofline,
+        "breakdown": extra,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    return line
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_sample(c, budget_s: float):
+    """Rows of C from the fp32 sources with the CPU oracle, until the time
+    budget is spent: quantize the whole B once, then quantize and multiply
+    A rows in chunks.  Returns (flops done, seconds, rows, threads)."""
+    import oracle
+    A, B = workloads.sources(c)
+    t0 = time.perf_counter()
+    if c.kind in ("f16", "bf16"):
+        bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa
+        Ab, Bb = bits(A), bits(B)
+        code = oracle.F16 if c.kind == "f16" else oracle.BF16
+        rows = 0
+        chunk = 8
+        while rows < c.M:
+            r = list(range(rows, min(c.M, rows + chunk)))
+            oracle.gemm_f16(Ab, Bb, code, rows=r)
+            rows += len(r)
+            if time.perf_counter() - t0 > budget_s:
+                break
+    else:
+        fmt = oracle.E4M3 if c.kind == "mxfp8" else oracle.E2M1
+        cb, sb = oracle.quantize(B.numpy(), fmt, k_axis=0)
+        An = A.numpy()
+        rows = 0
+        chunk = 16
+        while rows < c.M:
+            ca, sa = oracle.quantize(An[rows:rows + chunk], fmt, k_axis=1)
+            oracle.gemm_mx(ca, sa, cb, sb, fmt)
+            rows += ca.shape[0]
+            if time.perf_counter() - t0 > budget_s:
+                break
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * c.N * c.K, dt, rows, oracle.num_threads()
+
+
+def run_reference(args):
+    c = workloads.case(args.workload)
+    budget = max(1.0, args.ref_budget / max(1, args.steps))
+    vals = []
+    last = None
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(c, min(budget, 2.0))
+    for _ in range(args.steps):
+        fl, dt, rows, thr = oracle_sample(c, budget)
+        vals.append(fl / dt / 1e12)
+        last = (rows, thr, dt)
+    v = statistics.median(vals)
+    rows, thr, dt = last
+    sample = ("rows of C computed from the fp32 sources: quantize all of B, "
+              "then %d rows of A quantized and multiplied (%.1f s per step)"
+              % (rows, dt)) if c.kind in ("mxfp8", "mxfp4") else \
+        ("%d rows of C (%.1f s per step)" % (rows, dt))
+    return {
+        "impl": "reference",
+        "metric": "%s GEMM TFLOP/s" % c.kind, "value": v, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": c.name, "M": c.M, "N": c.N, "K": c.K,
+                   "out": c.out},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": thr,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mxfp8_8192")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline key")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="total seconds of oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(
+            "nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        c = workloads.case(args.workload)
+        fl, dt, rows, thr = oracle_sample(c, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr,
+            "kind": "oracle",
+            "sample": "%d rows of C from the fp32 sources (all of B "
+                      "quantized), %.1f s" % (rows, dt)}
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

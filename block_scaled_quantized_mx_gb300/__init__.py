@@ -1,0 +1,218 @@
+"""Python binding of libmx_gb300.so (the C ABI in include/mx.h).
+
+Argument marshalling only: every step of quantization and matrix multiply runs
+in the library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  There is no fallback: if the shared library is missing or fails to
+load, every call raises.
+
+    from block_scaled_quantized_mx_gb300 import mx_quantize, mx_gemm, gemm_f16
+    a = mx_quantize(A_fp32, E4M3)                      # A: M x K, K contiguous
+    b = mx_quantize(B_fp32, E4M3, k_strided=True)      # B: K x N row-major
+    C = mx_gemm(a, b, out_dtype=torch.bfloat16)        # C = A @ B
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+E4M3 = 1
+E2M1 = 2
+DT_F32, DT_BF16, DT_F16 = 0, 1, 2
+SRC_K_CONTIGUOUS, SRC_K_STRIDED = 0, 1
+
+STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
+          3: "MX_ERR_ALIGN", 4: "MX_ERR_UNSUPPORTED", 5: "MX_ERR_CUDA",
+          6: "MX_ERR_TIMEOUT"}
+
+EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
+           "gemm_f16", "mx_last_error", "mx_selftest_wait_timeout",
+           "mx_scales_to_rowmajor", "mx_status_string", "mx_version")
+
+
+class MXError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed: %s" % (what, STATUS.get(status, status)))
+        self.status = status
+
+
+class CMXTensor(ctypes.Structure):
+    """Mirror of struct mx_tensor."""
+    _fields_ = [("data", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("fmt", ctypes.c_int32), ("outer", ctypes.c_int64),
+                ("K", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA sources for sm_103a into the in-tree shared library."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB_PATH):
+        raise RuntimeError("%s is not built: call "
+                           "block_scaled_quantized_mx_gb300.build() first"
+                           % _build.LIB_PATH)
+    L = ctypes.CDLL(_build.LIB_PATH)
+    i32, i64, p, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, \
+        ctypes.c_size_t
+    pt = ctypes.POINTER(CMXTensor)
+    L.mx_data_bytes.restype = sz
+    L.mx_data_bytes.argtypes = [i32, i64, i64]
+    L.mx_scale_bytes.restype = sz
+    L.mx_scale_bytes.argtypes = [i64, i64]
+    L.mx_quantize.restype = i32
+    L.mx_quantize.argtypes = [p, i64, i32, pt, p]
+    L.mx_gemm.restype = i32
+    L.mx_gemm.argtypes = [pt, pt, p, i32, i64, p]
+    L.gemm_f16.restype = i32
+    L.gemm_f16.argtypes = [p, p, p, i32, i64, i64, i64, i64, i64, i64, p]
+    L.mx_last_error.restype = i32
+    L.mx_last_error.argtypes = [p]
+    L.mx_selftest_wait_timeout.restype = i32
+    L.mx_selftest_wait_timeout.argtypes = [i64, p]
+    L.mx_scales_to_rowmajor.restype = i32
+    L.mx_scales_to_rowmajor.argtypes = [p, p, i64, i64]
+    L.mx_status_string.restype = ctypes.c_char_p
+    L.mx_status_string.argtypes = [i32]
+    L.mx_version.restype = i32
+    L.mx_version.argtypes = []
+    _lib = L
+    return L
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MXError(status, what)
+
+
+@dataclass
+class MXTensor:
+    """An MX tensor: data plane and scale plane (device uint8 tensors) of an
+    outer x K matrix, K being the contraction axis."""
+    data: torch.Tensor
+    scales: torch.Tensor
+    fmt: int
+    outer: int
+    K: int
+
+    def c(self) -> CMXTensor:
+        return CMXTensor(self.data.data_ptr() if self.data.numel() else None,
+                         self.scales.data_ptr() if self.scales.numel() else None,
+                         self.fmt, self.outer, self.K)
+
+
+def data_bytes(fmt: int, outer: int, K: int) -> int:
+    return int(lib().mx_data_bytes(fmt, outer, K))
+
+
+def scale_bytes(outer: int, K: int) -> int:
+    return int(lib().mx_scale_bytes(outer, K))
+
+
+def empty_mx(fmt: int, outer: int, K: int, device="cuda") -> MXTensor:
+    nd = data_bytes(fmt, outer, K)
+    ns = scale_bytes(outer, K)
+    return MXTensor(torch.empty(nd, dtype=torch.uint8, device=device),
+                    torch.empty(ns, dtype=torch.uint8, device=device),
+                    fmt, outer, K)
+
+
+def mx_quantize(src: torch.Tensor, fmt: int, k_strided: bool = False,
+                out: MXTensor | None = None, stream=None) -> MXTensor:
+    """Quantize a 2-D fp32 CUDA tensor.  ``k_strided=False``: src is
+    outer x K; ``k_strided=True``: src is K x outer (e.g. a row-major K x N
+    B operand).  The row stride may exceed the width."""
+    if src.dtype != torch.float32 or src.dim() != 2 or not src.is_cuda:
+        raise ValueError("src must be a 2-D float32 CUDA tensor")
+    if src.stride(1) != 1:
+        raise ValueError("src must have a unit inner stride")
+    if k_strided:
+        K, outer = src.shape
+    else:
+        outer, K = src.shape
+    if out is None:
+        out = empty_mx(fmt, outer, K, src.device)
+    ct = out.c()
+    _check(lib().mx_quantize(src.data_ptr(), src.stride(0),
+                             SRC_K_STRIDED if k_strided else SRC_K_CONTIGUOUS,
+                             ctypes.byref(ct), _stream(stream)), "mx_quantize")
+    return out
+
+
+def mx_gemm(A: MXTensor, B: MXTensor, out_dtype=torch.bfloat16,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C = A * B for MX tensors A (M x K) and B (quantized from K x N)."""
+    dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    if out is None:
+        out = torch.empty((A.outer, B.outer), dtype=out_dtype,
+                          device=A.data.device)
+    ca, cb = A.c(), B.c()
+    _check(lib().mx_gemm(ctypes.byref(ca), ctypes.byref(cb),
+                         out.data_ptr() if out.numel() else None, dt,
+                         out.stride(0) if out.dim() == 2 else B.outer,
+                         _stream(stream)), "mx_gemm")
+    return out
+
+
+def gemm_f16(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """C (fp32) = A * B for row-major fp16 or bf16 CUDA tensors."""
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("A and B must both be fp16 or both bf16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    dt = DT_F16 if A.dtype == torch.float16 else DT_BF16
+    _check(lib().gemm_f16(A.data_ptr() if A.numel() else None,
+                          B.data_ptr() if B.numel() else None,
+                          out.data_ptr() if out.numel() else None, dt, M, N, K,
+                          A.stride(0), B.stride(0), out.stride(0),
+                          _stream(stream)), "gemm_f16")
+    return out
+
+
+def mx_last_error(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the library's device
+    status (0 = MX_OK, 6 = MX_ERR_TIMEOUT)."""
+    return int(lib().mx_last_error(_stream(stream)))
+
+
+def mx_selftest_wait_timeout(limit_cycles: int, stream=None) -> int:
+    return int(lib().mx_selftest_wait_timeout(limit_cycles, _stream(stream)))
+
+
+def scales_to_rowmajor(tiled, outer: int, K: int):
+    """Host helper: tiled scale plane (numpy uint8) -> outer x K/32 array."""
+    import numpy as np
+    t = np.ascontiguousarray(tiled, dtype=np.uint8)
+    out = np.empty((outer, K // 32), dtype=np.uint8)
+    _check(lib().mx_scales_to_rowmajor(t.ctypes.data, out.ctypes.data, outer,
+                                       K), "mx_scales_to_rowmajor")
+    return out

@@ -1,0 +1,173 @@
+// api.cu -- the C ABI of include/mx.h: argument, shape and alignment checks
+// on the host, then one asynchronous launch on the caller's stream.
+//
+// The pages' interface (WWDC26 session 330, 3:53 / 4:48 listings): a quantized
+// tensor is one object carrying a data plane and a scale plane, and creating
+// one reports failure through a status rather than by crashing; the matmul
+// takes two such tensors and a plain output with no transposes.  Here that is
+// the mx_tensor struct plus mx_status codes.
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/mx.h"
+#include "common.cuh"
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The library ships sm_103a code only: require compute capability 10.3.
+mx_status check_device() {
+  static int ok_cache[64] = {};   // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
+  if (dev < 64 && ok_cache[dev]) return ok_cache[dev] == 1 ? MX_OK : MX_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MX_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev < 64) ok_cache[dev] = ok ? 1 : 2;
+  return ok ? MX_OK : MX_ERR_UNSUPPORTED;
+}
+
+mx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+mx_status check_tensor(const mx_tensor* t) {
+  if (!t) return MX_ERR_INVALID_ARG;
+  if (t->fmt != MX_FMT_E4M3 && t->fmt != MX_FMT_E2M1) return MX_ERR_INVALID_ARG;
+  if (t->outer < 0 || t->K < 0 || t->outer > kMaxDim || t->K > kMaxDim) return MX_ERR_SHAPE;
+  if (t->K % 32) return MX_ERR_SHAPE;
+  if (t->outer > 0 && t->K > 0) {
+    if (!t->data || !t->scales) return MX_ERR_INVALID_ARG;
+    if (!aligned16(t->data) || !aligned16(t->scales)) return MX_ERR_ALIGN;
+  }
+  return MX_OK;
+}
+
+}  // namespace
+
+#pragma GCC visibility push(default)
+extern "C" {
+
+size_t mx_data_bytes(int32_t fmt, int64_t outer, int64_t K) {
+  if (outer < 0 || K < 0 || K % 32) return 0;
+  if (fmt == MX_FMT_E4M3) return static_cast<size_t>(outer) * static_cast<size_t>(K);
+  if (fmt == MX_FMT_E2M1) return static_cast<size_t>(outer) * static_cast<size_t>(K) / 2;
+  return 0;
+}
+
+size_t mx_scale_bytes(int64_t outer, int64_t K) {
+  if (outer < 0 || K < 0 || K % 32) return 0;
+  return static_cast<size_t>(mxk::sf_row_atoms(outer)) *
+         static_cast<size_t>(mxk::sf_k_atoms(K)) * mxk::SF_ATOM_BYTES;
+}
+
+mx_status mx_quantize(const float* src, int64_t ld, int32_t src_layout, const mx_tensor* out,
+                      void* stream) {
+  mx_status s = check_tensor(out);
+  if (s != MX_OK) return s;
+  if (src_layout != MX_SRC_K_CONTIGUOUS && src_layout != MX_SRC_K_STRIDED)
+    return MX_ERR_INVALID_ARG;
+  if (out->outer == 0 || out->K == 0) return MX_OK;
+  if (!src) return MX_ERR_INVALID_ARG;
+  const int64_t inner = (src_layout == MX_SRC_K_CONTIGUOUS) ? out->K : out->outer;
+  if (ld < inner || ld % 4) return MX_ERR_SHAPE;
+  if (!aligned16(src)) return MX_ERR_ALIGN;
+  // grid limits: 65535 CTAs along the second grid dimension
+  const int64_t ra = mxk::sf_row_atoms(out->outer), ka = mxk::sf_k_atoms(out->K);
+  if ((src_layout == MX_SRC_K_CONTIGUOUS ? ra : ka) > 65535) return MX_ERR_SHAPE;
+  if ((s = check_device()) != MX_OK) return s;
+  return from_cuda(mxk::launch_quantize(src, ld, src_layout == MX_SRC_K_STRIDED, out->fmt,
+                                        out->outer, out->K, out->data, out->scales,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dtype,
+                  int64_t ldc, void* stream) {
+  mx_status s;
+  if ((s = check_tensor(A)) != MX_OK) return s;
+  if ((s = check_tensor(B)) != MX_OK) return s;
+  if (A->fmt != B->fmt || A->K != B->K) return MX_ERR_SHAPE;
+  if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  const int64_t M = A->outer, N = B->outer, K = A->K;
+  if (M == 0 || N == 0) return MX_OK;
+  if (!C) return MX_ERR_INVALID_ARG;
+  const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
+  if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
+  if (!aligned16(C)) return MX_ERR_ALIGN;
+  if ((s = check_device()) != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_mx(A->fmt, A->data, A->scales, B->data, B->scales, C,
+                                       c_dtype, ldc, M, N, K,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,
+                   int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                   void* stream) {
+  if (ab_dtype != MX_DT_F16 && ab_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MX_ERR_SHAPE;
+  if (M == 0 || N == 0) return MX_OK;
+  if (!C) return MX_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 4) return MX_ERR_SHAPE;
+  if (!aligned16(C)) return MX_ERR_ALIGN;
+  if (K > 0) {
+    if (!A || !B) return MX_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || lda % 8 || ldb % 8) return MX_ERR_SHAPE;
+    if (!aligned16(A) || !aligned16(B)) return MX_ERR_ALIGN;
+  }
+  mx_status s = check_device();
+  if (s != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_last_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MX_ERR_CUDA;
+  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
+  const unsigned a = mxk::fetch_and_clear_status_quantize(&e1);
+  const unsigned b = mxk::fetch_and_clear_status_gemm(&e2);
+  if (e1 != cudaSuccess || e2 != cudaSuccess) return MX_ERR_CUDA;
+  if ((a | b) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
+  return MX_OK;
+}
+
+mx_status mx_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t{1} << 40)) return MX_ERR_INVALID_ARG;
+  mx_status s = check_device();
+  if (s != MX_OK) return s;
+  return from_cuda(
+      mxk::launch_selftest_timeout(limit_cycles, static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_scales_to_rowmajor(const uint8_t* tiled, uint8_t* rowmajor, int64_t outer,
+                                int64_t K) {
+  if (outer < 0 || K < 0 || K % 32) return MX_ERR_SHAPE;
+  if ((outer > 0 && K > 0) && (!tiled || !rowmajor)) return MX_ERR_INVALID_ARG;
+  const int64_t nb = K / 32, ka = mxk::sf_k_atoms(K);
+  for (int64_t r = 0; r < outer; ++r)
+    for (int64_t j = 0; j < nb; ++j) rowmajor[r * nb + j] = tiled[mxk::sf_offset(r, j, ka)];
+  return MX_OK;
+}
+
+const char* mx_status_string(int32_t status) {
+  switch (status) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+    case MX_ERR_SHAPE: return "MX_ERR_SHAPE";
+    case MX_ERR_ALIGN: return "MX_ERR_ALIGN";
+    case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+    default: return "MX_ERR_UNKNOWN";
+  }
+}
+
+int32_t mx_version(void) { return 100; }
+
+}  // extern "C"
+#pragma GCC visibility pop

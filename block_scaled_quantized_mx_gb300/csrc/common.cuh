@@ -1,0 +1,67 @@
+// common.cuh -- definitions shared by the library's kernels and host code:
+// the scale-plane layout (one definition, used by the quantizer that writes it
+// and by the GEMM loaders that read it), format codes and launch entry points.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mxk {
+
+enum Format : int { FMT_E4M3 = 1, FMT_E2M1 = 2 };
+enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+
+// Status word bits recorded by kernels (the host maps any non-zero word to
+// MX_ERR_TIMEOUT; the low byte says which wait gave up).
+constexpr unsigned STATUS_TIMEOUT = 0x100u;
+
+// ---------------------------------------------------------------- scale plane
+// Scales are grouped in atoms of 128 rows x 4 blocks (128 K elements): 512
+// contiguous bytes, the byte of (row r, block j) at 16*(r%32) + 4*((r/32)%4)
+// + j%4.  This is the arrangement in which one 32-lane x 16-byte tensor-memory
+// copy, replicated to the four lane quarters, hands each accumulator row its
+// four scales.  Atoms are ordered K-chunk fastest.
+constexpr int SF_ATOM_ROWS = 128;
+constexpr int SF_ATOM_BLOCKS = 4;
+constexpr int SF_ATOM_BYTES = 512;
+
+__host__ __device__ __forceinline__ int64_t sf_k_atoms(int64_t K) {
+  return (K + 127) / 128;
+}
+__host__ __device__ __forceinline__ int64_t sf_row_atoms(int64_t outer) {
+  return (outer + 127) / 128;
+}
+__host__ __device__ __forceinline__ int sf_in_atom(int r, int j) {
+  return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t j,
+                                                      int64_t k_atoms) {
+  return ((r >> 7) * k_atoms + (j >> 2)) * SF_ATOM_BYTES +
+         sf_in_atom(static_cast<int>(r & 127), static_cast<int>(j & 3));
+}
+
+// ---------------------------------------------------------------- launches
+cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt,
+                            int64_t outer, int64_t K, void* data, uint8_t* scales,
+                            cudaStream_t st);
+
+// mx GEMM: A data outer=M, B data outer=N, both K-major; C row-major.
+cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
+                           const void* b_data, const uint8_t* b_sf, void* C,
+                           int c_dtype, int64_t ldc, int64_t M, int64_t N,
+                           int64_t K, cudaStream_t st);
+
+cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
+                            int64_t M, int64_t N, int64_t K, int64_t lda,
+                            int64_t ldb, int64_t ldc, cudaStream_t st);
+
+cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc,
+                             int elem_bytes, cudaStream_t st);
+
+cudaError_t launch_selftest_timeout(long long limit_cycles, cudaStream_t st);
+
+// Read and clear the device status word of each translation unit.
+unsigned fetch_and_clear_status_quantize(cudaError_t* err);
+unsigned fetch_and_clear_status_gemm(cudaError_t* err);
+
+}  // namespace mxk

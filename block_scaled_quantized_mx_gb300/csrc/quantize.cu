@@ -1,0 +1,324 @@
+// quantize.cu -- OCP MX quantization, fp32 -> E4M3 / E2M1 data plane plus
+// UE8M0 scale plane in the tensor-core scale-factor layout.
+//
+// The rule (OCP Microscaling v1.0 conversion; block of 32 along the
+// innermost / K axis as in the WWDC26 session 330 "Multi-plane tensors"
+// chapter and its 4:48 listing, block factors {32, 1}):
+//   amax = max |x| over the 32 values of the block
+//   e    = floor(log2 amax), read off the fp32 exponent field (for a subnormal
+//          amax, from the position of its leading one) -- never via a log
+//          function, which can round up just below a power of two
+//   X    = 2^clamp(e - emax, -127, 127), emax = 8 (E4M3) / 2 (E2M1)
+//   code = e_s + 127 (UE8M0); all-zero block -> 0; NaN/Inf in block -> 0xFF
+//   q_i  = RNE-saturate(x_i / X) to the element format.
+// x / X is a multiplication by a power of two in fp32; it is exact except when
+// the product is an fp32 subnormal, which both formats round to +-0 anyway.
+//
+// Both kernels are HBM-streaming passes: each CTA owns one 128-row x 128-K
+// region, i.e. exactly one 512-byte scale atom, which it assembles in shared
+// memory and writes out as one coalesced 512-byte store.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mxk {
+
+namespace {
+
+__device__ unsigned int g_status_quantize = 0;
+
+constexpr int QT_THREADS = 256;   // 8 warps per CTA
+
+__device__ __forceinline__ uint32_t abs_bits(float x) {
+  return __float_as_uint(x) & 0x7FFFFFFFu;
+}
+
+// Scale code and the multiplier 1/X for a block whose largest |x| has the bit
+// pattern amax (sign cleared).  emax: 8 for E4M3, 2 for E2M1.
+__device__ __forceinline__ void block_scale(uint32_t amax, int emax,
+                                            uint32_t& code, float& inv_x) {
+  if (amax >= 0x7F800000u) {          // Inf or NaN somewhere in the block
+    code = 0xFFu;
+    inv_x = 1.0f;
+    return;
+  }
+  int es;
+  if (amax == 0u) {
+    es = -127;
+  } else {
+    const int E = static_cast<int>(amax >> 23);
+    const int e = E ? (E - 127) : ((31 - __clz(static_cast<int>(amax))) - 149);
+    es = e - emax;
+    es = es < -127 ? -127 : (es > 127 ? 127 : es);
+  }
+  code = static_cast<uint32_t>(es + 127);
+  // 2^-es as an fp32: biased exponent 127 - es lies in [2, 254] because
+  // e <= 127 bounds es above by 119 (E4M3) / 125 (E2M1).
+  inv_x = __uint_as_float(static_cast<uint32_t>(127 - es) << 23);
+}
+
+// ---------------------------------------------------------------------------
+// Source outer x K, K contiguous.  CTA = (K chunk kc, row group rg); each warp
+// owns 16 rows; for one row a warp reads the chunk's 128 floats as 32 float4,
+// lane l covering k = 4l..4l+3 of block l/8.  The block amax is a max over 8
+// lanes (shuffles), the 4 codes of a lane are one 32-bit (E4M3) or 16-bit
+// (E2M1) store, so a warp stores 128 (64) contiguous bytes per row.
+template <int FMT>
+__global__ void __launch_bounds__(QT_THREADS)
+quantize_kcontig(const float* __restrict__ src, int64_t ld, int64_t outer,
+                 int64_t K, uint8_t* __restrict__ data, uint8_t* __restrict__ sf) {
+  constexpr int EMAX = (FMT == FMT_E4M3) ? 8 : 2;
+  constexpr int ROWS_PER_WARP = 16;
+  constexpr int BATCH = 8;
+  __shared__ __align__(16) uint8_t atom[SF_ATOM_BYTES];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t kc = blockIdx.x;
+  const int64_t rg = blockIdx.y;
+  const int64_t k_atoms = sf_k_atoms(K);
+
+  for (int i = threadIdx.x; i < SF_ATOM_BYTES / 16; i += QT_THREADS)
+    reinterpret_cast<uint4*>(atom)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  const int64_t k = kc * 128 + 4 * lane;
+  const bool kvalid = (kc * 128 + 32 * (lane >> 3)) < K;   // K % 32 == 0
+  const int j = lane >> 3;
+
+#pragma unroll
+  for (int b0 = 0; b0 < ROWS_PER_WARP; b0 += BATCH) {
+    float4 v[BATCH];
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int64_t r = rg * 128 + warp * ROWS_PER_WARP + b0 + i;
+      if (kvalid && r < outer)
+        v[i] = __ldcs(reinterpret_cast<const float4*>(src + r * ld + k));
+      else
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int rl = warp * ROWS_PER_WARP + b0 + i;     // row inside group
+      const int64_t r = rg * 128 + rl;
+      uint32_t a = max(max(abs_bits(v[i].x), abs_bits(v[i].y)),
+                       max(abs_bits(v[i].z), abs_bits(v[i].w)));
+      a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+      a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+      a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+      uint32_t code;
+      float s;
+      block_scale(a, EMAX, code, s);
+      if (r < outer && kvalid) {
+        if ((lane & 7) == 0) atom[sf_in_atom(rl, j)] = static_cast<uint8_t>(code);
+        if (FMT == FMT_E4M3) {
+          const uint32_t lo = cvt_e4m3x2(v[i].x * s, v[i].y * s);
+          const uint32_t hi = cvt_e4m3x2(v[i].z * s, v[i].w * s);
+          *reinterpret_cast<uint32_t*>(data + r * K + k) = lo | (hi << 16);
+        } else {
+          const uint32_t lo = cvt_e2m1x2(v[i].x * s, v[i].y * s);
+          const uint32_t hi = cvt_e2m1x2(v[i].z * s, v[i].w * s);
+          *reinterpret_cast<uint16_t*>(data + (r * K + k) / 2) =
+              static_cast<uint16_t>(lo | (hi << 8));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < SF_ATOM_BYTES / 16) {
+    uint4* dst = reinterpret_cast<uint4*>(sf + (rg * k_atoms + kc) * SF_ATOM_BYTES);
+    dst[threadIdx.x] = reinterpret_cast<const uint4*>(atom)[threadIdx.x];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Source K x outer, outer contiguous (a row-major K x N operand); output is
+// outer x K (K-major).  CTA = (row group rg of outer, K chunk kc): the
+// 128 (K) x 128 (outer) fp32 tile is staged in shared memory with coalesced
+// float4 row loads, then each thread takes whole blocks (one output row n,
+// one block j of 32 K values) by reading a column of the tile -- consecutive
+// lanes read consecutive n, so the column reads are free of bank conflicts.
+template <int FMT>
+__global__ void __launch_bounds__(QT_THREADS)
+quantize_kstrided(const float* __restrict__ src, int64_t ld, int64_t outer,
+                  int64_t K, uint8_t* __restrict__ data, uint8_t* __restrict__ sf) {
+  constexpr int EMAX = (FMT == FMT_E4M3) ? 8 : 2;
+  extern __shared__ __align__(16) float tile[];   // [128][128] + atom
+  uint8_t* atom = reinterpret_cast<uint8_t*>(tile + 128 * 128);
+
+  const int64_t rg = blockIdx.x;     // group of 128 output rows (outer)
+  const int64_t kc = blockIdx.y;     // chunk of 128 K
+  const int64_t k_atoms = sf_k_atoms(K);
+  const int tid = threadIdx.x;
+
+  for (int i = tid; i < SF_ATOM_BYTES / 16; i += QT_THREADS)
+    reinterpret_cast<uint4*>(atom)[i] = make_uint4(0, 0, 0, 0);
+
+  // stage: tile[kk][nn] = src[(kc*128 + kk) * ld + rg*128 + nn]
+  {
+    const int c4 = tid & 31;                   // float4 column
+    const int64_t n = rg * 128 + 4 * c4;
+#pragma unroll 4
+    for (int kk = tid >> 5; kk < 128; kk += QT_THREADS / 32) {
+      const int64_t kg = kc * 128 + kk;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kg < K) {
+        const float* p = src + kg * ld + n;
+        if (n + 3 < outer) {
+          v = __ldcs(reinterpret_cast<const float4*>(p));
+        } else {
+          if (n + 0 < outer) v.x = __ldcs(p + 0);
+          if (n + 1 < outer) v.y = __ldcs(p + 1);
+          if (n + 2 < outer) v.z = __ldcs(p + 2);
+        }
+      }
+      reinterpret_cast<float4*>(tile + kk * 128)[c4] = v;
+    }
+  }
+  __syncthreads();
+
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int u = tid + QT_THREADS * h;
+    const int nl = u & 127;                    // output row inside the group
+    const int j = u >> 7;                      // block inside the chunk
+    const int64_t n = rg * 128 + nl;
+    const int64_t kb = kc * 128 + 32 * j;      // first K of the block
+    if (n >= outer || kb >= K) continue;
+    float x[32];
+    uint32_t a = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      x[i] = tile[(32 * j + i) * 128 + nl];
+      a = max(a, abs_bits(x[i]));
+    }
+    uint32_t code;
+    float s;
+    block_scale(a, EMAX, code, s);
+    atom[sf_in_atom(nl, j)] = static_cast<uint8_t>(code);
+    if (FMT == FMT_E4M3) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = cvt_e4m3x2(x[4 * i] * s, x[4 * i + 1] * s) |
+               (cvt_e4m3x2(x[4 * i + 2] * s, x[4 * i + 3] * s) << 16);
+      uint4* dst = reinterpret_cast<uint4*>(data + n * K + kb);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float* y = x + 8 * i;
+        w[i] = cvt_e2m1x2(y[0] * s, y[1] * s) | (cvt_e2m1x2(y[2] * s, y[3] * s) << 8) |
+               (cvt_e2m1x2(y[4] * s, y[5] * s) << 16) |
+               (cvt_e2m1x2(y[6] * s, y[7] * s) << 24);
+      }
+      *reinterpret_cast<uint4*>(data + (n * K + kb) / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  __syncthreads();
+  if (tid < SF_ATOM_BYTES / 16) {
+    uint4* dst = reinterpret_cast<uint4*>(sf + (rg * k_atoms + kc) * SF_ATOM_BYTES);
+    dst[tid] = reinterpret_cast<const uint4*>(atom)[tid];
+  }
+}
+
+constexpr int KSTRIDED_SMEM = 128 * 128 * 4 + SF_ATOM_BYTES;
+
+template <int FMT>
+cudaError_t launch_fmt(const float* src, int64_t ld, int k_strided, int64_t outer,
+                       int64_t K, uint8_t* data, uint8_t* sf, cudaStream_t st) {
+  const int64_t ra = sf_row_atoms(outer), ka = sf_k_atoms(K);
+  if (!k_strided) {
+    dim3 grid(static_cast<unsigned>(ka), static_cast<unsigned>(ra));
+    quantize_kcontig<FMT><<<grid, QT_THREADS, 0, st>>>(src, ld, outer, K, data, sf);
+  } else {
+    static bool attr_set[64] = {};   // per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr_set[dev]) {
+      e = cudaFuncSetAttribute(quantize_kstrided<FMT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, KSTRIDED_SMEM);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) attr_set[dev] = true;
+    }
+    dim3 grid(static_cast<unsigned>(ra), static_cast<unsigned>(ka));
+    quantize_kstrided<FMT><<<grid, QT_THREADS, KSTRIDED_SMEM, st>>>(src, ld, outer, K,
+                                                                    data, sf);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt,
+                            int64_t outer, int64_t K, void* data, uint8_t* scales,
+                            cudaStream_t st) {
+  if (outer == 0 || K == 0) return cudaSuccess;
+  uint8_t* d = static_cast<uint8_t*>(data);
+  if (fmt == FMT_E4M3) return launch_fmt<FMT_E4M3>(src, ld, k_strided, outer, K, d, scales, st);
+  return launch_fmt<FMT_E2M1>(src, ld, k_strided, outer, K, d, scales, st);
+}
+
+// ---------------------------------------------------------------------------
+// Small utility kernels that share this translation unit.
+
+namespace {
+
+__global__ void zero_fill_kernel(uint8_t* C, int64_t rows, int64_t row_bytes,
+                                 int64_t ld_bytes) {
+  const int64_t total = rows * row_bytes;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / row_bytes, c = i - r * row_bytes;
+    C[r * ld_bytes + c] = 0;
+  }
+}
+
+// Waits on an mbarrier that nothing arrives at; the bound always runs out.
+__global__ void selftest_timeout_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    bool done = false;
+    while (!done) {
+      done = mbar_try_wait(b, 0);
+      if (clock64() - t0 > limit) break;
+    }
+    if (!done) atomicOr(&g_status_quantize, STATUS_TIMEOUT | 0xEEu);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc,
+                             int elem_bytes, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t total = rows * cols * elem_bytes;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  zero_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<uint8_t*>(C), rows, cols * elem_bytes, ldc * elem_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_timeout(long long limit_cycles, cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(limit_cycles);
+  return cudaGetLastError();
+}
+
+unsigned fetch_and_clear_status_quantize(cudaError_t* err) {
+  unsigned v = 0, z = 0;
+  *err = cudaMemcpyFromSymbol(&v, g_status_quantize, sizeof(v));
+  if (*err == cudaSuccess) *err = cudaMemcpyToSymbol(g_status_quantize, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace mxk

@@ -1,0 +1,194 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) MX block-scaled / FP16 GEMM library
+ * (libmx_gb300.so).
+ *
+ * Three operations, all launched asynchronously on the caller's CUDA stream:
+ *
+ *   mx_quantize  fp32 matrix -> MX tensor (E4M3 or E2M1 data plane plus a
+ *                UE8M0 scale plane, one scale per 32 consecutive K elements)
+ *   mx_gemm      C = A * B on two MX tensors, fp32 accumulation, dequantize
+ *                inside the tensor-core matmul, fp32 or bf16 C
+ *   gemm_f16     C = A * B on row-major fp16 or bf16 matrices, fp32
+ *                accumulation, fp32 C
+ *
+ * Where these come from.  The quantized tensor as one object holding a data
+ * plane and a scale plane, the scale format ("FP8 E8M0") and the block of 32
+ * along the innermost dimension are the WWDC26 session 330 pages ("Metal
+ * tensors ... / Optimize custom ML ops with Metal tensors"), chapters
+ * "Multi-plane tensors" (4:23) and "Quantized matrix multiplication" (5:17),
+ * and the listings at 4:48 (scale plane with block factors {32, 1}) and 7:19
+ * (matmul of two quantized tensors with no transposes, dequantization done
+ * by the matmul).  FP16 matmul with fp32 accumulation is the "Passo 6" step
+ * of the dicastech tutorial "Treinar LLM em Swift: multiplicacao de matrizes
+ * do Gflop/s ao Tflop/s".  The element and scale encodings and the rule
+ * X = 2^(floor(log2 amax) - emax) follow the OCP Microscaling (MX) v1.0
+ * specification.
+ *
+ * Memory.  Every pointer argument except those of mx_scales_to_rowmajor is a
+ * device pointer owned by the caller; the library never allocates, frees or
+ * synchronizes on these calls (mx_last_error is the one call that
+ * synchronizes).  Inputs are only read; outputs are written in full.
+ *
+ * Errors.  Argument, shape and alignment checks run on the host before
+ * anything is launched and return a status without touching the GPU.  A
+ * launch failure returns MX_ERR_CUDA.  Every wait inside a kernel is bounded;
+ * a wait that runs out records MX_ERR_TIMEOUT in a device status word, the
+ * kernel returns cleanly, and mx_last_error reports it.
+ */
+#ifndef MX_GB300_H
+#define MX_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mx_status {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1, /* null pointer, unknown enum value             */
+  MX_ERR_SHAPE = 2,       /* sizes or leading dimensions not supported     */
+  MX_ERR_ALIGN = 3,       /* pointer or stride not 16-byte aligned         */
+  MX_ERR_UNSUPPORTED = 4, /* no device of compute capability 10.3          */
+  MX_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed          */
+  MX_ERR_TIMEOUT = 6      /* a kernel gave up on a bounded wait            */
+} mx_status;
+
+/* Element format of an MX data plane. */
+typedef enum mx_format {
+  MX_FMT_E4M3 = 1, /* MXFP8: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+                      one code per byte; no infinity; max 448            */
+  MX_FMT_E2M1 = 2  /* MXFP4: 1 sign, 2 exponent (bias 1), 1 mantissa bit;
+                      two codes per byte, the element with even k in the
+                      low nibble; max 6                                   */
+} mx_format;
+
+/* Element type of a plain matrix. */
+typedef enum mx_dtype { MX_DT_F32 = 0, MX_DT_BF16 = 1, MX_DT_F16 = 2 } mx_dtype;
+
+/* Orientation of mx_quantize's fp32 source. */
+typedef enum mx_src_layout {
+  MX_SRC_K_CONTIGUOUS = 0, /* source is outer x K row-major (the A operand)   */
+  MX_SRC_K_STRIDED = 1     /* source is K x outer row-major (a row-major K x N
+                              B operand); blocks of 32 still run along K     */
+} mx_src_layout;
+
+/*
+ * An MX tensor: the quantized form of an outer x K matrix whose K axis is the
+ * contraction axis (A: outer = M; B: outer = N).
+ *
+ *   data    device, outer x K codes, K contiguous, rows packed back to back:
+ *           mx_data_bytes(fmt, outer, K) bytes; 16-byte aligned.
+ *   scales  device, UE8M0 codes (value 2^(c-127), 0xFF = NaN) in the
+ *           tensor-core scale-factor layout: the scale matrix, padded to a
+ *           multiple of 128 rows and of 4 blocks, is cut into atoms of 128 rows
+ *           x 4 blocks (128 K elements) of 512 contiguous bytes; the scale of
+ *           (row r, block j) is byte 16*(r%32) + 4*((r%128)/32) + (j%4) of atom
+ *           (r/128) * ceil(K/128) + j/4.  mx_scale_bytes(outer, K) bytes;
+ *           16-byte aligned.  Padding bytes must not be 0xFF (mx_quantize
+ *           writes 0 there).
+ *   fmt     mx_format
+ *   outer   rows (M for A, N for B), >= 0
+ *   K       contraction length, a multiple of 32, >= 0
+ */
+typedef struct mx_tensor {
+  void* data;
+  uint8_t* scales;
+  int32_t fmt;
+  int64_t outer;
+  int64_t K;
+} mx_tensor;
+
+/* Bytes of the data plane: outer*K (E4M3) or outer*K/2 (E2M1); 0 on bad
+ * arguments. */
+size_t mx_data_bytes(int32_t fmt, int64_t outer, int64_t K);
+
+/* Bytes of the scale plane: ceil(outer/128) * ceil(K/128) * 512; 0 on bad
+ * arguments. */
+size_t mx_scale_bytes(int64_t outer, int64_t K);
+
+/*
+ * mx_quantize -- OCP MX quantization of an fp32 matrix into out (the planes
+ * must already be allocated by the caller at the sizes above).
+ *
+ * For every row r of out and every block j of 32 consecutive K elements:
+ *   amax = max |x| over the block; e = floor(log2(amax)) from the fp32
+ *   exponent; X = 2^clamp(e - emax, -127, 127) with emax = 8 (E4M3) or 2
+ *   (E2M1); the scale code is log2(X) + 127; each element is x / X rounded
+ *   to nearest-even and saturated to the format's largest finite value.
+ *   An all-zero block gets scale code 0; a block holding a NaN or an
+ *   infinity gets scale code 0xFF (its element codes are then unspecified).
+ *
+ *   src         device fp32; element (r, k) at src[r*ld + k]
+ *               (MX_SRC_K_CONTIGUOUS) or src[k*ld + r] (MX_SRC_K_STRIDED)
+ *   ld          leading dimension in elements; ld >= K (K_CONTIGUOUS) or
+ *               ld >= outer (K_STRIDED); a multiple of 4
+ *   src_layout  mx_src_layout
+ *   out         fmt, outer, K, data and scales as described above
+ *   stream      cudaStream_t (NULL: the legacy default stream)
+ * Returns MX_OK, or an error status before any launch.
+ */
+mx_status mx_quantize(const float* src, int64_t ld, int32_t src_layout,
+                      const mx_tensor* out, void* stream);
+
+/*
+ * mx_gemm -- C = A * B^T over the MX tensors A (M x K) and B (N x K), i.e. the
+ * product of the M x K matrix A and the K x N matrix that B was quantized
+ * from, with fp32 accumulation:
+ *   C[i][j] = sum_k (a_ik * Xa_i,k/32) * (b_jk * Xb_j,k/32).
+ *
+ *   A, B     MX tensors of the same fmt and K (A->outer = M, B->outer = N)
+ *   C        device, M x N row-major, element type c_dtype (MX_DT_F32 or
+ *            MX_DT_BF16, rounded to nearest-even); 16-byte aligned
+ *   ldc      leading dimension of C in elements, >= N; ldc * element size
+ *            a multiple of 16 bytes
+ *   stream   cudaStream_t
+ * M, N >= 0 and K >= 0 (K a multiple of 32).  K = 0 writes C = 0.
+ */
+mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C,
+                  int32_t c_dtype, int64_t ldc, void* stream);
+
+/*
+ * gemm_f16 -- C = A * B with A (M x K) and B (K x N) row-major fp16 or bf16,
+ * fp32 accumulation, fp32 C (M x N row-major).
+ *
+ *   ab_dtype  MX_DT_F16 or MX_DT_BF16 (both operands)
+ *   lda, ldb  leading dimensions in elements (lda >= K, ldb >= N), multiples
+ *             of 8; A and B 16-byte aligned
+ *   ldc       >= N, a multiple of 4; C 16-byte aligned
+ * K = 0 writes C = 0.
+ */
+mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype,
+                   int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                   int64_t ldc, void* stream);
+
+/* Synchronize the stream, then return (and clear) the first error recorded
+ * by a kernel of this library on the current device: MX_OK,
+ * MX_ERR_TIMEOUT, or MX_ERR_CUDA if the synchronization itself failed. */
+mx_status mx_last_error(void* stream);
+
+/* Failure-detection self test: launch one small kernel that waits, with a
+ * bound of limit_cycles SM clock cycles (1 .. 2^40), on an mbarrier that
+ * nothing ever arrives at.  The wait runs out, the kernel records
+ * MX_ERR_TIMEOUT in the status word and returns; the context stays usable.
+ * A following mx_last_error(stream) returns MX_ERR_TIMEOUT. */
+mx_status mx_selftest_wait_timeout(int64_t limit_cycles, void* stream);
+
+/* Host-only helper: convert a tiled scale plane (host memory,
+ * mx_scale_bytes(outer, K) bytes) into the row-major outer x K/32 scale
+ * matrix (host memory).  Not used on the GPU path. */
+mx_status mx_scales_to_rowmajor(const uint8_t* tiled, uint8_t* rowmajor,
+                                int64_t outer, int64_t K);
+
+/* Name of a status code (static string). */
+const char* mx_status_string(int32_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t mx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_GB300_H */

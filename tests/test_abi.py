@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/mx.h declares, rejects bad arguments on the host before any launch,
+and its host-side helpers agree with the oracle's independent restatement of
+the memory layouts."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_scaled_quantized_mx_gb300 as mx
+from oracle import layout
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mx.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    mx.build()
+    return mx.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:[\w\s\*]+?)\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_exports_every_declared_function(L):
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(mx.EXPORTS)
+
+
+def test_status_strings_and_version(L):
+    for code, name in mx.STATUS.items():
+        assert L.mx_status_string(code).decode() == name
+    assert L.mx_status_string(99).decode() == "MX_ERR_UNKNOWN"
+    assert L.mx_version() >= 100
+
+
+@pytest.mark.parametrize("outer,K", [(0, 0), (1, 32), (128, 128), (300, 160),
+                                     (8192, 8192), (16384, 2048)])
+def test_plane_sizes(L, outer, K):
+    assert mx.data_bytes(mx.E4M3, outer, K) == outer * K
+    assert mx.data_bytes(mx.E2M1, outer, K) == outer * K // 2
+    assert mx.scale_bytes(outer, K) == layout.scale_plane_bytes(outer, K)
+
+
+def test_plane_sizes_reject_bad(L):
+    assert mx.data_bytes(mx.E4M3, 4, 33) == 0
+    assert mx.data_bytes(7, 4, 32) == 0
+    assert mx.scale_bytes(-1, 32) == 0
+
+
+@pytest.mark.parametrize("outer,K", [(128, 128), (200, 96), (1, 32),
+                                     (300, 544)])
+def test_scales_to_rowmajor_matches_oracle_layout(L, outer, K):
+    g = np.random.default_rng(outer * 7 + K)
+    s = g.integers(0, 255, (outer, K // 32)).astype(np.uint8)
+    tiled = layout.tile_scales(s, K)
+    assert np.array_equal(mx.scales_to_rowmajor(tiled, outer, K), s)
+
+
+def _t(fmt=mx.E4M3, outer=128, K=128, data=0x1000, scales=0x2000):
+    return mx.CMXTensor(data, scales, fmt, outer, K)
+
+
+def test_host_validation_without_launch(L):
+    P = 0x10000            # never dereferenced: every call fails its checks
+    byref = ctypes.byref
+    # mx_quantize
+    assert L.mx_quantize(P, 128, 0, None, None) == 1
+    assert L.mx_quantize(P, 128, 0, byref(_t(fmt=3)), None) == 1
+    assert L.mx_quantize(P, 128, 5, byref(_t()), None) == 1
+    assert L.mx_quantize(None, 128, 0, byref(_t()), None) == 1
+    assert L.mx_quantize(P, 128, 0, byref(_t(K=100)), None) == 2
+    assert L.mx_quantize(P, 64, 0, byref(_t()), None) == 2       # ld < K
+    assert L.mx_quantize(P, 130, 0, byref(_t()), None) == 2      # ld % 4
+    assert L.mx_quantize(P + 4, 128, 0, byref(_t()), None) == 3
+    assert L.mx_quantize(P, 128, 0, byref(_t(data=0x1001)), None) == 3
+    assert L.mx_quantize(P, 128, 0, byref(_t(scales=None)), None) == 1
+    assert L.mx_quantize(P, 128, 0, byref(_t(outer=-1)), None) == 2
+    # empty problems are a no-op success, with no launch
+    assert L.mx_quantize(None, 0, 0, byref(_t(outer=0)), None) == 0
+    assert L.mx_quantize(None, 0, 0, byref(_t(K=0, data=None,
+                                                 scales=None)), None) == 0
+    # mx_gemm
+    a, b = _t(), _t(outer=256)
+    assert L.mx_gemm(None, byref(b), P, 1, 256, None) == 1
+    assert L.mx_gemm(byref(a), byref(_t(fmt=2, outer=256)), P, 1, 256,
+                     None) == 2
+    assert L.mx_gemm(byref(a), byref(_t(outer=256, K=256)), P, 1, 256,
+                     None) == 2
+    assert L.mx_gemm(byref(a), byref(b), P, 2, 256, None) == 1   # f16 out
+    assert L.mx_gemm(byref(a), byref(b), None, 1, 256, None) == 1
+    assert L.mx_gemm(byref(a), byref(b), P, 1, 200, None) == 2   # ldc < N
+    assert L.mx_gemm(byref(a), byref(b), P, 1, 260, None) == 2   # ldc*2 % 16
+    assert L.mx_gemm(byref(a), byref(b), P + 8, 1, 256, None) == 3
+    assert L.mx_gemm(byref(_t(outer=0)), byref(b), None, 1, 256, None) == 0
+    # gemm_f16
+    assert L.gemm_f16(P, P, P, 0, 128, 128, 128, 128, 128, 128, None) == 1
+    assert L.gemm_f16(P, P, P, 2, -1, 128, 128, 128, 128, 128, None) == 2
+    assert L.gemm_f16(P, P, P, 2, 128, 128, 128, 100, 128, 128, None) == 2
+    assert L.gemm_f16(P, P, P, 2, 128, 128, 128, 132, 128, 128, None) == 2
+    assert L.gemm_f16(P, P, P, 2, 128, 128, 128, 128, 128, 126, None) == 2
+    assert L.gemm_f16(P + 2, P, P, 2, 128, 128, 128, 128, 128, 128,
+                      None) == 3
+    assert L.gemm_f16(None, P, P, 1, 128, 128, 128, 128, 128, 128,
+                      None) == 1
+    assert L.gemm_f16(None, None, None, 1, 0, 128, 128, 128, 128, 128,
+                      None) == 0
+    # self test bound
+    assert L.mx_selftest_wait_timeout(0, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(mx, "_lib", None)
+    monkeypatch.setattr(mx._build, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        mx.lib()

@@ -1,0 +1,251 @@
+"""mx_gemm and gemm_f16 on the GPU vs the float64 oracle.
+
+Every check fills C with NaN first (a tile the kernel forgot to write shows
+up as a failure), compares element by element within the stated tolerance
+(tests/_parity.py), and covers: exact integer products, the accumulator-width
+probe from the RIGEL summary, GEMM-only parity on random codes (ragged
+M/N/K tails, extreme scales), every workload configuration (full outputs where
+the oracle is fast enough, sampled rows at full size otherwise, in the same
+launch configuration the benchmark times), and run-to-run determinism."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_quantized_mx_gb300 as mx
+import oracle
+import workloads
+from tests._parity import (check_close, f16_bits, fmt_code, nan_like,
+                           planes_from_codes, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    mx.build()
+    mx.lib()
+
+
+def _out_dtype(out):
+    return torch.bfloat16 if out == "bf16" else torch.float32
+
+
+def _mx_run(A32, B32, fmt, out):
+    """quantize A (M x K) and B (K x N) on the GPU, multiply, return C."""
+    a = mx.mx_quantize(A32.cuda(), fmt)
+    b = mx.mx_quantize(B32.cuda(), fmt, k_strided=True)
+    C = nan_like((a.outer, b.outer), _out_dtype(out))
+    mx.mx_gemm(a, b, out_dtype=_out_dtype(out), out=C)
+    assert mx.mx_last_error() == 0
+    return C.float().cpu().numpy()
+
+
+def _mx_ref(A32, B32, fmt, rows=None):
+    ca, sa = oracle.quantize(A32.numpy(), fmt, k_axis=1)
+    cb, sb = oracle.quantize(B32.numpy(), fmt, k_axis=0)
+    return oracle.gemm_mx(ca, sa, cb, sb, fmt, rows=rows)
+
+
+# ---------------------------------------------------------------- exact cases
+
+@pytest.mark.parametrize("fmt,values", [
+    (oracle.E4M3, np.arange(-14, 15)),
+    (oracle.E2M1, np.array([0, 1, 2, 3, 4, 6, -1, -2, -3, -4, -6]))])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_integer_matrices_exact(fmt, values, out):
+    g = np.random.default_rng(17)
+    M, N, K = 256, 384, 512
+    A = torch.from_numpy(g.choice(values, (M, K)).astype(np.float32))
+    B = torch.from_numpy(g.choice(values, (K, N)).astype(np.float32))
+    C = _mx_run(A, B, fmt, out)
+    want = (A.numpy().astype(np.int64) @ B.numpy().astype(np.int64))
+    if out == "f32":
+        assert np.array_equal(C, want.astype(np.float64))
+    else:
+        want_bf = torch.from_numpy(want.astype(np.float64)).to(
+            torch.bfloat16).float().numpy()
+        assert np.array_equal(C, want_bf)
+
+
+def test_identity_b_reproduces_dequantized_a():
+    g = torch.Generator().manual_seed(3)
+    A = torch.randn(256, 256, generator=g)
+    C = _mx_run(A, torch.eye(256), oracle.E4M3, "f32")
+    Cr, S = _mx_ref(A, torch.eye(256), oracle.E4M3)
+    assert np.array_equal(C, Cr)
+
+
+def _golden(name):
+    out = {}
+    for ln in open(os.path.join(GOLDEN, name)):
+        ln = ln.strip()
+        if ln and not ln.startswith("#"):
+            k, v = ln.split()
+            out[k] = float(v)
+    return out
+
+
+def test_hostile_accumulator_mx_and_f16():
+    """One large term and 127 small ones must come out exactly (fp32
+    accumulation); embedded in a 128 x 128 x 128 problem."""
+    gd = _golden("hostile_accumulator.txt")
+    K = 1 + int(gd["small_count"])
+    A = torch.zeros(128, K)
+    A[5, 0] = gd["large"]
+    A[5, 1:] = gd["small"]
+    B = torch.zeros(K, 128)
+    B[:, 7] = 1.0
+    C = _mx_run(A, B, oracle.E4M3, "f32")
+    assert C[5, 7] == gd["expected"]
+    Ch = mx.gemm_f16(A.half().cuda(), B.half().cuda())
+    assert Ch[5, 7].item() == gd["expected"]
+
+
+# ---------------------------------------------------------------- GEMM only
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 256, 256),
+                                   (200, 296, 160), (128, 384, 512),
+                                   (1000, 520, 1056), (129, 136, 32),
+                                   (384, 768, 4096)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_gemm_random_codes(fmt, M, N, K, out):
+    ca, sa = workloads.random_codes((M, K), fmt, seed=M + 7 * K)
+    cb, sb = workloads.random_codes((N, K), fmt, seed=N + 11 * K + 1)
+    a = planes_from_codes(ca, sa, fmt)
+    b = planes_from_codes(cb, sb, fmt)
+    C = nan_like((M, N), _out_dtype(out))
+    mx.mx_gemm(a, b, out_dtype=_out_dtype(out), out=C)
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
+    check_close(C.float().cpu().numpy(), Cr, S, out, f"{fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
+def test_gemm_extreme_scales(fmt):
+    """Scale codes across the whole finite range, per block."""
+    M = N = 256
+    K = 512
+    ca, sa = workloads.random_codes((M, K), fmt, 41, scale_lo=1,
+                                    scale_hi=254)
+    cb, sb = workloads.random_codes((N, K), fmt, 42, scale_lo=60,
+                                    scale_hi=194)
+    a = planes_from_codes(ca, sa, fmt)
+    b = planes_from_codes(cb, sb, fmt)
+    C = mx.mx_gemm(a, b, out_dtype=torch.float32)
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
+    # products whose magnitude is out of fp32 range are skipped
+    ok = (S < 1e37) & (S > 1e-30)
+    Cg = C.cpu().numpy().astype(np.float64)
+    check_close(np.where(ok, Cg, Cr), Cr, S, "f32", "extreme scales")
+
+
+def test_k_zero_writes_zero():
+    a = mx.empty_mx(oracle.E4M3, 128, 0)
+    b = mx.empty_mx(oracle.E4M3, 256, 0)
+    C = nan_like((128, 256), torch.float32)
+    mx.mx_gemm(a, b, out_dtype=torch.float32, out=C)
+    assert torch.count_nonzero(C).item() == 0
+    Cf = nan_like((64, 72), torch.float32)
+    mx.gemm_f16(torch.empty(64, 0, dtype=torch.half, device="cuda"),
+                torch.empty(0, 72, dtype=torch.half, device="cuda"), out=Cf)
+    assert torch.count_nonzero(Cf).item() == 0
+
+
+def test_padded_ldc():
+    fmt = oracle.E4M3
+    ca, sa = workloads.random_codes((256, 256), fmt, 5)
+    cb, sb = workloads.random_codes((256, 256), fmt, 6)
+    big = nan_like((256, 320), torch.float32)
+    mx.mx_gemm(planes_from_codes(ca, sa, fmt), planes_from_codes(cb, sb, fmt),
+               out_dtype=torch.float32, out=big[:, :256])
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
+    check_close(big[:, :256].cpu().numpy(), Cr, S, "f32", "ldc 320")
+    assert torch.isnan(big[:, 256:]).all()
+
+
+# ---------------------------------------------------------------- 16-bit path
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 1024),
+                                   (200, 296, 168), (1024, 1024, 1024),
+                                   (136, 264, 8)])
+def test_gemm_f16_small(dt, M, N, K):
+    tdt = torch.float16 if dt == "f16" else torch.bfloat16
+    g = torch.Generator().manual_seed(M + N + K)
+    A = (torch.rand(M, K, generator=g) * 2 - 1).to(tdt)
+    B = (torch.rand(K, N, generator=g) * 2 - 1).to(tdt)
+    C = nan_like((M, N), torch.float32)
+    mx.gemm_f16(A.cuda(), B.cuda(), out=C)
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_f16(f16_bits(A), f16_bits(B),
+                            oracle.F16 if dt == "f16" else oracle.BF16)
+    check_close(C.cpu().numpy(), Cr, S, "f32", f"{dt} {M}x{N}x{K}")
+
+
+def test_gemm_f16_strided_operands():
+    g = torch.Generator().manual_seed(2)
+    Abig = (torch.rand(256, 200, generator=g) * 2 - 1).half()
+    Bbig = (torch.rand(136, 328, generator=g) * 2 - 1).half()
+    A, B = Abig[:, :136], Bbig[:, :256]          # lda 200, ldb 328
+    C = mx.gemm_f16(A.cuda(), B.cuda())
+    Cr, S = oracle.gemm_f16(f16_bits(A), f16_bits(B), oracle.F16)
+    check_close(C.cpu().numpy(), Cr, S, "f32", "strided")
+
+
+# ---------------------------------------------------------------- workloads
+
+def _case_check(c, rows=None):
+    A, B = workloads.sources(c)
+    if c.kind in ("f16", "bf16"):
+        C = nan_like((c.M, c.N), torch.float32)
+        mx.gemm_f16(A.cuda(), B.cuda(), out=C)
+        assert mx.mx_last_error() == 0
+        Cg = C.cpu().numpy()
+        Cr, S = oracle.gemm_f16(f16_bits(A), f16_bits(B),
+                                oracle.F16 if c.kind == "f16" else oracle.BF16,
+                                rows=rows)
+    else:
+        fmt = fmt_code(c.kind)
+        Cg = _mx_run(A, B, fmt, c.out)
+        Cr, S = _mx_ref(A, B, fmt, rows=rows)
+    if rows is not None:
+        Cg = Cg[rows]
+    return check_close(Cg, Cr, S, c.out, c.name)
+
+
+SMALL = ["mx256", "f16_1024", "bf16_1024", "mxfp8_2048"]
+LARGE = ["f16_2048", "bf16_2048", "f16_4096", "bf16_4096", "mxfp8_4096",
+         "mxfp8_8192", "mxfp4_4096", "mxfp4_8192", "proj_qkv", "proj_out",
+         "proj_up", "proj_down"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_output(name):
+    _case_check(workloads.case(name))
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_sampled_rows(name):
+    c = workloads.case(name)
+    _case_check(c, rows=sample_rows(c.M, seed=c.seed_a))
+
+
+@pytest.mark.parametrize("name", ["mxfp8_4096", "bf16_2048", "mxfp4_4096"])
+def test_deterministic(name):
+    c = workloads.case(name)
+    A, B = workloads.sources(c)
+    if c.kind in ("f16", "bf16"):
+        A, B = A.cuda(), B.cuda()
+        C1, C2 = mx.gemm_f16(A, B), mx.gemm_f16(A, B)
+    else:
+        fmt = fmt_code(c.kind)
+        a = mx.mx_quantize(A.cuda(), fmt)
+        b = mx.mx_quantize(B.cuda(), fmt, k_strided=True)
+        C1 = mx.mx_gemm(a, b)
+        C2 = mx.mx_gemm(a, b)
+    assert torch.equal(C1.view(torch.uint8), C2.view(torch.uint8))

@@ -1,0 +1,127 @@
+"""mx_quantize on the GPU vs the oracle: bit-exact data codes and scale codes
+(scale plane compared through the oracle's own layout restatement), padding
+bytes zero, both source orientations, both formats, the full-size sources of
+the benchmark workloads, ragged shapes and adversarial blocks."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_quantized_mx_gb300 as mx
+import oracle
+import workloads
+from oracle import layout
+from tests._parity import lib_quantize_to_oracle_form
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [oracle.E4M3, oracle.E2M1]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    mx.build()
+    mx.lib()
+
+
+def _compare(src: torch.Tensor, fmt: int, k_strided: bool, nonfinite_rows=()):
+    q = mx.mx_quantize(src.cuda(), fmt, k_strided=k_strided)
+    torch.cuda.synchronize()
+    assert mx.mx_last_error() == 0
+    codes_g, scales_g = lib_quantize_to_oracle_form(q)
+    codes_o, scales_o = oracle.quantize(src.numpy(), fmt,
+                                        k_axis=0 if k_strided else 1)
+    assert np.array_equal(scales_g, scales_o), \
+        f"scales differ at {np.argwhere(scales_g != scales_o)[:5]}"
+    finite = scales_o != 0xFF
+    keep = np.repeat(finite, 32, axis=1)
+    diff = (codes_g != codes_o) & keep
+    assert not diff.any(), f"codes differ at {np.argwhere(diff)[:5]}"
+    pad = layout.pad_positions(q.outer, q.K)
+    assert not q.scales.cpu().numpy()[pad].any(), "padding bytes not zero"
+    return q
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("k_strided", [False, True])
+@pytest.mark.parametrize("outer,K", [(256, 256), (128, 32), (1, 32),
+                                     (300, 160), (130, 96), (512, 1024),
+                                     (1000, 544), (4, 4096)])
+def test_quantize_shapes(fmt, k_strided, outer, K):
+    g = torch.Generator().manual_seed(outer * 31 + K)
+    x = torch.randn(outer, K, generator=g)
+    x[torch.rand(outer, K, generator=g) < 0.01] *= 100
+    src = x.t().contiguous() if k_strided else x
+    _compare(src, fmt, k_strided)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("k_strided", [False, True])
+def test_quantize_padded_leading_dimension(fmt, k_strided):
+    g = torch.Generator().manual_seed(5)
+    big = torch.randn(200, 300, generator=g)
+    src = big[:, :256] if not k_strided else big[:192, :260]
+    q = mx.mx_quantize(src.cuda(), fmt, k_strided=k_strided)
+    codes_g, scales_g = lib_quantize_to_oracle_form(q)
+    codes_o, scales_o = oracle.quantize(src.contiguous().numpy(), fmt,
+                                        k_axis=0 if k_strided else 1)
+    assert np.array_equal(scales_g, scales_o)
+    assert np.array_equal(codes_g, codes_o)
+
+
+def _adversarial_blocks():
+    """128 x 1024 source whose 32-blocks hit the corner cases of the rule."""
+    rows = []
+    f32 = np.float32
+
+    def blk(vals):
+        b = np.zeros(32, dtype=f32)
+        b[:len(vals)] = vals
+        return b
+
+    specials = [
+        [1.0], [2.0], [0.5], [2.0 ** 127], [2.0 ** -126], [2.0 ** -149],
+        [float(np.nextafter(f32(2), f32(0)))],           # just below 2
+        [float(np.nextafter(f32(256), f32(0))), 1.0],     # just below 2^8
+        [0.0], [-0.0, 0.0, -0.0], [448.0], [449.0], [464.0], [480.0],
+        [500.0, -500.0], [15.0, 1.0, -7.5], [3.4e38, -1e-30],
+        [1.0, 2.0 ** -10, -2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -11],
+        [6.0, 5.0, 2.5, 0.25, 0.75, -1.25, 1.75, 3.5],   # E2M1 ties
+        [2.0 ** -130, -2.0 ** -140, 2.0 ** -149],         # subnormal block
+        list(2.0 ** np.arange(-15, 17, dtype=np.float64)),
+        list(-(2.0 ** np.arange(-20, 12, dtype=np.float64))),
+        [float("nan"), 1.0], [float("inf")], [-float("inf"), 3.0],
+    ]
+    for s in specials:
+        rows.append(blk(s))
+    g = np.random.default_rng(9)
+    while len(rows) < 128 * 32:
+        e = g.integers(-140, 127)
+        rows.append((g.standard_normal(32) * 2.0 ** e).astype(f32))
+    return np.stack(rows).reshape(128, 1024)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("k_strided", [False, True])
+def test_quantize_adversarial_blocks(fmt, k_strided):
+    x = torch.from_numpy(_adversarial_blocks())
+    src = x.t().contiguous() if k_strided else x
+    _compare(src, fmt, k_strided)
+
+
+@pytest.mark.parametrize("name", ["mx256", "mxfp8_8192", "mxfp4_8192",
+                                  "proj_down"])
+def test_quantize_full_size_sources(name):
+    """The full-size sources the benchmark quantizes, bit for bit."""
+    c = workloads.case(name)
+    A, B = workloads.sources(c)
+    fmt = oracle.E4M3 if c.kind == "mxfp8" else oracle.E2M1
+    _compare(A, fmt, False)
+    _compare(B, fmt, True)
+
+
+def test_quantize_is_deterministic():
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn(512, 512, generator=g).cuda()
+    q1 = mx.mx_quantize(x, oracle.E4M3)
+    q2 = mx.mx_quantize(x, oracle.E4M3)
+    assert torch.equal(q1.data, q2.data) and torch.equal(q1.scales, q2.scales)
