@@ -23,12 +23,20 @@ def _built():
     mx.lib()
 
 
-def _compare(src: torch.Tensor, fmt: int, k_strided: bool, nonfinite_rows=()):
-    q = mx.mx_quantize(src.cuda(), fmt, k_strided=k_strided)
+def _to_device_keep_stride(src: torch.Tensor) -> torch.Tensor:
+    if src.is_contiguous():
+        return src.cuda()
+    base = torch.empty(src.shape[0], src.stride(0), device="cuda")
+    base[:, :src.shape[1]] = src.cuda()
+    return base[:, :src.shape[1]]
+
+
+def _compare(src: torch.Tensor, fmt: int, k_strided: bool):
+    q = mx.mx_quantize(_to_device_keep_stride(src), fmt, k_strided=k_strided)
     torch.cuda.synchronize()
     assert mx.mx_last_error() == 0
     codes_g, scales_g = lib_quantize_to_oracle_form(q)
-    codes_o, scales_o = oracle.quantize(src.numpy(), fmt,
+    codes_o, scales_o = oracle.quantize(src.contiguous().numpy(), fmt,
                                         k_axis=0 if k_strided else 1)
     assert np.array_equal(scales_g, scales_o), \
         f"scales differ at {np.argwhere(scales_g != scales_o)[:5]}"
@@ -50,7 +58,15 @@ def test_quantize_shapes(fmt, k_strided, outer, K):
     g = torch.Generator().manual_seed(outer * 31 + K)
     x = torch.randn(outer, K, generator=g)
     x[torch.rand(outer, K, generator=g) < 0.01] *= 100
-    src = x.t().contiguous() if k_strided else x
+    if k_strided:
+        # K x outer source; its row stride is rounded up to 4 floats (16 B),
+        # as the API requires
+        ld = -(-outer // 4) * 4
+        wide = torch.zeros(K, ld)
+        wide[:, :outer] = x.t()
+        src = wide[:, :outer]
+    else:
+        src = x
     _compare(src, fmt, k_strided)
 
 
@@ -60,7 +76,9 @@ def test_quantize_padded_leading_dimension(fmt, k_strided):
     g = torch.Generator().manual_seed(5)
     big = torch.randn(200, 300, generator=g)
     src = big[:, :256] if not k_strided else big[:192, :260]
-    q = mx.mx_quantize(src.cuda(), fmt, k_strided=k_strided)
+    dsrc = _to_device_keep_stride(src)
+    assert dsrc.stride(0) == 300
+    q = mx.mx_quantize(dsrc, fmt, k_strided=k_strided)
     codes_g, scales_g = lib_quantize_to_oracle_form(q)
     codes_o, scales_o = oracle.quantize(src.contiguous().numpy(), fmt,
                                         k_axis=0 if k_strided else 1)
