@@ -9,7 +9,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/mx.h"
+#include "mx.h"
 #include "common.cuh"
 
 namespace {

@@ -10,23 +10,25 @@
 // here the tensor core applies the two scales per 32-wide K block itself.
 //
 // Design (GB300-first, not the pages' threadgroup-tile design):
-//   * tile 128 (M) x BN (N), BN = 256; one CTA per SM, persistent over tiles
-//     in a grouped raster order so that concurrently running CTAs share A and
-//     B tiles in L2;
-//   * warp 0: TMA producer -- A and B tiles (128-byte swizzled, 128 bytes of K
-//     per row per stage) plus the stage's scale atoms by bulk copy, into a
-//     STAGES-deep shared-memory ring guarded by mbarriers;
-//   * warp 1: allocates tensor memory and issues, from one thread, the
-//     scale-factor copies (tcgen05.cp, shared -> tensor memory) and 4 MMAs
-//     per stage (32 bytes of K each), then commits the stage back to the
-//     producer; after the last stage it commits the accumulator to the
-//     epilogue;
+//   * CG = 2 (default): a cluster of two CTAs on two SMs shares one
+//     256 (M) x 256 (N) MMA tile (tcgen05 cta_group::2).  Each CTA stages its
+//     own 128 rows of A and its own 128-row half of B, so per SM a stage is
+//     32 KB of operands for 256 x 256 x (128 bytes of K) of work; the leader
+//     CTA (rank 0) issues the MMAs for both.  CG = 1: one CTA, 128 x 256.
+//   * persistent: each cluster walks the tiles in a grouped raster order so
+//     that co-running clusters share A and B tiles in L2;
+//   * warp 0: TMA producer -- A, B (128-byte swizzle, 128 bytes of K per row
+//     per stage) and the stage's scale atoms, into a STAGES-deep ring; in a
+//     pair, both CTAs' copies complete on the leader's "full" barrier;
+//   * warp 1: tensor-memory allocation; in the leader, one thread issues the
+//     scale-factor copies (tcgen05.cp) and 4 MMAs per stage, commits each
+//     stage back to both producers and, per tile, the accumulator to both
+//     epilogues;
 //   * warps 2..9: epilogue -- each warp drains 128 accumulator columns of its
-//     32-lane quarter into registers (tcgen05.ld), hands the accumulator back
-//     to the MMA warp at once, then converts (fp32 or bf16, RNE) and stores
-//     while the next tile's main loop already runs.
-// Tensor memory: accumulator in columns [0, BN); per-stage scale factors from
-// column 256 on.
+//     32-lane quarter into registers, hands the accumulator back to the MMA
+//     issuer at once, then converts (fp32, or bf16 RNE) and stores while the
+//     next tile's main loop runs.
+// Tensor memory: accumulator in columns [0, BN); per-stage scales from 256.
 //
 // Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records a
 // timeout in g_status_gemm and the CTA shuts down in order.
@@ -43,14 +45,18 @@ __device__ unsigned int g_status_gemm = 0;
 
 enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_MXF8 = 2, KIND_MXF4 = 3 };
 
-constexpr int BM = 128;
-constexpr int NUM_THREADS = 320;    // 10 warps
-constexpr int EPI_WARP0 = 2;
-constexpr int NUM_EPI_THREADS = 256;
+constexpr int BM = 128;              // rows of A per CTA
+constexpr int BN = 256;              // columns of C per tile
 constexpr int TMEM_COLS = 512;
 constexpr int SF_TMEM_BASE = 256;
-constexpr int MMAS_PER_STAGE = 4;   // 4 x 32 bytes of K per 128-byte row
-constexpr int GROUP_M = 16;         // raster group height in M tiles
+constexpr int MMAS_PER_STAGE = 4;    // 4 x 32 bytes of K per 128-byte row
+constexpr int GROUP_M = 8;           // raster group height in M tiles
+// warp roles
+constexpr int EPI_WARP0 = 2;         // warps 2..9: epilogue, EPI_COLS columns each
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);
+constexpr int SF_WARP = EPI_WARP0 + NUM_EPI_WARPS;    // warp 10: scale-factor copies
+constexpr int NUM_THREADS = 32 * (SF_WARP + 1);       // 352
 
 template <int KIND>
 struct KT {
@@ -62,53 +68,52 @@ struct KT {
   static constexpr int CK = MX ? KPS / 128 : 0;
 };
 
-template <int KIND, int BN, int STAGES>
+template <int KIND, int CG, int STAGES>
 struct Smem {
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
-  static constexpr int SFA_BYTES = KT<KIND>::CK * 512;
-  static constexpr int SFB_BYTES = (BN / 128) * KT<KIND>::CK * 512;
+  static constexpr int B_BYTES = (BN / CG) * 128;       // this CTA's part of B
+  static constexpr int SFA_BYTES = KT<KIND>::CK * 512;  // this CTA's 128 rows
+  static constexpr int SFB_BYTES = (BN / 128) * KT<KIND>::CK * 512;  // all of BN
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
   static constexpr int SFA_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int SFB_OFF = SFA_OFF + STAGES * SFA_BYTES;
   static constexpr int BAR_OFF = (SFB_OFF + STAGES * SFB_BYTES + 7) / 8 * 8;
-  // full[STAGES], empty[STAGES], acc_full, acc_empty
-  static constexpr int MISC_OFF = BAR_OFF + (2 * STAGES + 2) * 8;
+  // full[STAGES], empty[STAGES], sf_ready[STAGES], acc_full, acc_empty
+  static constexpr int MISC_OFF = BAR_OFF + (3 * STAGES + 2) * 8;
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;   // slack to align the base to 1024
   // TMEM columns of scale factors per stage: A then B
   static constexpr int SF_COLS = KT<KIND>::CK * 4 * (1 + BN / 128);
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(BN <= SF_TMEM_BASE, "accumulator must fit below the scales");
+  static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 // Instruction descriptor, kind::f16: D f32, A/B f16 or bf16, A K-major,
-// B MN-major, N>>3 at bit 17, M>>4 at bit 24.
-template <int KIND, int BN>
+// B MN-major, N>>3 at bit 17, M>>4 at bit 24 (M = 128 per CTA of the group).
+template <int KIND, int CG>
 __host__ __device__ constexpr uint32_t idesc_f16() {
-  return (1u << 4) |                                   // D = f32
-         ((KIND == KIND_BF16 ? 1u : 0u) << 7) |        // A type
-         ((KIND == KIND_BF16 ? 1u : 0u) << 10) |       // B type
-         (0u << 15) |                                  // A K-major
-         (1u << 16) |                                  // B MN-major
+  return (1u << 4) | ((KIND == KIND_BF16 ? 1u : 0u) << 7) |
+         ((KIND == KIND_BF16 ? 1u : 0u) << 10) | (0u << 15) | (1u << 16) |
          (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>((BM * CG) >> 4) << 24);
 }
 
 // Instruction descriptor, block-scaled kinds: A/B format (E4M3 = 0 for
 // mxf8f6f4, E2M1 = 1 for mxf4), both K-major, N>>3 at bit 17, scale type
-// UE8M0 (bit 23), M>>4 at bit 24; scale-factor byte selectors at bits 4-5 (B)
-// and 29-30 (A) are filled in per MMA.
-template <int KIND, int BN>
+// UE8M0 (bit 23), M>>4 at bit 24; the scale-factor byte selectors (bits 4-5
+// for B, 29-30 for A) are filled in per MMA.
+template <int KIND, int CG>
 __host__ __device__ constexpr uint32_t idesc_mx() {
   return ((KIND == KIND_MXF4 ? 1u : 0u) << 7) | ((KIND == KIND_MXF4 ? 1u : 0u) << 10) |
          (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>((BM * CG) >> 4) << 24);
 }
 
 struct TileSched {
-  int num_m, num_n, total;
+  int num_m, num_n, total;   // in tiles of (BM*CG) x BN
   __device__ __forceinline__ void tile(int t, int& mb, int& nb) const {
     const int per_group = GROUP_M * num_n;
     const int g = t / per_group;
@@ -125,13 +130,14 @@ __device__ __forceinline__ void record_timeout(volatile int* abort, unsigned sit
   atomicOr(&g_status_gemm, STATUS_TIMEOUT | site);
 }
 
-template <int KIND, int BN, int STAGES, int OUT_BF16>
+template <int KIND, int CG, int STAGES, int OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const uint8_t* __restrict__ sfA, const uint8_t* __restrict__ sfB,
-            void* __restrict__ Cptr, int64_t ldc, int M, int N, int K) {
+            const __grid_constant__ CUtensorMap tmSFA,
+            const __grid_constant__ CUtensorMap tmSFB, void* __restrict__ Cptr,
+            int64_t ldc, int M, int N, int K) {
   using T = KT<KIND>;
-  using L = Smem<KIND, BN, STAGES>;
+  using L = Smem<KIND, CG, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -139,96 +145,105 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
   const uint32_t bar_full = base + L::BAR_OFF;
   const uint32_t bar_empty = bar_full + 8 * STAGES;
-  const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+  const uint32_t bar_sf_ready = bar_empty + 8 * STAGES;
+  const uint32_t bar_acc_full = bar_sf_ready + 8 * STAGES;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC_OFF);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const bool leader = (rank == 0);
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
 
   TileSched sched;
-  sched.num_m = (M + BM - 1) / BM;
+  sched.num_m = (M + BM * CG - 1) / (BM * CG);
   sched.num_n = (N + BN - 1) / BN;
   sched.total = sched.num_m * sched.num_n;
   const int num_kb = (K + T::KPS - 1) / T::KPS;
   const int k_atoms = (K + 127) / 128;
-  const int n_row_atoms = (N + 127) / 128;
+  // tiles of this cluster, and MMAs in a tile's last (possibly partial) stage
+  const int my_tiles = (sched.total - cluster_id + num_clusters - 1) / num_clusters;
+  const int last_nmma = min(MMAS_PER_STAGE,
+                            (K - (num_kb - 1) * T::KPS + T::MMA_K - 1) / T::MMA_K);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sf_ready + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, NUM_EPI_THREADS);
+    mbar_init(bar_acc_empty, CG * NUM_EPI_WARPS);
     *abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (T::MX) {
+      prefetch_tmap(&tmSFA);
+      prefetch_tmap(&tmSFB);
+    }
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
-  }
+  if (warp == 1) tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
-  __syncthreads();
+  if (CG == 2)
+    cluster_sync();   // peers' barriers are initialised before any remote use
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // all copies of the group complete on the leader's full barrier
+      const uint32_t full0 = (CG == 2) ? map_to_cta(bar_full, 0) : bar_full;
       uint32_t it = 0;
+      int s = 0;
+      uint32_t ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      for (int t = cluster_id; t < sched.total && ok; t += num_clusters) {
         int mb, nb;
         sched.tile(t, mb, nb);
+        const int m0 = mb * BM * CG + static_cast<int>(rank) * BM;   // this CTA's rows
+        const int nb_cta = nb * BN + static_cast<int>(rank) * (BN / CG);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = static_cast<int>(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort)) {
             record_timeout(abort, 1);
             ok = false;
             break;
           }
-          const uint32_t full = bar_full + 8 * s;
-          uint32_t bytes = L::A_BYTES + L::B_BYTES;
-          int ck_valid = 0;
-          if (T::MX) {
-            ck_valid = min(T::CK, k_atoms - kb * T::CK);
-            int nh = 0;
-            for (int h = 0; h < BN / 128; ++h)
-              if (nb * (BN / 128) + h < n_row_atoms) ++nh;
-            bytes += static_cast<uint32_t>(ck_valid * 512 * (1 + nh));
-          }
-          mbar_arrive_expect_tx(full, bytes);
+          if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, CG * L::STAGE_TX);
+          const uint32_t full = full0 + 8 * s;
           const uint32_t a_dst = base + L::A_OFF + s * L::A_BYTES;
           const uint32_t b_dst = base + L::B_OFF + s * L::B_BYTES;
           if (T::MX) {
             // data planes are byte matrices: x counts bytes of K
-            tma_load_2d(a_dst, &tmA, full, kb * 128, mb * BM);
-            tma_load_2d(b_dst, &tmB, full, kb * 128, nb * BN);
-            const uint32_t sfa_dst = base + L::SFA_OFF + s * L::SFA_BYTES;
-            bulk_load(sfa_dst, sfA + (static_cast<int64_t>(mb) * k_atoms + kb * T::CK) * 512,
-                      ck_valid * 512, full);
-            const uint32_t sfb_dst = base + L::SFB_OFF + s * L::SFB_BYTES;
-            for (int h = 0; h < BN / 128; ++h) {
-              const int ra = nb * (BN / 128) + h;
-              if (ra < n_row_atoms)
-                bulk_load(sfb_dst + h * T::CK * 512,
-                          sfB + (static_cast<int64_t>(ra) * k_atoms + kb * T::CK) * 512,
-                          ck_valid * 512, full);
-            }
+            tma_load_2d_cg<CG>(a_dst, &tmA, full, kb * 128, m0);
+            tma_load_2d_cg<CG>(b_dst, &tmB, full, kb * 128, nb_cta);
+            // scale planes viewed as [atoms][128 x u32]: one box = CK atoms;
+            // each CTA takes the atoms of its own A rows and of all BN rows
+            tma_load_2d_cg<CG>(base + L::SFA_OFF + s * L::SFA_BYTES, &tmSFA, full, 0,
+                               (m0 / 128) * k_atoms + kb * T::CK);
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d_cg<CG>(base + L::SFB_OFF + s * L::SFB_BYTES + h * T::CK * 512,
+                                 &tmSFB, full, 0,
+                                 (nb * (BN / 128) + h) * k_atoms + kb * T::CK);
           } else {
-            tma_load_2d(a_dst, &tmA, full, kb * 64, mb * BM);
-            // B is K x N row-major: BN/64 boxes of 64 (N) x 64 (K rows)
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * 64 * 128, &tmB, full, nb * BN + 64 * j, kb * 64);
+            tma_load_2d_cg<CG>(a_dst, &tmA, full, kb * 64, m0);
+            // B is K x N row-major: boxes of 64 (N) x 64 (K rows)
+            for (int j = 0; j < BN / CG / 64; ++j)
+              tma_load_2d_cg<CG>(b_dst + j * 64 * 128, &tmB, full, nb_cta + 64 * j, kb * 64);
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // let copies already issued land before the CTA retires
         const uint32_t first = it >= STAGES ? it - STAGES : 0;
         for (uint32_t i = first; i < it; ++i) {
@@ -242,76 +257,84 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, tc = 0;
+    // One thread of the leader issues every MMA of the group.  The issuing
+    // thread is the critical path (each tcgen05.mma occupies it for about as
+    // long as the tensor core takes to run it), so it does nothing else per
+    // stage: one wait, the stage's MMAs, one commit.  Scale factors are
+    // copied into tensor memory by the scale-copy warp.
+    if (leader && lane == 0) {
+      const uint64_t a_desc0 = smem_desc(base + L::A_OFF, 16, 1024, 2);
+      const uint64_t b_desc0 = T::MX ? smem_desc(base + L::B_OFF, 16, 1024, 2)
+                                     : smem_desc(base + L::B_OFF, 64 * 128, 1024, 2);
+      // per MMA: A advances 32 bytes of K; B 32 bytes (K-major) or 16 K rows
+      // of 128 bytes (MN-major); descriptors count 16-byte units
+      constexpr uint32_t A_STEP = 32 >> 4;
+      constexpr uint32_t B_STEP = (T::MX ? 32 : 2048) >> 4;
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t tc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x, ++tc) {
+      for (int ti = 0; ti < my_tiles && ok; ++ti, ++tc) {
         if (!mbar_wait(bar_acc_empty, (tc & 1u) ^ 1u, abort)) {
           record_timeout(abort, 2);
-          ok = false;
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = static_cast<int>(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(bar_full + 8 * s, ph, abort)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          // MX: the scale copy of this stage is done (which implies its data
+          // has landed); 16-bit kinds: the data has landed
+          const uint32_t ready = (T::MX ? bar_sf_ready : bar_full) + 8 * s;
+          if (!mbar_wait(ready, ph, abort)) {
             record_timeout(abort, 3);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_s = base + L::A_OFF + s * L::A_BYTES;
-          const uint32_t b_s = base + L::B_OFF + s * L::B_BYTES;
+          const uint64_t a_d = a_desc0 + static_cast<uint64_t>((s * L::A_BYTES) >> 4);
+          const uint64_t b_d = b_desc0 + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
           const uint32_t sfa_t = tmem_base + SF_TMEM_BASE + s * L::SF_COLS;
           const uint32_t sfb_t = sfa_t + T::CK * 4;
-          const int k_left = K - kb * T::KPS;
-          const int nmma = min(MMAS_PER_STAGE, (k_left + T::MMA_K - 1) / T::MMA_K);
-          if (T::MX) {
-            const int ck_valid = min(T::CK, k_atoms - kb * T::CK);
-            const uint32_t sfa_s = base + L::SFA_OFF + s * L::SFA_BYTES;
-            const uint32_t sfb_s = base + L::SFB_OFF + s * L::SFB_BYTES;
-            for (int c = 0; c < ck_valid; ++c) {
-              tc_cp_32x128b_x4(sfa_t + 4 * c, smem_desc(sfa_s + c * 512, 0, 128, 0));
-              for (int h = 0; h < BN / 128; ++h)
-                tc_cp_32x128b_x4(sfb_t + c * 4 * (BN / 128) + 4 * h,
-                                 smem_desc(sfb_s + (h * T::CK + c) * 512, 0, 128, 0));
+          const int nmma = (kb + 1 < num_kb) ? MMAS_PER_STAGE : last_nmma;
+#pragma unroll
+          for (int m = 0; m < MMAS_PER_STAGE; ++m) {
+            if (m < nmma) {
+              const uint32_t acc = (kb > 0 || m > 0) ? 1u : 0u;
+              const uint64_t ad = a_d + m * A_STEP;
+              const uint64_t bd = b_d + m * B_STEP;
+              if (KIND == KIND_F16 || KIND == KIND_BF16) {
+                mma_f16_cg<CG>(tmem_base, ad, bd, idesc_f16<KIND, CG>(), acc);
+              } else if (KIND == KIND_MXF8) {
+                constexpr uint32_t ID = idesc_mx<KIND, CG>();
+                mma_mxf8_cg<CG>(tmem_base, ad, bd,
+                                ID | (static_cast<uint32_t>(m) << 4) |
+                                    (static_cast<uint32_t>(m) << 29),
+                                sfa_t, sfb_t, acc);
+              } else {
+                constexpr uint32_t ID = idesc_mx<KIND, CG>();
+                const uint32_t sf_id = static_cast<uint32_t>((m & 1) * 2);
+                mma_mxf4_cg<CG>(tmem_base, ad, bd, ID | (sf_id << 4) | (sf_id << 29),
+                                sfa_t + 4 * (m >> 1), sfb_t + (m >> 1) * 4 * (BN / 128),
+                                acc);
+              }
             }
           }
-          for (int m = 0; m < nmma; ++m) {
-            const uint32_t acc = (kb > 0 || m > 0) ? 1u : 0u;
-            const uint64_t a_desc = smem_desc(a_s + 32 * m, 16, 1024, 2);
-            if (KIND == KIND_F16 || KIND == KIND_BF16) {
-              // B MN-major: 64-wide N chunks LBO = 64 K rows * 128 B apart,
-              // 8-row K groups SBO = 1024 B apart; 16 K rows per MMA
-              const uint64_t b_desc = smem_desc(b_s + 2048 * m, 64 * 128, 1024, 2);
-              mma_f16(tmem_base, a_desc, b_desc, idesc_f16<KIND, BN>(), acc);
-            } else if (KIND == KIND_MXF8) {
-              const uint64_t b_desc = smem_desc(b_s + 32 * m, 16, 1024, 2);
-              const uint32_t id = idesc_mx<KIND, BN>() | (static_cast<uint32_t>(m) << 4) |
-                                  (static_cast<uint32_t>(m) << 29);
-              mma_mxf8(tmem_base, a_desc, b_desc, id, sfa_t, sfb_t, acc);
-            } else {
-              const uint64_t b_desc = smem_desc(b_s + 32 * m, 16, 1024, 2);
-              const int c = m >> 1;                       // scale atom along K
-              const uint32_t sf_id = static_cast<uint32_t>((m & 1) * 2);
-              const uint32_t id = idesc_mx<KIND, BN>() | (sf_id << 4) | (sf_id << 29);
-              mma_mxf4(tmem_base, a_desc, b_desc, id, sfa_t + 4 * c,
-                       sfb_t + c * 4 * (BN / 128), acc);
-            }
+          tc_commit_cg<CG>(bar_empty + 8 * s);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
           }
-          tc_commit(bar_empty + 8 * s);
         }
         if (!ok) break;
-        tc_commit(bar_acc_full);
+        tc_commit_cg<CG>(bar_acc_full);
       }
     }
-  } else {
+  } else if (warp < SF_WARP) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                        // TMEM lane quarter
-    const int half = (warp - EPI_WARP0) >> 2;      // which BN/2 columns
+    const int q = warp & 3;                          // TMEM lane quarter
+    const int cg_ = (warp - EPI_WARP0) >> 2;         // which EPI_COLS columns
+    const uint32_t acc_empty0 = (CG == 2) ? map_to_cta(bar_acc_empty, 0) : bar_acc_empty;
     uint32_t tc = 0;
-    for (int t = blockIdx.x; t < sched.total; t += gridDim.x, ++tc) {
+    for (int t = cluster_id; t < sched.total; t += num_clusters, ++tc) {
       int mb, nb;
       sched.tile(t, mb, nb);
       if (!mbar_wait(bar_acc_full, tc & 1u, abort)) {
@@ -319,23 +342,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         break;
       }
       tc_fence_after();
-      uint32_t r[BN / 2];
+      uint32_t r[EPI_COLS];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                             static_cast<uint32_t>(half * (BN / 2));
+                             static_cast<uint32_t>(cg_ * EPI_COLS);
 #pragma unroll
-      for (int i = 0; i < BN / 64; ++i)
+      for (int i = 0; i < EPI_COLS / 32; ++i)
         tmem_ld_32x32b_x32(taddr + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * i));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar_acc_empty);
+      __syncwarp();
+      if (lane == 0) {
+        if (CG == 2)
+          mbar_arrive_cluster(acc_empty0);
+        else
+          mbar_arrive(bar_acc_empty);
+      }
 
-      const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
-      const int col0 = nb * BN + half * (BN / 2);
+      const int64_t row = static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q + lane;
+      const int col0 = nb * BN + cg_ * EPI_COLS;
       if (row < M) {
         if (OUT_BF16) {
           uint16_t* crow = reinterpret_cast<uint16_t*>(Cptr) + row * ldc;
 #pragma unroll
-          for (int v = 0; v < BN / 16; ++v) {       // 8 columns per vector
+          for (int v = 0; v < EPI_COLS / 8; ++v) {    // 8 columns per vector
             const int c = col0 + 8 * v;
             uint32_t w[4];
 #pragma unroll
@@ -347,15 +376,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e)
-                if (c + e < N)
-                  crow[c + e] =
-                      static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+                if (c + e < N) crow[c + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
             }
           }
         } else {
           float* crow = reinterpret_cast<float*>(Cptr) + row * ldc;
 #pragma unroll
-          for (int v = 0; v < BN / 8; ++v) {        // 4 columns per vector
+          for (int v = 0; v < EPI_COLS / 4; ++v) {    // 4 columns per vector
             const int c = col0 + 4 * v;
             if (c + 3 < N) {
               *reinterpret_cast<uint4*>(crow + c) =
@@ -369,13 +396,56 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
       }
     }
+  } else if (T::MX) {
+    // ------------------------------------------------------------ scale copies
+    // For every stage: once its data (and scale atoms) have landed, copy the
+    // scale atoms into that stage's tensor-memory slot with tcgen05.cp (each
+    // 512-byte atom -> 4 columns of every lane quarter), then commit the copies
+    // to the stage's sf_ready barrier, which the MMA issuer waits on.  The
+    // slot is free: the stage was refilled only after the MMAs that last read
+    // it had completed.
+    if (leader && lane == 0) {
+      const uint32_t total_it = static_cast<uint32_t>(my_tiles) * num_kb;
+      int s = 0;
+      uint32_t ph = 0;
+      int kb = 0;
+      for (uint32_t j = 0; j < total_it; ++j) {
+        if (!mbar_wait(bar_full + 8 * s, ph, abort)) {
+          record_timeout(abort, 5);
+          break;
+        }
+        tc_fence_after();
+        const int nmma = (kb + 1 < num_kb) ? MMAS_PER_STAGE : last_nmma;
+        const int ck_used = (nmma * T::MMA_K + 127) / 128;
+        const uint32_t sfa_t = tmem_base + SF_TMEM_BASE + s * L::SF_COLS;
+        const uint32_t sfb_t = sfa_t + T::CK * 4;
+        const uint32_t sfa_s = base + L::SFA_OFF + s * L::SFA_BYTES;
+        const uint32_t sfb_s = base + L::SFB_OFF + s * L::SFB_BYTES;
+        for (int c = 0; c < ck_used; ++c) {
+          tc_cp_32x128b_x4_cg<CG>(sfa_t + 4 * c, smem_desc(sfa_s + c * 512, 0, 128, 0));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tc_cp_32x128b_x4_cg<CG>(sfb_t + c * 4 * (BN / 128) + 4 * h,
+                                    smem_desc(sfb_s + (h * T::CK + c) * 512, 0, 128, 0));
+        }
+        tc_commit_leader<CG>(bar_sf_ready + 8 * s);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++kb == num_kb) kb = 0;
+      }
+    }
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (CG == 2)
+    cluster_sync();   // no CTA of the pair retires while the other may use it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_cg<CG>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -395,10 +465,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D tensor map, row-major rows x cols (cols contiguous), 128-byte swizzle.
+// 2-D tensor map, row-major rows x cols (cols contiguous).
 bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
                uint64_t cols, uint64_t rows, uint64_t ld_elems, uint32_t box_cols,
-               uint32_t box_rows) {
+               uint32_t box_rows, CUtensorMapSwizzle swz) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -406,9 +476,16 @@ bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The scale plane as rows of 512-byte atoms (128 x u32); one box = ck atoms.
+bool make_sf_tmap(CUtensorMap* m, const uint8_t* sf, int64_t outer, int64_t K, int ck) {
+  const uint64_t atoms = static_cast<uint64_t>(sf_row_atoms(outer) * sf_k_atoms(K));
+  return make_tmap(m, sf, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128, atoms, 128, 128,
+                   static_cast<uint32_t>(ck), CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int sm_count() {
@@ -423,12 +500,12 @@ int sm_count() {
   return n;
 }
 
-template <int KIND, int BN, int STAGES, int OUT_BF16>
-cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* sfa,
-                const uint8_t* sfb, void* C, int64_t ldc, int M, int N, int K,
+template <int KIND, int CG, int STAGES, int OUT_BF16>
+cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
                 cudaStream_t st) {
-  using L = Smem<KIND, BN, STAGES>;
-  auto kern = gemm_kernel<KIND, BN, STAGES, OUT_BF16>;
+  using L = Smem<KIND, CG, STAGES>;
+  auto kern = gemm_kernel<KIND, CG, STAGES, OUT_BF16>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -438,14 +515,35 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* sfa
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(ta, tb, sfa, sfb, C, ldc, M, N, K);
-  return cudaGetLastError();
+  const int tiles = ((M + BM * CG - 1) / (BM * CG)) * ((N + BN - 1) / BN);
+  const int max_clusters = sm_count() / CG;
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, C, ldc, M, N, K);
 }
 
-constexpr int BN_DEF = 256;
-constexpr int STAGES_DEF = 4;
+constexpr int STAGES_CG1 = 4;
+constexpr int STAGES_CG2 = 6;
+
+template <int KIND, int OUT_BF16>
+cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                     const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
+                     cudaStream_t st) {
+  if (M > BM)
+    return run<KIND, 2, STAGES_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
+  return run<KIND, 1, STAGES_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
+}
 
 }  // namespace
 
@@ -457,20 +555,23 @@ cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
   const int eb = (c_dtype == DT_BF16) ? 2 : 4;
   if (K == 0) return launch_zero_fill(C, M, N, ldc, eb, st);
   const uint64_t kbytes = (fmt == FMT_E4M3) ? K : K / 2;
-  CUtensorMap ta, tb;
-  if (!make_tmap(&ta, a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, M, kbytes, 128, BM) ||
-      !make_tmap(&tb, b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, N, kbytes, 128,
-                 BN_DEF))
+  const int ck = (fmt == FMT_E4M3) ? KT<KIND_MXF8>::CK : KT<KIND_MXF4>::CK;
+  // one TMA box of B is this CTA's half of the N tile when M > BM
+  const uint32_t b_rows = (M > BM) ? BN / 2 : BN;
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!make_tmap(&ta, a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, M, kbytes, 128, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tb, b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, N, kbytes, 128, b_rows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_sf_tmap(&tsa, a_sf, M, K, ck) || !make_sf_tmap(&tsb, b_sf, N, K, ck))
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (fmt == FMT_E4M3) {
-    if (c_dtype == DT_BF16)
-      return run<KIND_MXF8, BN_DEF, STAGES_DEF, 1>(ta, tb, a_sf, b_sf, C, ldc, m, n, k, st);
-    return run<KIND_MXF8, BN_DEF, STAGES_DEF, 0>(ta, tb, a_sf, b_sf, C, ldc, m, n, k, st);
+    if (c_dtype == DT_BF16) return dispatch<KIND_MXF8, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
+    return dispatch<KIND_MXF8, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
   }
-  if (c_dtype == DT_BF16)
-    return run<KIND_MXF4, BN_DEF, STAGES_DEF, 1>(ta, tb, a_sf, b_sf, C, ldc, m, n, k, st);
-  return run<KIND_MXF4, BN_DEF, STAGES_DEF, 0>(ta, tb, a_sf, b_sf, C, ldc, m, n, k, st);
+  if (c_dtype == DT_BF16) return dispatch<KIND_MXF4, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
+  return dispatch<KIND_MXF4, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
 }
 
 cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
@@ -481,13 +582,13 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
   const CUtensorMapDataType dt = (ab_dtype == DT_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, A, dt, 2, K, M, lda, 64, BM) ||
-      !make_tmap(&tb, B, dt, 2, N, K, ldb, 64, 64))
+  if (!make_tmap(&ta, A, dt, 2, K, M, lda, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tb, B, dt, 2, N, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  if (ab_dtype == DT_BF16)
-    return run<KIND_BF16, BN_DEF, STAGES_DEF, 0>(ta, tb, nullptr, nullptr, C, ldc, m, n, k, st);
-  return run<KIND_F16, BN_DEF, STAGES_DEF, 0>(ta, tb, nullptr, nullptr, C, ldc, m, n, k, st);
+  // the scale maps are unused by the 16-bit kinds
+  if (ab_dtype == DT_BF16) return dispatch<KIND_BF16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, st);
+  return dispatch<KIND_F16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, st);
 }
 
 unsigned fetch_and_clear_status_gemm(cudaError_t* err) {
