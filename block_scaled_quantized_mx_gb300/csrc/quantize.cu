@@ -132,98 +132,89 @@ quantize_kcontig(const float* __restrict__ src, int64_t ld, int64_t outer,
 
 // ---------------------------------------------------------------------------
 // Source K x outer, outer contiguous (a row-major K x N operand); output is
-// outer x K (K-major).  CTA = (row group rg of outer, K chunk kc): the
-// 128 (K) x 128 (outer) fp32 tile is staged in shared memory with coalesced
-// float4 row loads, then each thread takes whole blocks (one output row n,
-// one block j of 32 K values) by reading a column of the tile -- consecutive
-// lanes read consecutive n, so the column reads are free of bank conflicts.
+// outer x K (K-major).  CTA = (row group rg of 128 outputs, K chunk kc of 128),
+// 4 warps; warp w owns block j = w (32 consecutive K) and lane l owns the four
+// output rows n = 128*rg + 4l .. 4l+3.  For i = 0..31 the warp loads source
+// row k = 128*kc + 32*w + i at columns 128*rg + 4l.. as one float4 per lane --
+// 512 contiguous bytes per warp instruction -- so each lane ends up holding the
+// complete 32-element block of each of its four output rows in registers: the
+// transpose costs no shared-memory pass and the amax no shuffles.
 template <int FMT>
-__global__ void __launch_bounds__(QT_THREADS)
+__global__ void __launch_bounds__(128)
 quantize_kstrided(const float* __restrict__ src, int64_t ld, int64_t outer,
                   int64_t K, uint8_t* __restrict__ data, uint8_t* __restrict__ sf) {
   constexpr int EMAX = (FMT == FMT_E4M3) ? 8 : 2;
-  extern __shared__ __align__(16) float tile[];   // [128][128] + atom
-  uint8_t* atom = reinterpret_cast<uint8_t*>(tile + 128 * 128);
+  __shared__ __align__(16) uint8_t atom[SF_ATOM_BYTES];
 
-  const int64_t rg = blockIdx.x;     // group of 128 output rows (outer)
-  const int64_t kc = blockIdx.y;     // chunk of 128 K
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int64_t rg = blockIdx.x;
+  const int64_t kc = blockIdx.y;
   const int64_t k_atoms = sf_k_atoms(K);
-  const int tid = threadIdx.x;
 
-  for (int i = tid; i < SF_ATOM_BYTES / 16; i += QT_THREADS)
-    reinterpret_cast<uint4*>(atom)[i] = make_uint4(0, 0, 0, 0);
-
-  // stage: tile[kk][nn] = src[(kc*128 + kk) * ld + rg*128 + nn]
-  {
-    const int c4 = tid & 31;                   // float4 column
-    const int64_t n = rg * 128 + 4 * c4;
-#pragma unroll 4
-    for (int kk = tid >> 5; kk < 128; kk += QT_THREADS / 32) {
-      const int64_t kg = kc * 128 + kk;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (kg < K) {
-        const float* p = src + kg * ld + n;
-        if (n + 3 < outer) {
-          v = __ldcs(reinterpret_cast<const float4*>(p));
-        } else {
-          if (n + 0 < outer) v.x = __ldcs(p + 0);
-          if (n + 1 < outer) v.y = __ldcs(p + 1);
-          if (n + 2 < outer) v.z = __ldcs(p + 2);
-        }
-      }
-      reinterpret_cast<float4*>(tile + kk * 128)[c4] = v;
-    }
-  }
+  reinterpret_cast<uint32_t*>(atom)[threadIdx.x] = 0u;   // 128 threads x 4 B
   __syncthreads();
 
+  const int64_t kb = kc * 128 + 32 * w;            // first K of this warp's block
+  const int64_t n = rg * 128 + 4 * lane;           // first of the lane's 4 rows
+  if (kb < K) {                                    // K % 32 == 0: whole block valid
+    float4 v[32];
+    const float* p = src + kb * ld + n;
+    if (n + 3 < outer) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int u = tid + QT_THREADS * h;
-    const int nl = u & 127;                    // output row inside the group
-    const int j = u >> 7;                      // block inside the chunk
-    const int64_t n = rg * 128 + nl;
-    const int64_t kb = kc * 128 + 32 * j;      // first K of the block
-    if (n >= outer || kb >= K) continue;
-    float x[32];
-    uint32_t a = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      x[i] = tile[(32 * j + i) * 128 + nl];
-      a = max(a, abs_bits(x[i]));
-    }
-    uint32_t code;
-    float s;
-    block_scale(a, EMAX, code, s);
-    atom[sf_in_atom(nl, j)] = static_cast<uint8_t>(code);
-    if (FMT == FMT_E4M3) {
-      uint32_t w[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        w[i] = cvt_e4m3x2(x[4 * i] * s, x[4 * i + 1] * s) |
-               (cvt_e4m3x2(x[4 * i + 2] * s, x[4 * i + 3] * s) << 16);
-      uint4* dst = reinterpret_cast<uint4*>(data + n * K + kb);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      for (int i = 0; i < 32; ++i) v[i] = __ldcs(reinterpret_cast<const float4*>(p + i * ld));
     } else {
-      uint32_t w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float* y = x + 8 * i;
-        w[i] = cvt_e2m1x2(y[0] * s, y[1] * s) | (cvt_e2m1x2(y[2] * s, y[3] * s) << 8) |
-               (cvt_e2m1x2(y[4] * s, y[5] * s) << 16) |
-               (cvt_e2m1x2(y[6] * s, y[7] * s) << 24);
+      for (int i = 0; i < 32; ++i) {
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (n + 0 < outer) v[i].x = __ldcs(p + i * ld + 0);
+        if (n + 1 < outer) v[i].y = __ldcs(p + i * ld + 1);
+        if (n + 2 < outer) v[i].z = __ldcs(p + i * ld + 2);
       }
-      *reinterpret_cast<uint4*>(data + (n * K + kb) / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (n + c >= outer) break;
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        x[i] = (c == 0) ? v[i].x : (c == 1) ? v[i].y : (c == 2) ? v[i].z : v[i].w;
+      uint32_t a = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a = max(a, abs_bits(x[i]));
+      uint32_t code;
+      float s;
+      block_scale(a, EMAX, code, s);
+      atom[sf_in_atom(4 * lane + c, w)] = static_cast<uint8_t>(code);
+      if (FMT == FMT_E4M3) {
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          q[i] = cvt_e4m3x2(x[4 * i] * s, x[4 * i + 1] * s) |
+                 (cvt_e4m3x2(x[4 * i + 2] * s, x[4 * i + 3] * s) << 16);
+        uint4* dst = reinterpret_cast<uint4*>(data + (n + c) * K + kb);
+        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      } else {
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float* y = x + 8 * i;
+          q[i] = cvt_e2m1x2(y[0] * s, y[1] * s) | (cvt_e2m1x2(y[2] * s, y[3] * s) << 8) |
+                 (cvt_e2m1x2(y[4] * s, y[5] * s) << 16) |
+                 (cvt_e2m1x2(y[6] * s, y[7] * s) << 24);
+        }
+        *reinterpret_cast<uint4*>(data + ((n + c) * K + kb) / 2) =
+            make_uint4(q[0], q[1], q[2], q[3]);
+      }
     }
   }
   __syncthreads();
-  if (tid < SF_ATOM_BYTES / 16) {
+  if (threadIdx.x < SF_ATOM_BYTES / 16) {
     uint4* dst = reinterpret_cast<uint4*>(sf + (rg * k_atoms + kc) * SF_ATOM_BYTES);
-    dst[tid] = reinterpret_cast<const uint4*>(atom)[tid];
+    dst[threadIdx.x] = reinterpret_cast<const uint4*>(atom)[threadIdx.x];
   }
 }
-
-constexpr int KSTRIDED_SMEM = 128 * 128 * 4 + SF_ATOM_BYTES;
 
 template <int FMT>
 cudaError_t launch_fmt(const float* src, int64_t ld, int k_strided, int64_t outer,
@@ -233,19 +224,8 @@ cudaError_t launch_fmt(const float* src, int64_t ld, int k_strided, int64_t oute
     dim3 grid(static_cast<unsigned>(ka), static_cast<unsigned>(ra));
     quantize_kcontig<FMT><<<grid, QT_THREADS, 0, st>>>(src, ld, outer, K, data, sf);
   } else {
-    static bool attr_set[64] = {};   // per device ordinal
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_set[dev]) {
-      e = cudaFuncSetAttribute(quantize_kstrided<FMT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, KSTRIDED_SMEM);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) attr_set[dev] = true;
-    }
     dim3 grid(static_cast<unsigned>(ra), static_cast<unsigned>(ka));
-    quantize_kstrided<FMT><<<grid, QT_THREADS, KSTRIDED_SMEM, st>>>(src, ld, outer, K,
-                                                                    data, sf);
+    quantize_kstrided<FMT><<<grid, 128, 0, st>>>(src, ld, outer, K, data, sf);
   }
   return cudaGetLastError();
 }
