@@ -49,7 +49,7 @@ constexpr int BM = 128;              // rows of A per CTA
 constexpr int BN = 256;              // columns of C per tile
 constexpr int TMEM_COLS = 512;
 constexpr int SF_TMEM_BASE = 256;
-constexpr int MMAS_PER_STAGE = 4;    // 4 x 32 bytes of K per 128-byte row
+constexpr int MMAS_PER_SUB = 4;      // 4 x 32 bytes of K per 128-byte sub-tile
 constexpr int GROUP_M = 8;           // raster group height in M tiles
 // warp roles
 constexpr int EPI_WARP0 = 2;         // warps 2..9: epilogue, EPI_COLS columns each
@@ -58,22 +58,28 @@ constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);
 constexpr int SF_WARP = EPI_WARP0 + NUM_EPI_WARPS;    // warp 10: scale-factor copies
 constexpr int NUM_THREADS = 32 * (SF_WARP + 1);       // 352
 
-template <int KIND>
+// A stage holds KSUB sub-tiles of 128 bytes of K per operand row (each its
+// own 128-byte-swizzled region); 4 MMAs per sub-tile.
+template <int KIND, int KSUB>
 struct KT {
   static constexpr bool MX = (KIND == KIND_MXF8 || KIND == KIND_MXF4);
-  // K elements per stage (128 bytes of K per operand row)
-  static constexpr int KPS = (KIND == KIND_MXF4) ? 256 : (MX ? 128 : 64);
-  static constexpr int MMA_K = KPS / MMAS_PER_STAGE;
+  // K elements per 128-byte sub-tile, and per stage
+  static constexpr int KPSUB = (KIND == KIND_MXF4) ? 256 : (MX ? 128 : 64);
+  static constexpr int KPS = KPSUB * KSUB;
+  static constexpr int MMAS_PER_STAGE = MMAS_PER_SUB * KSUB;
+  static constexpr int MMA_K = KPSUB / MMAS_PER_SUB;
   // scale atoms (128 K each) per stage along K
   static constexpr int CK = MX ? KPS / 128 : 0;
 };
 
-template <int KIND, int CG, int STAGES>
+template <int KIND, int CG, int STAGES, int KSUB>
 struct Smem {
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = (BN / CG) * 128;       // this CTA's part of B
-  static constexpr int SFA_BYTES = KT<KIND>::CK * 512;  // this CTA's 128 rows
-  static constexpr int SFB_BYTES = (BN / 128) * KT<KIND>::CK * 512;  // all of BN
+  static constexpr int A_SUB = BM * 128;                // one sub-tile of A
+  static constexpr int B_SUB = (BN / CG) * 128;         // this CTA's part of B
+  static constexpr int A_BYTES = A_SUB * KSUB;
+  static constexpr int B_BYTES = B_SUB * KSUB;
+  static constexpr int SFA_BYTES = KT<KIND, KSUB>::CK * 512;  // this CTA's 128 rows
+  static constexpr int SFB_BYTES = (BN / 128) * KT<KIND, KSUB>::CK * 512;  // all of BN
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
@@ -85,7 +91,7 @@ struct Smem {
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;   // slack to align the base to 1024
   // TMEM columns of scale factors per stage: A then B
-  static constexpr int SF_COLS = KT<KIND>::CK * 4 * (1 + BN / 128);
+  static constexpr int SF_COLS = KT<KIND, KSUB>::CK * 4 * (1 + BN / 128);
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(BN <= SF_TMEM_BASE, "accumulator must fit below the scales");
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -130,14 +136,14 @@ __device__ __forceinline__ void record_timeout(volatile int* abort, unsigned sit
   atomicOr(&g_status_gemm, STATUS_TIMEOUT | site);
 }
 
-template <int KIND, int CG, int STAGES, int OUT_BF16>
+template <int KIND, int CG, int STAGES, int KSUB, int OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmSFA,
             const __grid_constant__ CUtensorMap tmSFB, void* __restrict__ Cptr,
             int64_t ldc, int M, int N, int K) {
-  using T = KT<KIND>;
-  using L = Smem<KIND, CG, STAGES>;
+  using T = KT<KIND, KSUB>;
+  using L = Smem<KIND, CG, STAGES, KSUB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -166,7 +172,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const int k_atoms = (K + 127) / 128;
   // tiles of this cluster, and MMAs in a tile's last (possibly partial) stage
   const int my_tiles = (sched.total - cluster_id + num_clusters - 1) / num_clusters;
-  const int last_nmma = min(MMAS_PER_STAGE,
+  const int last_nmma = min(T::MMAS_PER_STAGE,
                             (K - (num_kb - 1) * T::KPS + T::MMA_K - 1) / T::MMA_K);
 
   if (threadIdx.x == 0) {
@@ -221,8 +227,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           const uint32_t b_dst = base + L::B_OFF + s * L::B_BYTES;
           if (T::MX) {
             // data planes are byte matrices: x counts bytes of K
-            tma_load_2d_cg<CG>(a_dst, &tmA, full, kb * 128, m0);
-            tma_load_2d_cg<CG>(b_dst, &tmB, full, kb * 128, nb_cta);
+#pragma unroll
+            for (int u = 0; u < KSUB; ++u) {
+              const int kx = (kb * KSUB + u) * 128;
+              tma_load_2d_cg<CG>(a_dst + u * L::A_SUB, &tmA, full, kx, m0);
+              tma_load_2d_cg<CG>(b_dst + u * L::B_SUB, &tmB, full, kx, nb_cta);
+            }
             // scale planes viewed as [atoms][128 x u32]: one box = CK atoms;
             // each CTA takes the atoms of its own A rows and of all BN rows
             tma_load_2d_cg<CG>(base + L::SFA_OFF + s * L::SFA_BYTES, &tmSFA, full, 0,
@@ -232,10 +242,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                  &tmSFB, full, 0,
                                  (nb * (BN / 128) + h) * k_atoms + kb * T::CK);
           } else {
-            tma_load_2d_cg<CG>(a_dst, &tmA, full, kb * 64, m0);
-            // B is K x N row-major: boxes of 64 (N) x 64 (K rows)
-            for (int j = 0; j < BN / CG / 64; ++j)
-              tma_load_2d_cg<CG>(b_dst + j * 64 * 128, &tmB, full, nb_cta + 64 * j, kb * 64);
+#pragma unroll
+            for (int u = 0; u < KSUB; ++u) {
+              const int k0 = kb * T::KPS + u * 64;
+              tma_load_2d_cg<CG>(a_dst + u * L::A_SUB, &tmA, full, k0, m0);
+              // B is K x N row-major: boxes of 64 (N) x 64 (K rows)
+              for (int j = 0; j < BN / CG / 64; ++j)
+                tma_load_2d_cg<CG>(b_dst + u * L::B_SUB + j * 64 * 128, &tmB, full,
+                                   nb_cta + 64 * j, k0);
+            }
           }
           if (++s == STAGES) {
             s = 0;
@@ -294,27 +309,31 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           const uint64_t b_d = b_desc0 + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
           const uint32_t sfa_t = tmem_base + SF_TMEM_BASE + s * L::SF_COLS;
           const uint32_t sfb_t = sfa_t + T::CK * 4;
-          const int nmma = (kb + 1 < num_kb) ? MMAS_PER_STAGE : last_nmma;
+          const int nmma = (kb + 1 < num_kb) ? T::MMAS_PER_STAGE : last_nmma;
 #pragma unroll
-          for (int m = 0; m < MMAS_PER_STAGE; ++m) {
+          for (int m = 0; m < T::MMAS_PER_STAGE; ++m) {
             if (m < nmma) {
               const uint32_t acc = (kb > 0 || m > 0) ? 1u : 0u;
-              const uint64_t ad = a_d + m * A_STEP;
-              const uint64_t bd = b_d + m * B_STEP;
+              const int u = m / MMAS_PER_SUB, mm = m % MMAS_PER_SUB;
+              const uint64_t ad = a_d + ((u * L::A_SUB) >> 4) + mm * A_STEP;
+              const uint64_t bd = b_d + ((u * L::B_SUB) >> 4) + mm * B_STEP;
               if (KIND == KIND_F16 || KIND == KIND_BF16) {
                 mma_f16_cg<CG>(tmem_base, ad, bd, idesc_f16<KIND, CG>(), acc);
               } else if (KIND == KIND_MXF8) {
+                // one scale atom (4 blocks) per sub-tile; byte mm of it
                 constexpr uint32_t ID = idesc_mx<KIND, CG>();
                 mma_mxf8_cg<CG>(tmem_base, ad, bd,
-                                ID | (static_cast<uint32_t>(m) << 4) |
-                                    (static_cast<uint32_t>(m) << 29),
-                                sfa_t, sfb_t, acc);
+                                ID | (static_cast<uint32_t>(mm) << 4) |
+                                    (static_cast<uint32_t>(mm) << 29),
+                                sfa_t + 4 * u, sfb_t + u * 4 * (BN / 128), acc);
               } else {
+                // two scale atoms per sub-tile, two MMAs per atom; bytes
+                // {0,1} or {2,3} of it
                 constexpr uint32_t ID = idesc_mx<KIND, CG>();
+                const int c = m >> 1;
                 const uint32_t sf_id = static_cast<uint32_t>((m & 1) * 2);
                 mma_mxf4_cg<CG>(tmem_base, ad, bd, ID | (sf_id << 4) | (sf_id << 29),
-                                sfa_t + 4 * (m >> 1), sfb_t + (m >> 1) * 4 * (BN / 128),
-                                acc);
+                                sfa_t + 4 * c, sfb_t + c * 4 * (BN / 128), acc);
               }
             }
           }
@@ -415,7 +434,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           break;
         }
         tc_fence_after();
-        const int nmma = (kb + 1 < num_kb) ? MMAS_PER_STAGE : last_nmma;
+        const int nmma = (kb + 1 < num_kb) ? T::MMAS_PER_STAGE : last_nmma;
         const int ck_used = (nmma * T::MMA_K + 127) / 128;
         const uint32_t sfa_t = tmem_base + SF_TMEM_BASE + s * L::SF_COLS;
         const uint32_t sfb_t = sfa_t + T::CK * 4;
@@ -500,12 +519,12 @@ int sm_count() {
   return n;
 }
 
-template <int KIND, int CG, int STAGES, int OUT_BF16>
+template <int KIND, int CG, int STAGES, int KSUB, int OUT_BF16>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                 const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
                 cudaStream_t st) {
-  using L = Smem<KIND, CG, STAGES>;
-  auto kern = gemm_kernel<KIND, CG, STAGES, OUT_BF16>;
+  using L = Smem<KIND, CG, STAGES, KSUB>;
+  auto kern = gemm_kernel<KIND, CG, STAGES, KSUB, OUT_BF16>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -533,16 +552,20 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, C, ldc, M, N, K);
 }
 
+// K sub-tiles per stage and ring depth; the ring holds the same bytes either
+// way, more K per stage means fewer waits and commits per MMA
+constexpr int KSUB_CG2 = 1;
+constexpr int STAGES_CG2 = 6 / KSUB_CG2;
+constexpr int KSUB_CG1 = 1;
 constexpr int STAGES_CG1 = 4;
-constexpr int STAGES_CG2 = 6;
 
 template <int KIND, int OUT_BF16>
 cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                      const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
                      cudaStream_t st) {
   if (M > BM)
-    return run<KIND, 2, STAGES_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
-  return run<KIND, 1, STAGES_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
+    return run<KIND, 2, STAGES_CG2, KSUB_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
+  return run<KIND, 1, STAGES_CG1, KSUB_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
 }
 
 }  // namespace
@@ -555,7 +578,11 @@ cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
   const int eb = (c_dtype == DT_BF16) ? 2 : 4;
   if (K == 0) return launch_zero_fill(C, M, N, ldc, eb, st);
   const uint64_t kbytes = (fmt == FMT_E4M3) ? K : K / 2;
-  const int ck = (fmt == FMT_E4M3) ? KT<KIND_MXF8>::CK : KT<KIND_MXF4>::CK;
+  // scale atoms per stage of the configuration dispatch() picks
+  const bool pair = M > BM;
+  const int ck = (fmt == FMT_E4M3)
+                     ? (pair ? KT<KIND_MXF8, KSUB_CG2>::CK : KT<KIND_MXF8, KSUB_CG1>::CK)
+                     : (pair ? KT<KIND_MXF4, KSUB_CG2>::CK : KT<KIND_MXF4, KSUB_CG1>::CK);
   // one TMA box of B is this CTA's half of the N tile when M > BM
   const uint32_t b_rows = (M > BM) ? BN / 2 : BN;
   CUtensorMap ta, tb, tsa, tsb;
