@@ -118,6 +118,22 @@ def flops_of(c):
     return 2.0 * c.M * c.N * c.K
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Largest elapsed time over all ranks (every rank gets the result).
+    Ranks are independent replicas of the step, so the job's time is the
+    slowest rank's; with one rank this is the identity."""
+    if world <= 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def quant_bytes(fmt, rows, K):
     """Algorithmic bytes of one mx_quantize: fp32 in, codes + scales out."""
     code = rows * K if fmt == 1 else rows * K / 2
@@ -196,12 +212,9 @@ def run_ours(args, rank, world, local_rank):
     ms = t0.elapsed_time(t1)
     per_kernel = [[e[j].elapsed_time(e[j + 1]) for e in evs]
                   for j in range(nev - 1)]
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
-    tflops = flops_of(c) * world / (ms_step * 1e-3) / 1e12
+    tflops = job_throughput(flops_of(c), world, ms_step)
 
     gemm_ms = statistics.mean(per_kernel[-1])
     gemm_tf = flops_of(c) / (gemm_ms * 1e-3) / 1e12
@@ -242,12 +255,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": flops_of(c) * world / (ems * 1e-3) / 1e12,
+        ems = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": job_throughput(flops_of(c), world, ems),
                "unit": "TFLOP/s", "ms_per_step": ems,
                "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
                                          hB.numel() * hB.element_size()),
@@ -351,7 +360,7 @@ def run_reference(args):
     }
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -365,7 +374,11 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="total seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 
@@ -374,6 +387,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
+        # the CPU oracle runs once, on rank 0; other ranks exit without work
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
