@@ -134,6 +134,59 @@ def job_throughput(flops_per_rank: float, world: int, ms: float) -> float:
     return flops_per_rank * world / (ms * 1e-3) / 1e12
 
 
+L2_BYTES = 129 * 2 ** 20
+
+
+class L2Flusher:
+    """Writes a buffer larger than L2 so that the next kernel starts cold."""
+
+    def __init__(self, dev):
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32,
+                               device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
+    """CUDA-event time of the GEMM kernel alone on pre-quantized operands
+    (mean over iters; L2 flushed before every launch when a flusher is
+    given).  Returns (ms, TFLOP/s)."""
+    A, B = workloads.sources(c)
+    dA, dB = A.to(dev), B.to(dev)
+    out_dt = torch.bfloat16 if c.out == "bf16" else torch.float32
+    C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
+    if c.kind in ("mxfp8", "mxfp4"):
+        fmt = mx.E4M3 if c.kind == "mxfp8" else mx.E2M1
+        qa = mx.mx_quantize(dA, fmt)
+        qb = mx.mx_quantize(dB, fmt, k_strided=True)
+        del dA, dB
+        nb = mx.mx_gemm_workspace_bytes(fmt, c.M, c.N, c.K) if splitk else 0
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        f = lambda: mx.mx_gemm(qa, qb, out_dtype=out_dt, out=C, workspace=ws)  # noqa
+    else:
+        nb = mx.gemm_f16_workspace_bytes(c.M, c.N, c.K) if splitk else 0
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        f = lambda: mx.gemm_f16(dA, dB, out=C, workspace=ws)  # noqa
+    for _ in range(3):
+        f()
+    stream = torch.cuda.current_stream()
+    tot = 0.0
+    for _ in range(iters):
+        if flusher is not None:
+            flusher()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        f()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    assert mx.mx_last_error() == 0
+    ms = tot / iters
+    return ms, flops_of(c) / (ms * 1e-3) / 1e12
+
+
 def quant_bytes(fmt, rows, K):
     """Algorithmic bytes of one mx_quantize: fp32 in, codes + scales out."""
     code = rows * K if fmt == 1 else rows * K / 2
@@ -159,6 +212,14 @@ def run_ours(args, rank, world, local_rank):
     if is_mx:
         qa = mx.empty_mx(fmt, c.M, c.K, dev)
         qb = mx.empty_mx(fmt, c.N, c.K, dev)
+        ws_bytes = mx.mx_gemm_workspace_bytes(fmt, c.M, c.N, c.K)
+    else:
+        ws_bytes = mx.gemm_f16_workspace_bytes(c.M, c.N, c.K)
+    # scratch for the K-split of the last wave of tiles (allocated here,
+    # once); off by default: measured on GB300 it does not beat the unsplit
+    # kernel on the default workload
+    ws = (torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+          if ws_bytes and args.splitk else None)
 
     # per-kernel events so every launch's duration is known
     def step(ev=None):
@@ -171,17 +232,23 @@ def run_ours(args, rank, world, local_rank):
             mx.mx_quantize(dB, fmt, k_strided=True, out=qb)
             if ev is not None:
                 ev[2].record(stream)
-            mx.mx_gemm(qa, qb, out_dtype=out_dt, out=C)
+            mx.mx_gemm(qa, qb, out_dtype=out_dt, out=C, workspace=ws)
             if ev is not None:
                 ev[3].record(stream)
         else:
             if ev is not None:
                 ev[0].record(stream)
-            mx.gemm_f16(dA, dB, out=C)
+            mx.gemm_f16(dA, dB, out=C, workspace=ws)
             if ev is not None:
                 ev[1].record(stream)
 
-    launches_per_step = 3 if is_mx else 1
+    # our kernels per step: 2 quantizes (MX) + the GEMM (+ the partials'
+    # reduction when the K-split is active)
+    launches_per_step = (3 if is_mx else 1) + (1 if ws is not None else 0)
+    # operands smaller than L2: flush it between timed steps, and take the
+    # step time from the kernels' own events (the flush is not timed)
+    src_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
+    flusher = L2Flusher(dev) if src_bytes < 2 * L2_BYTES else None
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -204,6 +271,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     t0.record(stream)
     for i in range(args.steps):
+        if flusher is not None:
+            flusher()
         step(evs[i])
     t1.record(stream)
     barrier()
@@ -212,6 +281,8 @@ def run_ours(args, rank, world, local_rank):
     ms = t0.elapsed_time(t1)
     per_kernel = [[e[j].elapsed_time(e[j + 1]) for e in evs]
                   for j in range(nev - 1)]
+    if flusher is not None:
+        ms = sum(e[0].elapsed_time(e[nev - 1]) for e in evs)
     ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
     tflops = job_throughput(flops_of(c), world, ms_step)
@@ -262,6 +333,19 @@ def run_ours(args, rank, world, local_rank):
                                          hB.numel() * hB.element_size()),
                "d2h_bytes_per_step": int(hC.numel() * hC.element_size())}
 
+    others = {}
+    if not args.no_others and rank == 0:
+        fl = L2Flusher(dev)
+        for name in args.others.split(","):
+            if not name or name == c.name:
+                continue
+            oc = workloads.case(name)
+            ms_o, tf_o = time_gemm_only(mx, oc, dev, flusher=fl,
+                                        splitk=args.splitk)
+            others[name] = {"gemm_ms": ms_o, "tflops": tf_o,
+                            "frac_of_peak": tf_o / (bf16 * NOMINAL_RATIO[oc.kind])}
+        del fl
+
     roofline = {"bound": "tensor", "kernel": "mx_gemm" if is_mx else "gemm_f16",
                 "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
                 "frac": gemm_tf / peak, "traffic": None,
@@ -277,14 +361,15 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded)",
         "config": {"workload": c.name, "M": c.M, "N": c.N, "K": c.K,
                    "out": c.out, "dist": c.dist_a,
-                   "l2": "inputs larger than L2 (fp32 sources %d MB each)"
-                         % (4 * c.M * c.K // 2 ** 20) if is_mx else
-                         "operands %d MB + %d MB; no flush" %
-                         (2 * c.M * c.K // 2 ** 20, 2 * c.K * c.N // 2 ** 20),
+                   "l2": ("inputs larger than L2 (sources %d MB + %d MB)" %
+                          (src_bytes // 2 ** 21, src_bytes // 2 ** 21))
+                         if flusher is None else
+                         "L2 flushed between steps (258 MB write, not timed)",
                    "parallelism": "replicas%d" % world},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
         "breakdown": extra,
+        "gemm_only_other_workloads": others,
         "e2e": e2e,
         "clocks": clk,
     }
@@ -374,6 +459,14 @@ def parse_args(argv=None):
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="total seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--others", default="mxfp8_4096,mxfp4_8192,mxfp4_4096,"
+                    "bf16_4096,f16_4096,bf16_2048,bf16_1024,proj_qkv,proj_out,"
+                    "proj_up,proj_down,mx256",
+                    help="workloads whose GEMM alone is also timed (L2 "
+                         "flushed before each launch)")
+    ap.add_argument("--no-others", action="store_true")
+    ap.add_argument("--splitk", action="store_true",
+                    help="use the K-split GEMM entry points (with a workspace)")
     return ap.parse_args(argv)
 
 

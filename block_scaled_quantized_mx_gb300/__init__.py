@@ -30,8 +30,10 @@ STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
           6: "MX_ERR_TIMEOUT"}
 
 EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
-           "gemm_f16", "mx_last_error", "mx_selftest_wait_timeout",
-           "mx_scales_to_rowmajor", "mx_status_string", "mx_version")
+           "gemm_f16", "mx_gemm_workspace_bytes", "mx_gemm_splitk",
+           "gemm_f16_workspace_bytes", "gemm_f16_splitk", "mx_last_error",
+           "mx_selftest_wait_timeout", "mx_scales_to_rowmajor",
+           "mx_status_string", "mx_version")
 
 
 class MXError(RuntimeError):
@@ -82,6 +84,15 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm.argtypes = [pt, pt, p, i32, i64, p]
     L.gemm_f16.restype = i32
     L.gemm_f16.argtypes = [p, p, p, i32, i64, i64, i64, i64, i64, i64, p]
+    L.mx_gemm_workspace_bytes.restype = sz
+    L.mx_gemm_workspace_bytes.argtypes = [i32, i64, i64, i64]
+    L.mx_gemm_splitk.restype = i32
+    L.mx_gemm_splitk.argtypes = [pt, pt, p, i32, i64, p, sz, p]
+    L.gemm_f16_workspace_bytes.restype = sz
+    L.gemm_f16_workspace_bytes.argtypes = [i64, i64, i64]
+    L.gemm_f16_splitk.restype = i32
+    L.gemm_f16_splitk.argtypes = [p, p, p, i32, i64, i64, i64, i64, i64, i64,
+                                  p, sz, p]
     L.mx_last_error.restype = i32
     L.mx_last_error.argtypes = [p]
     L.mx_selftest_wait_timeout.restype = i32
@@ -163,23 +174,41 @@ def mx_quantize(src: torch.Tensor, fmt: int, k_strided: bool = False,
     return out
 
 
+def mx_gemm_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:
+    return int(lib().mx_gemm_workspace_bytes(fmt, M, N, K))
+
+
+def gemm_f16_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().gemm_f16_workspace_bytes(M, N, K))
+
+
 def mx_gemm(A: MXTensor, B: MXTensor, out_dtype=torch.bfloat16,
-            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """C = A * B for MX tensors A (M x K) and B (quantized from K x N)."""
+            out: torch.Tensor | None = None, stream=None,
+            workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """C = A * B for MX tensors A (M x K) and B (quantized from K x N).
+    With a workspace (a CUDA tensor of at least mx_gemm_workspace_bytes()
+    bytes) the K-split entry point is used."""
     dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
     if out is None:
         out = torch.empty((A.outer, B.outer), dtype=out_dtype,
                           device=A.data.device)
     ca, cb = A.c(), B.c()
-    _check(lib().mx_gemm(ctypes.byref(ca), ctypes.byref(cb),
-                         out.data_ptr() if out.numel() else None, dt,
-                         out.stride(0) if out.dim() == 2 else B.outer,
-                         _stream(stream)), "mx_gemm")
+    cptr = out.data_ptr() if out.numel() else None
+    ldc = out.stride(0) if out.dim() == 2 else B.outer
+    if workspace is None:
+        _check(lib().mx_gemm(ctypes.byref(ca), ctypes.byref(cb), cptr, dt, ldc,
+                             _stream(stream)), "mx_gemm")
+    else:
+        _check(lib().mx_gemm_splitk(
+            ctypes.byref(ca), ctypes.byref(cb), cptr, dt, ldc,
+            workspace.data_ptr() if workspace.numel() else None,
+            workspace.numel() * workspace.element_size(), _stream(stream)),
+            "mx_gemm_splitk")
     return out
 
 
 def gemm_f16(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
-             stream=None) -> torch.Tensor:
+             stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """C (fp32) = A * B for row-major fp16 or bf16 CUDA tensors."""
     if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("A and B must both be fp16 or both bf16")
@@ -190,11 +219,17 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     dt = DT_F16 if A.dtype == torch.float16 else DT_BF16
-    _check(lib().gemm_f16(A.data_ptr() if A.numel() else None,
-                          B.data_ptr() if B.numel() else None,
-                          out.data_ptr() if out.numel() else None, dt, M, N, K,
-                          A.stride(0), B.stride(0), out.stride(0),
-                          _stream(stream)), "gemm_f16")
+    args = (A.data_ptr() if A.numel() else None,
+            B.data_ptr() if B.numel() else None,
+            out.data_ptr() if out.numel() else None, dt, M, N, K,
+            A.stride(0), B.stride(0), out.stride(0))
+    if workspace is None:
+        _check(lib().gemm_f16(*args, _stream(stream)), "gemm_f16")
+    else:
+        _check(lib().gemm_f16_splitk(
+            *args, workspace.data_ptr() if workspace.numel() else None,
+            workspace.numel() * workspace.element_size(), _stream(stream)),
+            "gemm_f16_splitk")
     return out
 
 

@@ -100,7 +100,34 @@ mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dty
   if (!aligned16(C)) return MX_ERR_ALIGN;
   if ((s = check_device()) != MX_OK) return s;
   return from_cuda(mxk::launch_gemm_mx(A->fmt, A->data, A->scales, B->data, B->scales, C,
-                                       c_dtype, ldc, M, N, K,
+                                       c_dtype, ldc, M, N, K, nullptr, 0,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t mx_gemm_workspace_bytes(int32_t fmt, int64_t M, int64_t N, int64_t K) {
+  if (fmt != MX_FMT_E4M3 && fmt != MX_FMT_E2M1) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 32 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return 0;
+  if (check_device() != MX_OK) return 0;
+  return mxk::gemm_workspace_bytes(fmt, M, N, K);
+}
+
+mx_status mx_gemm_splitk(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dtype,
+                         int64_t ldc, void* workspace, size_t workspace_bytes, void* stream) {
+  mx_status s;
+  if ((s = check_tensor(A)) != MX_OK) return s;
+  if ((s = check_tensor(B)) != MX_OK) return s;
+  if (A->fmt != B->fmt || A->K != B->K) return MX_ERR_SHAPE;
+  if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  const int64_t M = A->outer, N = B->outer, K = A->K;
+  if (M == 0 || N == 0) return MX_OK;
+  if (!C) return MX_ERR_INVALID_ARG;
+  const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
+  if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
+  if (!aligned16(C) || (workspace && !aligned16(workspace))) return MX_ERR_ALIGN;
+  if ((s = check_device()) != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_mx(A->fmt, A->data, A->scales, B->data, B->scales, C,
+                                       c_dtype, ldc, M, N, K, workspace, workspace_bytes,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -121,8 +148,35 @@ mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype, int
   }
   mx_status s = check_device();
   if (s != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc,
-                                        static_cast<cudaStream_t>(stream)));
+  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc, nullptr,
+                                        0, static_cast<cudaStream_t>(stream)));
+}
+
+size_t gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+  if (check_device() != MX_OK) return 0;
+  return mxk::gemm_workspace_bytes(0, M, N, K);
+}
+
+mx_status gemm_f16_splitk(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,
+                          int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (ab_dtype != MX_DT_F16 && ab_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MX_ERR_SHAPE;
+  if (M == 0 || N == 0) return MX_OK;
+  if (!C) return MX_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 4) return MX_ERR_SHAPE;
+  if (!aligned16(C) || (workspace && !aligned16(workspace))) return MX_ERR_ALIGN;
+  if (K > 0) {
+    if (!A || !B) return MX_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || lda % 8 || ldb % 8) return MX_ERR_SHAPE;
+    if (!aligned16(A) || !aligned16(B)) return MX_ERR_ALIGN;
+  }
+  mx_status s = check_device();
+  if (s != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc, workspace,
+                                        workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 mx_status mx_last_error(void* stream) {

@@ -46,14 +46,21 @@ cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt
                             cudaStream_t st);
 
 // mx GEMM: A data outer=M, B data outer=N, both K-major; C row-major.
+// ws: workspace for the fp32 partials of K-split tiles (nullptr, or fewer
+// than gemm_workspace_bytes() bytes: no splitting).
 cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
                            const void* b_data, const uint8_t* b_sf, void* C,
                            int c_dtype, int64_t ldc, int64_t M, int64_t N,
-                           int64_t K, cudaStream_t st);
+                           int64_t K, void* ws, size_t ws_bytes, cudaStream_t st);
 
 cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
                             int64_t M, int64_t N, int64_t K, int64_t lda,
-                            int64_t ldb, int64_t ldc, cudaStream_t st);
+                            int64_t ldb, int64_t ldc, void* ws, size_t ws_bytes,
+                            cudaStream_t st);
+
+// Workspace bytes the K-split needs (0: the problem is not split).
+// kind: FMT_E4M3, FMT_E2M1, or 0 for the 16-bit GEMM.
+size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K);
 
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc,
                              int elem_bytes, cudaStream_t st);

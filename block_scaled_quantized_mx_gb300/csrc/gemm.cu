@@ -120,7 +120,7 @@ __host__ __device__ constexpr uint32_t idesc_mx() {
 
 struct TileSched {
   int num_m, num_n, total;   // in tiles of (BM*CG) x BN
-  __device__ __forceinline__ void tile(int t, int& mb, int& nb) const {
+  __host__ __device__ __forceinline__ void tile(int t, int& mb, int& nb) const {
     const int per_group = GROUP_M * num_n;
     const int g = t / per_group;
     const int first_m = g * GROUP_M;
@@ -128,6 +128,44 @@ struct TileSched {
     const int r = t - g * per_group;
     mb = first_m + r % gsz;
     nb = r / gsz;
+  }
+};
+
+// Work items: [0, full_tiles) are whole tiles in raster order; the remaining
+// tiles (the last, partial wave) are each split into `split` K ranges, one
+// work item per range, whose fp32 partial tiles go to the workspace and are
+// summed by reduce_partials_kernel.
+struct WorkList {
+  TileSched sched;
+  int num_kb;
+  int full_tiles;
+  int split;
+  int total;
+  __host__ __device__ void init(int num_m, int num_n, int kb, int full, int sp) {
+    sched.num_m = num_m;
+    sched.num_n = num_n;
+    sched.total = num_m * num_n;
+    num_kb = kb;
+    full_tiles = full;
+    split = sp;
+    total = full + (sched.total - full) * sp;
+  }
+  // unit < 0: a whole tile (write C); else index of the partial in the workspace
+  __host__ __device__ __forceinline__ void item(int w, int& mb, int& nb, int& kb0, int& kb1,
+                                       int& unit) const {
+    if (w < full_tiles) {
+      sched.tile(w, mb, nb);
+      kb0 = 0;
+      kb1 = num_kb;
+      unit = -1;
+    } else {
+      const int u = w - full_tiles;
+      const int sp = u % split;
+      sched.tile(full_tiles + u / split, mb, nb);
+      kb0 = sp * num_kb / split;
+      kb1 = (sp + 1) * num_kb / split;
+      unit = u;
+    }
   }
 };
 
@@ -141,7 +179,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmSFA,
             const __grid_constant__ CUtensorMap tmSFB, void* __restrict__ Cptr,
-            int64_t ldc, int M, int N, int K) {
+            int64_t ldc, int M, int N, int K, float* __restrict__ ws, int full_tiles,
+            int split) {
   using T = KT<KIND, KSUB>;
   using L = Smem<KIND, CG, STAGES, KSUB>;
   extern __shared__ uint8_t smem_raw[];
@@ -164,14 +203,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;
 
-  TileSched sched;
-  sched.num_m = (M + BM * CG - 1) / (BM * CG);
-  sched.num_n = (N + BN - 1) / BN;
-  sched.total = sched.num_m * sched.num_n;
   const int num_kb = (K + T::KPS - 1) / T::KPS;
   const int k_atoms = (K + 127) / 128;
-  // tiles of this cluster, and MMAs in a tile's last (possibly partial) stage
-  const int my_tiles = (sched.total - cluster_id + num_clusters - 1) / num_clusters;
+  WorkList work;
+  work.init((M + BM * CG - 1) / (BM * CG), (N + BN - 1) / BN, num_kb, full_tiles, split);
+  // MMAs in a tile's last (possibly partial) stage
   const int last_nmma = min(T::MMAS_PER_STAGE,
                             (K - (num_kb - 1) * T::KPS + T::MMA_K - 1) / T::MMA_K);
 
@@ -210,12 +246,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = cluster_id; t < sched.total && ok; t += num_clusters) {
-        int mb, nb;
-        sched.tile(t, mb, nb);
+      for (int w = cluster_id; w < work.total && ok; w += num_clusters) {
+        int mb, nb, kb0, kb1, unit;
+        work.item(w, mb, nb, kb0, kb1, unit);
         const int m0 = mb * BM * CG + static_cast<int>(rank) * BM;   // this CTA's rows
         const int nb_cta = nb * BN + static_cast<int>(rank) * (BN / CG);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort)) {
             record_timeout(abort, 1);
             ok = false;
@@ -289,13 +325,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       uint32_t ph = 0;
       uint32_t tc = 0;
       bool ok = true;
-      for (int ti = 0; ti < my_tiles && ok; ++ti, ++tc) {
+      for (int w = cluster_id; w < work.total && ok; w += num_clusters, ++tc) {
+        int mb, nb, kb0, kb1, unit;
+        work.item(w, mb, nb, kb0, kb1, unit);
         if (!mbar_wait(bar_acc_empty, (tc & 1u) ^ 1u, abort)) {
           record_timeout(abort, 2);
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           // MX: the scale copy of this stage is done (which implies its data
           // has landed); 16-bit kinds: the data has landed
           const uint32_t ready = (T::MX ? bar_sf_ready : bar_full) + 8 * s;
@@ -313,7 +351,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
           for (int m = 0; m < T::MMAS_PER_STAGE; ++m) {
             if (m < nmma) {
-              const uint32_t acc = (kb > 0 || m > 0) ? 1u : 0u;
+              const uint32_t acc = (kb > kb0 || m > 0) ? 1u : 0u;
               const int u = m / MMAS_PER_SUB, mm = m % MMAS_PER_SUB;
               const uint64_t ad = a_d + ((u * L::A_SUB) >> 4) + mm * A_STEP;
               const uint64_t bd = b_d + ((u * L::B_SUB) >> 4) + mm * B_STEP;
@@ -353,9 +391,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int cg_ = (warp - EPI_WARP0) >> 2;         // which EPI_COLS columns
     const uint32_t acc_empty0 = (CG == 2) ? map_to_cta(bar_acc_empty, 0) : bar_acc_empty;
     uint32_t tc = 0;
-    for (int t = cluster_id; t < sched.total; t += num_clusters, ++tc) {
-      int mb, nb;
-      sched.tile(t, mb, nb);
+    for (int w = cluster_id; w < work.total; w += num_clusters, ++tc) {
+      int mb, nb, kb0, kb1, unit;
+      work.item(w, mb, nb, kb0, kb1, unit);
       if (!mbar_wait(bar_acc_full, tc & 1u, abort)) {
         record_timeout(abort, 4);
         break;
@@ -377,6 +415,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           mbar_arrive(bar_acc_empty);
       }
 
+      if (unit >= 0) {
+        // partial of a split tile: the whole fp32 accumulator row segment to
+        // the workspace (rows and columns beyond M, N included; the reduction
+        // ignores them)
+        float* wrow = ws + static_cast<int64_t>(unit) * (BM * CG * BN) +
+                      static_cast<int64_t>(rank * BM + 32 * q + lane) * BN + cg_ * EPI_COLS;
+#pragma unroll
+        for (int v = 0; v < EPI_COLS / 4; ++v)
+          *reinterpret_cast<uint4*>(wrow + 4 * v) =
+              make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        continue;
+      }
       const int64_t row = static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q + lane;
       const int col0 = nb * BN + cg_ * EPI_COLS;
       if (row < M) {
@@ -424,13 +474,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // slot is free: the stage was refilled only after the MMAs that last read
     // it had completed.
     if (leader && lane == 0) {
-      const uint32_t total_it = static_cast<uint32_t>(my_tiles) * num_kb;
       int s = 0;
       uint32_t ph = 0;
-      int kb = 0;
-      for (uint32_t j = 0; j < total_it; ++j) {
+      bool ok = true;
+      for (int w = cluster_id; w < work.total && ok; w += num_clusters) {
+       int mb, nb, kb0, kb1, unit;
+       work.item(w, mb, nb, kb0, kb1, unit);
+       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(bar_full + 8 * s, ph, abort)) {
           record_timeout(abort, 5);
+          ok = false;
           break;
         }
         tc_fence_after();
@@ -452,7 +505,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           s = 0;
           ph ^= 1u;
         }
-        if (++kb == num_kb) kb = 0;
+       }
       }
     }
   }
@@ -465,6 +518,51 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_cg<CG>(tmem_base, TMEM_COLS);
+  }
+}
+
+// Sum the `split` fp32 partials of each split tile in a fixed order (so the
+// result does not depend on timing) and write C.  CTA = (split tile r,
+// group of 4 tile rows); each thread owns 4 consecutive columns.
+template <int OUT_BF16>
+__global__ void __launch_bounds__(256)
+reduce_partials_kernel(const float* __restrict__ ws, void* __restrict__ Cptr, int64_t ldc,
+                       int M, int N, WorkList work, int tile_rows) {
+  const int r = blockIdx.x;
+  int mb, nb;
+  work.sched.tile(work.full_tiles + r, mb, nb);
+  const int i = blockIdx.y * 4 + (threadIdx.x >> 6);          // row in tile
+  const int c = (threadIdx.x & 63) * 4;                       // column in tile
+  const int64_t row = static_cast<int64_t>(mb) * tile_rows + i;
+  const int col = nb * BN + c;
+  if (row >= M || col >= N) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < work.split; ++sp) {
+    const float4 v = *reinterpret_cast<const float4*>(
+        ws + (static_cast<int64_t>(r * work.split + sp) * tile_rows + i) * BN + c);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+  if (OUT_BF16) {
+    uint16_t* crow = reinterpret_cast<uint16_t*>(Cptr) + row * ldc;
+    const uint32_t lo = cvt_bf16x2(a[0], a[1]), hi = cvt_bf16x2(a[2], a[3]);
+    if (col + 3 < N) {
+      *reinterpret_cast<uint2*>(crow + col) = make_uint2(lo, hi);
+    } else {
+      const uint32_t w[2] = {lo, hi};
+      for (int e = 0; e < 4 && col + e < N; ++e)
+        crow[col + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+    }
+  } else {
+    float* crow = reinterpret_cast<float*>(Cptr) + row * ldc;
+    if (col + 3 < N) {
+      *reinterpret_cast<float4*>(crow + col) = acc;
+    } else {
+      for (int e = 0; e < 4 && col + e < N; ++e) crow[col + e] = a[e];
+    }
   }
 }
 
@@ -519,10 +617,41 @@ int sm_count() {
   return n;
 }
 
+// How the tiles of one GEMM are laid on the clusters.  Whole waves of tiles
+// run as whole tiles; the tiles of a last, partial wave (or of a problem with
+// fewer tiles than clusters) are split into `split` K ranges so that the idle
+// clusters share their work, provided a workspace for the fp32 partials is
+// given.  split = 1: no splitting.
+struct SplitPlan {
+  int clusters, full_tiles, split, rem;
+  size_t ws_bytes;
+};
+
+SplitPlan plan_split(int64_t M, int64_t N, int64_t K, int kps, bool use_split) {
+  const int cg = (M > BM) ? 2 : 1;
+  const int64_t tiles = ((M + BM * cg - 1) / (BM * cg)) * ((N + BN - 1) / BN);
+  const int maxc = sm_count() / cg;
+  const int num_kb = static_cast<int>((K + kps - 1) / kps);
+  SplitPlan p{static_cast<int>(tiles < maxc ? tiles : maxc), static_cast<int>(tiles), 1, 0, 0};
+  if (!use_split || tiles == 0) return p;
+  const int64_t full = (tiles / maxc) * maxc;
+  const int rem = static_cast<int>(tiles - full);
+  int sp = rem ? maxc / rem : 1;
+  if (sp > 4) sp = 4;                          // bound the partial traffic
+  if (sp > num_kb / 2) sp = num_kb / 2;        // at least 2 stages per range
+  if (sp < 2) return p;
+  p.clusters = maxc;
+  p.full_tiles = static_cast<int>(full);
+  p.split = sp;
+  p.rem = rem;
+  p.ws_bytes = static_cast<size_t>(rem) * sp * (BM * cg) * BN * sizeof(float);
+  return p;
+}
+
 template <int KIND, int CG, int STAGES, int KSUB, int OUT_BF16>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                 const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
-                cudaStream_t st) {
+                const SplitPlan& plan, float* ws, cudaStream_t st) {
   using L = Smem<KIND, CG, STAGES, KSUB>;
   auto kern = gemm_kernel<KIND, CG, STAGES, KSUB, OUT_BF16>;
   static bool attr_set[64] = {};
@@ -534,11 +663,8 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
-  const int tiles = ((M + BM * CG - 1) / (BM * CG)) * ((N + BN - 1) / BN);
-  const int max_clusters = sm_count() / CG;
-  const int clusters = tiles < max_clusters ? tiles : max_clusters;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::ALLOC;
   cfg.stream = st;
@@ -549,7 +675,15 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, C, ldc, M, N, K);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, C, ldc, M, N, K, ws, plan.full_tiles,
+                         plan.split);
+  if (e != cudaSuccess || plan.split < 2) return e;
+  WorkList work;
+  work.init((M + BM * CG - 1) / (BM * CG), (N + BN - 1) / BN,
+            (K + KT<KIND, KSUB>::KPS - 1) / KT<KIND, KSUB>::KPS, plan.full_tiles, plan.split);
+  dim3 grid(static_cast<unsigned>(plan.rem), BM * CG / 4);
+  reduce_partials_kernel<OUT_BF16><<<grid, 256, 0, st>>>(ws, C, ldc, M, N, work, BM * CG);
+  return cudaGetLastError();
 }
 
 // K sub-tiles per stage and ring depth; the ring holds the same bytes either
@@ -562,21 +696,40 @@ constexpr int STAGES_CG1 = 4;
 template <int KIND, int OUT_BF16>
 cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                      const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
-                     cudaStream_t st) {
+                     const SplitPlan& plan, float* ws, cudaStream_t st) {
   if (M > BM)
-    return run<KIND, 2, STAGES_CG2, KSUB_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
-  return run<KIND, 1, STAGES_CG1, KSUB_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, st);
+    return run<KIND, 2, STAGES_CG2, KSUB_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K,
+                                                       plan, ws, st);
+  return run<KIND, 1, STAGES_CG1, KSUB_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, plan,
+                                                     ws, st);
+}
+
+// K elements per stage of each kind (KSUB is the same for both CTA groups)
+int stage_k(int kind) {
+  static_assert(KSUB_CG1 == KSUB_CG2, "one K per stage for both CTA groups");
+  return kind == KIND_MXF4 ? KT<KIND_MXF4, KSUB_CG2>::KPS
+                           : kind == KIND_MXF8 ? KT<KIND_MXF8, KSUB_CG2>::KPS
+                                               : KT<KIND_F16, KSUB_CG2>::KPS;
 }
 
 }  // namespace
 
+size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const int k = (kind == FMT_E4M3) ? KIND_MXF8 : (kind == FMT_E2M1) ? KIND_MXF4 : KIND_F16;
+  return plan_split(M, N, K, stage_k(k), true).ws_bytes;
+}
+
 cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
                            const void* b_data, const uint8_t* b_sf, void* C,
                            int c_dtype, int64_t ldc, int64_t M, int64_t N,
-                           int64_t K, cudaStream_t st) {
+                           int64_t K, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   const int eb = (c_dtype == DT_BF16) ? 2 : 4;
   if (K == 0) return launch_zero_fill(C, M, N, ldc, eb, st);
+  const int kind = (fmt == FMT_E4M3) ? KIND_MXF8 : KIND_MXF4;
+  SplitPlan plan = plan_split(M, N, K, stage_k(kind), ws != nullptr);
+  if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = plan_split(M, N, K, stage_k(kind), false);
   const uint64_t kbytes = (fmt == FMT_E4M3) ? K : K / 2;
   // scale atoms per stage of the configuration dispatch() picks
   const bool pair = M > BM;
@@ -584,7 +737,7 @@ cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
                      ? (pair ? KT<KIND_MXF8, KSUB_CG2>::CK : KT<KIND_MXF8, KSUB_CG1>::CK)
                      : (pair ? KT<KIND_MXF4, KSUB_CG2>::CK : KT<KIND_MXF4, KSUB_CG1>::CK);
   // one TMA box of B is this CTA's half of the N tile when M > BM
-  const uint32_t b_rows = (M > BM) ? BN / 2 : BN;
+  const uint32_t b_rows = pair ? BN / 2 : BN;
   CUtensorMap ta, tb, tsa, tsb;
   if (!make_tmap(&ta, a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, M, kbytes, 128, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -593,19 +746,26 @@ cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
       !make_sf_tmap(&tsa, a_sf, M, K, ck) || !make_sf_tmap(&tsb, b_sf, N, K, ck))
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  float* w = static_cast<float*>(ws);
   if (fmt == FMT_E4M3) {
-    if (c_dtype == DT_BF16) return dispatch<KIND_MXF8, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
-    return dispatch<KIND_MXF8, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
+    if (c_dtype == DT_BF16)
+      return dispatch<KIND_MXF8, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
+    return dispatch<KIND_MXF8, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
   }
-  if (c_dtype == DT_BF16) return dispatch<KIND_MXF4, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
-  return dispatch<KIND_MXF4, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, st);
+  if (c_dtype == DT_BF16)
+    return dispatch<KIND_MXF4, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
+  return dispatch<KIND_MXF4, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
 }
 
 cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
                             int64_t M, int64_t N, int64_t K, int64_t lda,
-                            int64_t ldb, int64_t ldc, cudaStream_t st) {
+                            int64_t ldb, int64_t ldc, void* ws, size_t ws_bytes,
+                            cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0) return launch_zero_fill(C, M, N, ldc, 4, st);
+  SplitPlan plan = plan_split(M, N, K, stage_k(KIND_F16), ws != nullptr);
+  if (plan.split > 1 && ws_bytes < plan.ws_bytes)
+    plan = plan_split(M, N, K, stage_k(KIND_F16), false);
   const CUtensorMapDataType dt = (ab_dtype == DT_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
@@ -613,9 +773,11 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
       !make_tmap(&tb, B, dt, 2, N, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  float* w = static_cast<float*>(ws);
   // the scale maps are unused by the 16-bit kinds
-  if (ab_dtype == DT_BF16) return dispatch<KIND_BF16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, st);
-  return dispatch<KIND_F16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, st);
+  if (ab_dtype == DT_BF16)
+    return dispatch<KIND_BF16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, st);
+  return dispatch<KIND_F16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, st);
 }
 
 unsigned fetch_and_clear_status_gemm(cudaError_t* err) {

@@ -163,6 +163,33 @@ mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype,
                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                    int64_t ldc, void* stream);
 
+/*
+ * K-split variants.  When a problem's tiles leave clusters of SMs idle (a last,
+ * partial wave of tiles, or fewer tiles than cluster slots), these calls
+ * split the affected tiles along K across the idle clusters: each part writes
+ * its fp32 partial tile into the workspace and a second kernel adds the parts
+ * in a fixed order (so results do not depend on timing) and writes C.  The
+ * sum is grouped differently from the unsplit call, so the two can differ in
+ * the last bits; both are within the same accumulation bound.
+ *
+ *   workspace        device, 16-byte aligned, caller-owned scratch of at
+ *                    least *_workspace_bytes() bytes for the problem; its
+ *                    contents on entry do not matter and are garbage after.
+ *                    NULL or a smaller size: the call runs unsplit.
+ *   other arguments  as for mx_gemm / gemm_f16.
+ * *_workspace_bytes returns 0 when the problem is not split (or on bad
+ * arguments, or without a compute capability 10.3 device).
+ */
+size_t mx_gemm_workspace_bytes(int32_t fmt, int64_t M, int64_t N, int64_t K);
+mx_status mx_gemm_splitk(const mx_tensor* A, const mx_tensor* B, void* C,
+                         int32_t c_dtype, int64_t ldc, void* workspace,
+                         size_t workspace_bytes, void* stream);
+size_t gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K);
+mx_status gemm_f16_splitk(const void* A, const void* B, float* C,
+                          int32_t ab_dtype, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Synchronize the stream, then return (and clear) the first error recorded
  * by a kernel of this library on the current device: MX_OK,
  * MX_ERR_TIMEOUT, or MX_ERR_CUDA if the synchronization itself failed. */
