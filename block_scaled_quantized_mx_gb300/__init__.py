@@ -31,7 +31,8 @@ STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
 
 EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
            "gemm_f16", "mx_gemm_workspace_bytes", "mx_gemm_splitk",
-           "gemm_f16_workspace_bytes", "gemm_f16_splitk", "mx_last_error",
+           "gemm_f16_workspace_bytes", "gemm_f16_splitk",
+           "mx_gemm_splitk_noalloc", "mx_last_error",
            "mx_selftest_wait_timeout", "mx_scales_to_rowmajor",
            "mx_status_string", "mx_version")
 
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_splitk.restype = i32
     L.gemm_f16_splitk.argtypes = [p, p, p, i32, i64, i64, i64, i64, i64, i64,
                                   p, sz, p]
+    L.mx_gemm_splitk_noalloc.restype = i32
+    L.mx_gemm_splitk_noalloc.argtypes = [pt, pt, p, i32, i64, p]
     L.mx_last_error.restype = i32
     L.mx_last_error.argtypes = [p]
     L.mx_selftest_wait_timeout.restype = i32

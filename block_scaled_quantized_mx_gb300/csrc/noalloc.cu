@@ -1,0 +1,73 @@
+// noalloc.cu -- mx_gemm_splitk_noalloc: the K-split MX GEMM for callers that
+// cannot allocate device memory.
+//
+// mx_gemm_splitk needs a scratch buffer for the fp32 partial tiles of the
+// split.  Some callers cannot hand one over: code that owns only the operand
+// and result pointers (a plugin or operator interface with no workspace
+// argument), and processes whose device memory is all reserved up front by a
+// framework's caching allocator or by a fixed memory budget, where a call to
+// cudaMalloc would fail or would bypass that allocator's accounting.  This
+// entry point takes its scratch from a fixed array in the library's own
+// device memory instead, so it allocates nothing.
+//
+// The array lives as long as the process: every GPU on which this module has
+// been loaded (at the latest on the first call there) keeps its 24 MiB until
+// exit.  All calls share it.
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "mx.h"
+
+namespace {
+
+// 24 MiB.  The split never needs more than one fp32 tile of 256 x 256 per
+// cluster of two SMs (76 x 256 KiB ~ 19 MiB on a 152-SM GB300); a problem
+// that would need more is rejected with MX_ERR_SHAPE.
+constexpr size_t kScratchBytes = size_t{24} << 20;
+
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_ptr[64] = {};   // device address of g_scratch, per device ordinal
+
+// The device address of g_scratch on the current device.  The host-side name
+// g_scratch is only a stand-in and must never reach a kernel; the address is
+// looked up once per device, with that device current, and cached.
+mx_status scratch_on_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MX_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess || p == nullptr) return MX_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return MX_OK;
+}
+
+}  // namespace
+
+#pragma GCC visibility push(default)
+extern "C" {
+
+mx_status mx_gemm_splitk_noalloc(const mx_tensor* A, const mx_tensor* B, void* C,
+                                 int32_t c_dtype, int64_t ldc, void* stream) {
+  if (!A || !B) return MX_ERR_INVALID_ARG;
+  if (A->fmt == B->fmt && A->K == B->K && A->outer > 0 && B->outer > 0 && A->K > 0) {
+    const size_t need = mx_gemm_workspace_bytes(A->fmt, A->outer, B->outer, A->K);
+    if (need > kScratchBytes) return MX_ERR_SHAPE;
+  }
+  void* scratch = nullptr;
+  const mx_status s = scratch_on_current_device(&scratch);
+  if (s != MX_OK) return s;
+  // The partial tiles are written in full before they are read, within this
+  // call, so nothing in the scratch has to start at zero.
+  return mx_gemm_splitk(A, B, C, c_dtype, ldc, scratch, kScratchBytes, stream);
+}
+
+}  // extern "C"
+#pragma GCC visibility pop

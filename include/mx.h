@@ -190,6 +190,34 @@ mx_status gemm_f16_splitk(const void* A, const void* B, float* C,
                           int64_t lda, int64_t ldb, int64_t ldc, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/*
+ * mx_gemm_splitk_noalloc -- mx_gemm_splitk for callers that cannot allocate
+ * device memory: the split's scratch comes from a fixed 24 MiB array inside
+ * the library instead of a caller-provided workspace.  The pages have no
+ * counterpart to this call.
+ *
+ * Who needs it: code that sees only the operand and result pointers (an
+ * operator or plugin interface with no workspace argument) and processes
+ * whose device memory is reserved in advance by a framework's caching
+ * allocator or a fixed budget, where a library cudaMalloc would fail or
+ * escape the allocator's accounting.  This call makes no allocation at all.
+ *
+ *   A, B, C, c_dtype, ldc, stream   as for mx_gemm.
+ * Returns MX_ERR_SHAPE when the problem's split would need more than the
+ * 24 MiB (mx_gemm_workspace_bytes() > 24 MiB; not reachable on a 152-SM
+ * GB300, where the split needs at most about 19 MiB).
+ *
+ * The array is shared by every call in the process: two calls whose
+ * executions overlap on the GPU (different streams, or different host
+ * threads) race on it and give wrong results; serialize them.  Each GPU on
+ * which the library's module has been loaded keeps the 24 MiB until the
+ * process exits.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture on that device.
+ */
+mx_status mx_gemm_splitk_noalloc(const mx_tensor* A, const mx_tensor* B, void* C,
+                                 int32_t c_dtype, int64_t ldc, void* stream);
+
 /* Synchronize the stream, then return (and clear) the first error recorded
  * by a kernel of this library on the current device: MX_OK,
  * MX_ERR_TIMEOUT, or MX_ERR_CUDA if the synchronization itself failed. */
