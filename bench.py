@@ -303,35 +303,72 @@ def run_ours(args, rank, world, local_rank):
         extra["quantize_b_frac_hbm"] = extra["quantize_b_gbs"] / hbm
 
     # ---- end to end through the C ABI with host buffers
+    # Every step copies its fp32 inputs from pinned host memory and its
+    # result back, inside the timed region.  Steps are pipelined on three
+    # streams (copy in, compute, copy out) with double-buffered device
+    # buffers, so step i+1's inputs stream in while step i computes and
+    # copies out: the host link, not the GPU, sets the pace.
     e2e = None
     if not args.no_e2e:
         hA = A.pin_memory()
         hB = B.pin_memory()
-        hC = torch.empty((c.M, c.N), dtype=out_dt).pin_memory()
+        hC = [torch.empty((c.M, c.N), dtype=out_dt).pin_memory() for _ in range(2)]
+        dAs = [dA, torch.empty_like(dA)]
+        dBs = [dB, torch.empty_like(dB)]
+        Cs = [C, torch.empty_like(C)]
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev), torch.cuda.Stream(dev),
+                              torch.cuda.Stream(dev))
+        ev = {k: [torch.cuda.Event(), torch.cuda.Event()]
+              for k in ("in", "used", "done", "out")}
+        for k in ("used", "out"):
+            for e_ in ev[k]:
+                e_.record(stream)            # buffers start free
 
-        def e2e_step():
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            step()
-            hC.copy_(C, non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            s_in.wait_event(ev["used"][b])       # step i-2 has read dA/dB[b]
+            with torch.cuda.stream(s_in):
+                dAs[b].copy_(hA, non_blocking=True)
+                dBs[b].copy_(hB, non_blocking=True)
+                ev["in"][b].record(s_in)
+            s_cmp.wait_event(ev["in"][b])
+            s_cmp.wait_event(ev["out"][b])       # step i-2's C[b] is copied out
+            if is_mx:
+                mx.mx_quantize(dAs[b], fmt, out=qa, stream=s_cmp)
+                mx.mx_quantize(dBs[b], fmt, k_strided=True, out=qb, stream=s_cmp)
+                ev["used"][b].record(s_cmp)
+                mx.mx_gemm(qa, qb, out_dtype=out_dt, out=Cs[b], workspace=ws,
+                           stream=s_cmp)
+            else:
+                mx.gemm_f16(dAs[b], dBs[b], out=Cs[b], workspace=ws,
+                            stream=s_cmp)
+                ev["used"][b].record(s_cmp)
+            ev["done"][b].record(s_cmp)
+            s_out.wait_event(ev["done"][b])
+            with torch.cuda.stream(s_out):
+                hC[b].copy_(Cs[b], non_blocking=True)
+                ev["out"][b].record(s_out)
 
-        for _ in range(max(1, args.warmup // 2)):
-            e2e_step()
+        for i in range(max(2, args.warmup // 2)):
+            e2e_step(i)
         barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, args.e2e_steps)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
+        n_e2e = max(2, args.e2e_steps)
+        t_start = time.perf_counter()
+        for i in range(n_e2e):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        ems = (time.perf_counter() - t_start) * 1e3 / n_e2e
         barrier()
-        ems = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        assert mx.mx_last_error() == 0
+        ems = max_over_ranks(ems, world, dev)
         e2e = {"value": job_throughput(flops_of(c), world, ems),
                "unit": "TFLOP/s", "ms_per_step": ems,
                "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
                                          hB.numel() * hB.element_size()),
-               "d2h_bytes_per_step": int(hC.numel() * hC.element_size())}
+               "d2h_bytes_per_step": int(hC[0].numel() * hC[0].element_size()),
+               "timing": "host wall clock around n steps, synchronized",
+               "pipelining": "3 streams (copy in / compute / copy out), "
+                             "double-buffered device inputs and outputs"}
 
     others = {}
     if not args.no_others and rank == 0:
