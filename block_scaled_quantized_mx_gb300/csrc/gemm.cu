@@ -328,7 +328,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       for (int w = cluster_id; w < work.total && ok; w += num_clusters, ++tc) {
         int mb, nb, kb0, kb1, unit;
         work.item(w, mb, nb, kb0, kb1, unit);
-        if (!mbar_wait(bar_acc_empty, (tc & 1u) ^ 1u, abort)) {
+        // the hand-off is short and on the critical path: spin
+        if (!mbar_wait_spin(bar_acc_empty, (tc & 1u) ^ 1u, abort)) {
           record_timeout(abort, 2);
           break;
         }
@@ -409,7 +410,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (CG == 2)
+        if (CG == 2 && !leader)
           mbar_arrive_cluster(acc_empty0);
         else
           mbar_arrive(bar_acc_empty);
