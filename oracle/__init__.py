@@ -29,6 +29,7 @@ import numpy as np
 
 E4M3 = 1
 E2M1 = 2
+E5M2 = 3
 F16 = 2
 BF16 = 1
 
@@ -65,6 +66,10 @@ def _load():
         p = ctypes.c_void_p
         lib.mxo_decode_e4m3.restype = dbl
         lib.mxo_decode_e4m3.argtypes = [u8]
+        lib.mxo_decode_e5m2.restype = dbl
+        lib.mxo_decode_e5m2.argtypes = [u8]
+        lib.mxo_encode_e5m2.restype = u8
+        lib.mxo_encode_e5m2.argtypes = [dbl]
         lib.mxo_decode_e2m1.restype = dbl
         lib.mxo_decode_e2m1.argtypes = [u8]
         lib.mxo_decode_ue8m0.restype = dbl
@@ -82,8 +87,8 @@ def _load():
         lib.mxo_quantize.restype = None
         lib.mxo_quantize.argtypes = [p, i64, i64, i64, i64, i32, p, p]
         lib.mxo_gemm_mx.restype = None
-        lib.mxo_gemm_mx.argtypes = [p, p, p, p, i64, i64, i64, i32, p, i64,
-                                    p, p]
+        lib.mxo_gemm_mx.argtypes = [p, p, p, p, i64, i64, i64, i32, i32, p,
+                                    i64, p, p]
         lib.mxo_gemm_f16.restype = None
         lib.mxo_gemm_f16.argtypes = [p, p, i64, i64, i64, i32, p, i64, p, p]
         lib.mxo_num_threads.restype = i32
@@ -102,6 +107,14 @@ def _ptr(a: np.ndarray) -> int:
 
 def decode_e4m3(code: int) -> float:
     return _load().mxo_decode_e4m3(int(code) & 0xFF)
+
+
+def decode_e5m2(code: int) -> float:
+    return _load().mxo_decode_e5m2(int(code) & 0xFF)
+
+
+def encode_e5m2(v: float) -> int:
+    return int(_load().mxo_encode_e5m2(float(v)))
 
 
 def decode_e2m1(code: int) -> float:
@@ -133,9 +146,12 @@ def floor_log2_f32(a: float) -> int:
 
 
 def decode_table(fmt: int) -> np.ndarray:
-    """float64 value of every code: 256 entries for E4M3, 16 for E2M1."""
+    """float64 value of every code: 256 entries for E4M3 / E5M2, 16 for
+    E2M1."""
     if fmt == E4M3:
         return np.array([decode_e4m3(c) for c in range(256)])
+    if fmt == E5M2:
+        return np.array([decode_e5m2(c) for c in range(256)])
     return np.array([decode_e2m1(c) for c in range(16)])
 
 
@@ -183,11 +199,13 @@ def _rows_arg(rows, M):
     return r, int(r.size)
 
 
-def gemm_mx(codesA, scalesA, codesB, scalesB, fmt: int, rows=None):
+def gemm_mx(codesA, scalesA, codesB, scalesB, fmt: int, rows=None,
+            fmt_b: int | None = None):
     """float64 C = A_mx * B_mx^T and S = sum |products|.
 
     codesA M x K, scalesA M x K/32, codesB N x K, scalesB N x K/32 (both
-    operands K-major, as returned by ``quantize``).  ``rows`` restricts the
+    operands K-major, as returned by ``quantize``).  ``fmt`` is A's element
+    format and B's too unless ``fmt_b`` is given.  ``rows`` restricts the
     evaluation to those rows of A (C and S then have len(rows) rows).
     """
     lib = _load()
@@ -203,6 +221,7 @@ def gemm_mx(codesA, scalesA, codesB, scalesB, fmt: int, rows=None):
     C = np.empty((nr, N), dtype=np.float64)
     S = np.empty((nr, N), dtype=np.float64)
     lib.mxo_gemm_mx(_ptr(cA), _ptr(sA), _ptr(cB), _ptr(sB), M, N, K, fmt,
+                    fmt if fmt_b is None else fmt_b,
                     None if r is None else _ptr(r), nr, _ptr(C), _ptr(S))
     return C, S
 

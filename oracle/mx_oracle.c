@@ -17,9 +17,10 @@
  *    tensor is an E4M3 data plane plus a UE8M0 ("FP8 E8M0") scale plane with
  *    block factors {32, 1}: one scale per 32 consecutive elements of the
  *    innermost (K) dimension.
- *  - The OCP Microscaling (MX) v1.0 definitions of E4M3, E2M1 and UE8M0 and
- *    of the conversion rule: X = 2^(floor(log2(amax)) - emax_elem), elements
- *    rounded to nearest-even and saturated.
+ *  - The OCP Microscaling (MX) v1.0 definitions of E4M3, E5M2, E2M1 and UE8M0
+ *    and of the conversion rule: X = 2^(floor(log2(amax)) - emax_elem),
+ *    elements rounded to nearest-even and saturated (E5M2 included: an MX
+ *    block never encodes an infinity, only its scale can say NaN).
  *
  * Every arithmetic step is done in double, where all code values, all scales
  * and all products of two scaled codes are exact.  Formats are decoded from
@@ -37,6 +38,7 @@
 
 #define MXO_E4M3 1
 #define MXO_E2M1 2
+#define MXO_E5M2 3
 #define MXO_F16 2
 #define MXO_BF16 1
 
@@ -56,6 +58,21 @@ double mxo_decode_e4m3(uint8_t b)
         mag = ldexp((double)m, -9);                 /* m/8 * 2^(1-7) */
     else
         mag = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 mantissa bits; exponent 31
+ * holds infinity (mantissa 0) and NaN; the largest finite magnitude is
+ * 1.75 * 2^15 = 57344. */
+double mxo_decode_e5m2(uint8_t b)
+{
+    int s = (b >> 7) & 1, e = (b >> 2) & 31, m = b & 3;
+    double mag;
+    if (e == 31) return m ? NAN : (s ? -INFINITY : INFINITY);
+    if (e == 0)
+        mag = ldexp((double)m, -16);                /* m/4 * 2^(1-15) */
+    else
+        mag = ldexp(1.0 + m / 4.0, e - 15);
     return s ? -mag : mag;
 }
 
@@ -110,9 +127,11 @@ double mxo_decode_bf16(uint16_t h)
 /* ------------------------------------------------------------------------ */
 
 /* Non-negative codes of a format in increasing order of value, finite only.
- * For E4M3 these are 0x00..0x7E, for E2M1 0x0..0x7.  Value is increasing in
- * the code for both formats, so the code list is its own sorted order. */
+ * For E4M3 these are 0x00..0x7E, for E5M2 0x00..0x7B, for E2M1 0x0..0x7.
+ * Value is increasing in the code for all three, so the code list is its own
+ * sorted order. */
 static double e4m3_pos[127];
+static double e5m2_pos[124];
 static double e2m1_pos[8];
 static int tables_ready = 0;
 
@@ -120,6 +139,7 @@ static void build_tables(void)
 {
     if (tables_ready) return;
     for (int c = 0; c < 127; ++c) e4m3_pos[c] = mxo_decode_e4m3((uint8_t)c);
+    for (int c = 0; c < 124; ++c) e5m2_pos[c] = mxo_decode_e5m2((uint8_t)c);
     for (int c = 0; c < 8; ++c) e2m1_pos[c] = mxo_decode_e2m1((uint8_t)c);
     tables_ready = 1;
 }
@@ -149,6 +169,17 @@ uint8_t mxo_encode_e4m3(double v)
     return (uint8_t)(c | (neg << 7));
 }
 
+/* Finite codes only: values beyond 57344 saturate to it, as the scaled
+ * elements of an MX block are converted with saturation. */
+uint8_t mxo_encode_e5m2(double v)
+{
+    build_tables();
+    if (isnan(v)) return 0x7F;
+    int neg = signbit(v) ? 1 : 0;
+    int c = nearest_code(e5m2_pos, 124, fabs(v));
+    return (uint8_t)(c | (neg << 7));
+}
+
 uint8_t mxo_encode_e2m1(double v)
 {
     build_tables();
@@ -174,14 +205,14 @@ static int floor_log2(double a)
 int mxo_floor_log2_f32(float a) { return floor_log2((double)a); }
 
 /* Quantize one block of 32 values.  emax is the exponent of the element
- * format's largest power of two (8 for E4M3, 2 for E2M1).  Writes 32 codes
- * (one per byte, unpacked) and returns the UE8M0 scale code.
+ * format's largest power of two (8 for E4M3, 15 for E5M2, 2 for E2M1).
+ * Writes 32 codes (one per byte, unpacked) and returns the UE8M0 scale code.
  *   amax = 0          -> scale code 0 (2^-127), all elements +-0
  *   NaN/Inf in block  -> scale code 0xFF (NaN); element codes are then
  *                        meaningless and are written as the encoding of 0. */
 static uint8_t quantize_block(const double x[32], int fmt, uint8_t codes[32])
 {
-    int emax = (fmt == MXO_E4M3) ? 8 : 2;
+    int emax = (fmt == MXO_E4M3) ? 8 : (fmt == MXO_E5M2) ? 15 : 2;
     double amax = 0.0;
     int nonfinite = 0;
     for (int i = 0; i < 32; ++i) {
@@ -202,7 +233,8 @@ static uint8_t quantize_block(const double x[32], int fmt, uint8_t codes[32])
     }
     for (int i = 0; i < 32; ++i) {
         double q = ldexp(x[i], -es);            /* exact in double */
-        codes[i] = (fmt == MXO_E4M3) ? mxo_encode_e4m3(q) : mxo_encode_e2m1(q);
+        codes[i] = (fmt == MXO_E4M3) ? mxo_encode_e4m3(q)
+                   : (fmt == MXO_E5M2) ? mxo_encode_e5m2(q) : mxo_encode_e2m1(q);
     }
     return (uint8_t)(es + 127);
 }
@@ -233,22 +265,33 @@ void mxo_quantize(const float* src, int64_t rows, int64_t K, int64_t s_row,
 /* GEMMs in float64.                                                          */
 /* ------------------------------------------------------------------------ */
 
+/* Value of code c of an element format (E2M1 codes in the low nibble). */
+static double decode_fmt(int fmt, int c)
+{
+    return (fmt == MXO_E4M3) ? mxo_decode_e4m3((uint8_t)c)
+           : (fmt == MXO_E5M2) ? mxo_decode_e5m2((uint8_t)c)
+                               : mxo_decode_e2m1((uint8_t)(c & 15));
+}
+
 /* C[i][j] = sum_k (qa_ik * Xa_i,k/32) * (qb_jk * Xb_j,k/32), k ascending,
  * S[i][j] = sum_k |same product|.
- *   codesA  M x K (one code per byte), scalesA M x K/32
- *   codesB  N x K (B stored K-major, i.e. the transpose of the K x N operand)
+ *   codesA  M x K (one code per byte, format fmt_a), scalesA M x K/32
+ *   codesB  N x K (format fmt_b; B stored K-major, i.e. the transpose of the
+ *           K x N operand)
  *   rows    optional list of nrows row indices of A to evaluate (NULL: all M,
  *           nrows must equal M); C and S are nrows x N. */
+
 void mxo_gemm_mx(const uint8_t* codesA, const uint8_t* scalesA,
                  const uint8_t* codesB, const uint8_t* scalesB,
-                 int64_t M, int64_t N, int64_t K, int fmt,
+                 int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b,
                  const int64_t* rows, int64_t nrows, double* C, double* S)
 {
     (void)M;
-    double tab[256];
-    for (int c = 0; c < 256; ++c)
-        tab[c] = (fmt == MXO_E4M3) ? mxo_decode_e4m3((uint8_t)c)
-                                   : mxo_decode_e2m1((uint8_t)(c & 15));
+    double tab[256], tabb[256];
+    for (int c = 0; c < 256; ++c) {
+        tab[c] = decode_fmt(fmt_a, c);
+        tabb[c] = decode_fmt(fmt_b, c);
+    }
     int64_t nb = K / 32;
 #pragma omp parallel
     {
@@ -264,7 +307,7 @@ void mxo_gemm_mx(const uint8_t* codesA, const uint8_t* scalesA,
                 for (int64_t b = 0; b < nb; ++b) {
                     double xb = mxo_decode_ue8m0(scalesB[j * nb + b]);
                     for (int64_t k = b * 32; k < b * 32 + 32; ++k) {
-                        double p = a[k] * (tab[codesB[j * K + k]] * xb);
+                        double p = a[k] * (tabb[codesB[j * K + k]] * xb);
                         c += p;
                         s += fabs(p);
                     }

@@ -38,6 +38,15 @@ def _torch_e4m3_table():
     return u.view(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
+def _torch_e5m2_table():
+    u = torch.arange(256, dtype=torch.uint8)
+    return u.view(torch.float8_e5m2).to(torch.float64).numpy()
+
+
+def _e5m2_finite_code(c):
+    return (c & 0x7F) < 0x7C
+
+
 # Magnitudes of E2M1 codes 0..7 as listed in the OCP MX v1.0 format table.
 E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
@@ -66,6 +75,28 @@ def test_e4m3_landmarks():
     finite = [oracle.decode_e4m3(c) for c in range(0x7F)]
     assert all(a < b for a, b in zip(finite, finite[1:]))   # monotone
     assert len(set(finite)) == 127
+
+
+def test_e5m2_decode_all_codes_match_torch():
+    ref = _torch_e5m2_table()
+    ours = oracle.decode_table(oracle.E5M2)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert np.array_equal(ref[~nan], ours[~nan])        # +-Inf included
+    assert math.copysign(1.0, ours[0x80]) == -1.0
+
+
+def test_e5m2_landmarks():
+    assert oracle.decode_e5m2(0x7B) == 57344.0         # 1.75 * 2^15
+    assert oracle.decode_e5m2(0x7C) == math.inf
+    assert oracle.decode_e5m2(0xFC) == -math.inf
+    for c in (0x7D, 0x7E, 0x7F, 0xFF):
+        assert math.isnan(oracle.decode_e5m2(c))
+    assert oracle.decode_e5m2(0x01) == 2.0 ** -16      # smallest subnormal
+    assert oracle.decode_e5m2(0x03) == 0.75 * 2.0 ** -14
+    assert oracle.decode_e5m2(0x04) == 2.0 ** -14      # smallest normal
+    assert oracle.decode_e5m2(0x3C) == 1.0
+    assert oracle.decode_e5m2(0xBE) == -1.5
 
 
 def test_e2m1_decode_table():
@@ -144,6 +175,38 @@ def test_encode_e4m3_roundtrip_and_signed_zero():
     assert oracle.encode_e4m3(3 * 2.0 ** -10) == 0x02   # tie 1 vs 2 -> 2
 
 
+def test_encode_e5m2_matches_torch_inside_range():
+    table = _torch_e5m2_table()
+    finite = np.sort(table[:0x7C])
+    mids = (finite[:-1] + finite[1:]) / 2
+    rng = np.random.default_rng(12)
+    vals = np.concatenate([finite, -finite, mids, -mids,
+                           rng.uniform(-61000, 61000, 20000),
+                           rng.uniform(-2e-4, 2e-4, 5000),
+                           mids * (1 + 2 ** -40), mids * (1 - 2 ** -40)])
+    vals = vals[np.abs(vals) < 61440]              # torch turns >= 61440 to Inf
+    vals = vals.astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.float8_e5m2).view(
+        torch.uint8).numpy()
+    ours = np.array([oracle.encode_e5m2(float(v)) for v in vals],
+                    dtype=np.uint8)
+    assert np.array_equal(ours, ref)
+
+
+def test_encode_e5m2_saturates_and_roundtrips():
+    # Beyond the range an MX element saturates instead of becoming Inf.
+    for v, code in ((61440.0, 0x7B), (1e9, 0x7B), (math.inf, 0x7B),
+                    (-65536.0, 0xFB), (57344.0, 0x7B),
+                    (53248.0, 0x7A),                 # tie 1.5|1.75 -> even
+                    (55296.0, 0x7B), (50000.0, 0x7A)):
+        assert oracle.encode_e5m2(v) == code, v
+    for c in range(256):
+        if _e5m2_finite_code(c):
+            assert oracle.encode_e5m2(oracle.decode_e5m2(c)) == c
+    assert oracle.encode_e5m2(2.0 ** -17) == 0x00    # tie 0 | 2^-16 -> even
+    assert oracle.encode_e5m2(3 * 2.0 ** -17) == 0x02
+
+
 def test_encode_e2m1_hand_values():
     cases = {6.9: 0x7, 100.0: 0x7, 0.25: 0x0, 0.75: 0x2, 2.5: 0x4,
              5.0: 0x6, 1.25: 0x2, 1.75: 0x4, 3.5: 0x6, 0.2: 0x0,
@@ -158,8 +221,10 @@ def test_encode_nearest_by_brute_force():
     checked by scanning every code through the torch / hand tables."""
     rng = np.random.default_rng(3)
     t8 = _torch_e4m3_table()[:0x7F]
+    t5 = _torch_e5m2_table()[:0x7C]
     t4 = np.array(E2M1_MAGNITUDES)
     for table, enc, vmax in ((t8, oracle.encode_e4m3, 448.0),
+                             (t5, oracle.encode_e5m2, 57344.0),
                              (t4, oracle.encode_e2m1, 6.0)):
         for v in np.concatenate([rng.uniform(0, vmax * 1.1, 3000),
                                  rng.uniform(0, vmax / 64, 1000)]):
@@ -207,6 +272,18 @@ def test_scale_rule_hand_values():
     assert _qblock([float("inf")], oracle.E2M1)[1] == 0xFF
 
 
+def test_scale_rule_hand_values_e5m2():
+    assert _qblock([1.0], oracle.E5M2)[1] == 112       # 2^(0-15)
+    codes, s = _qblock([1.0, 0.25], oracle.E5M2)
+    assert codes[0] == 0x78 and codes[1] == 0x70       # 2^15, 2^13
+    codes, s = _qblock([1.9], oracle.E5M2)             # 1.9 * 2^15 > 57344
+    assert s == 112 and codes[0] == 0x7B
+    codes, s = _qblock([-3.0e38], oracle.E5M2)
+    # 3e38 = 1.763 * 2^127: significand above 1.75, so it saturates
+    assert s == 127 + 127 - 15 and codes[0] == 0xFB
+    assert _qblock([float("-inf")], oracle.E5M2)[1] == 0xFF
+
+
 def test_floor_log2_from_bits():
     assert oracle.floor_log2_f32(1.0) == 0
     assert oracle.floor_log2_f32(float(np.nextafter(np.float32(2), 0))) == 0
@@ -215,7 +292,7 @@ def test_floor_log2_from_bits():
     assert oracle.floor_log2_f32(float(np.float32(3 * 2.0 ** -140))) == -139
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.E2M1])
 def test_quantize_properties(fmt):
     """Per block: X * 2^emax <= amax < X * 2^(emax+1) unless clamped, and
     every element code is the nearest representable value of x / X."""
@@ -226,9 +303,15 @@ def test_quantize_properties(fmt):
     x[5, 64:96] *= 2.0 ** -120
     x = x.numpy()
     codes, scales = oracle.quantize(x, fmt)
-    emax = 8 if fmt == oracle.E4M3 else 2
-    table = _torch_e4m3_table() if fmt == oracle.E4M3 else \
-        np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+    emax = {oracle.E4M3: 8, oracle.E5M2: 15, oracle.E2M1: 2}[fmt]
+    if fmt == oracle.E4M3:
+        table = _torch_e4m3_table()
+    elif fmt == oracle.E5M2:
+        table = _torch_e5m2_table()
+        table[0x7C:0x80] = np.nan                       # no Inf in an MX block
+        table[0xFC:] = np.nan
+    else:
+        table = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
     for r in range(x.shape[0]):
         for b in range(x.shape[1] // 32):
             blk = x[r, b * 32:(b + 1) * 32].astype(np.float64)
@@ -246,7 +329,7 @@ def test_quantize_properties(fmt):
                     assert abs(got - v) == dist
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.E2M1])
 def test_quantize_k_axis_layouts_agree(fmt):
     g = torch.Generator().manual_seed(8)
     src = torch.randn(64, 96, generator=g).numpy()       # K=64 x outer=96
@@ -263,26 +346,37 @@ def _int_matrix(shape, values, seed):
     return g.choice(values, size=shape).astype(np.float32)
 
 
-@pytest.mark.parametrize("fmt,values", [
-    (oracle.E4M3, np.arange(-14, 15)),
-    (oracle.E2M1, np.array([0, 1, 2, 3, 4, 6, -1, -2, -3, -4, -6]))])
-def test_gemm_mx_integer_matrices_exact(fmt, values):
+E5M2_INTS = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 14, 16])
+E5M2_INTS = np.concatenate([E5M2_INTS, -E5M2_INTS[1:]])
+
+
+@pytest.mark.parametrize("fmt,fmt_b,values,values_b", [
+    (oracle.E4M3, None, np.arange(-14, 15), None),
+    (oracle.E5M2, None, E5M2_INTS, None),
+    (oracle.E4M3, oracle.E5M2, np.arange(-14, 15), E5M2_INTS),
+    (oracle.E5M2, oracle.E4M3, E5M2_INTS, np.arange(-14, 15)),
+    (oracle.E2M1, None, np.array([0, 1, 2, 3, 4, 6, -1, -2, -3, -4, -6]),
+     None)])
+def test_gemm_mx_integer_matrices_exact(fmt, fmt_b, values, values_b):
     """Integer-valued sources whose blocks quantize without loss must give
     exactly the integer product (numpy int64 matmul), for a non-square
-    problem so that a transposed operand would show."""
+    problem so that a transposed operand would show.  E5M2 holds 3
+    significant bits, so its integers are those of the form m * 2^e with
+    m <= 7 (any block maximum up to 16 scales without loss)."""
     M, N, K = 40, 24, 96
     A = _int_matrix((M, K), values, 1)
-    B = _int_matrix((K, N), values, 2)
+    B = _int_matrix((K, N), values if values_b is None else values_b, 2)
+    fb = fmt if fmt_b is None else fmt_b
     ca, sa = oracle.quantize(A, fmt, k_axis=1)
-    cb, sb = oracle.quantize(B, fmt, k_axis=0)
-    C, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
+    cb, sb = oracle.quantize(B, fb, k_axis=0)
+    C, S = oracle.gemm_mx(ca, sa, cb, sb, fmt, fmt_b=fb)
     want = A.astype(np.int64) @ B.astype(np.int64)
     assert np.array_equal(C, want.astype(np.float64))
     assert np.array_equal(S, (np.abs(A).astype(np.int64)
                               @ np.abs(B).astype(np.int64)).astype(float))
     # rows subset evaluates the same rows
     rows = [0, 7, 39]
-    C2, S2 = oracle.gemm_mx(ca, sa, cb, sb, fmt, rows=rows)
+    C2, S2 = oracle.gemm_mx(ca, sa, cb, sb, fmt, rows=rows, fmt_b=fb)
     assert np.array_equal(C2, C[rows]) and np.array_equal(S2, S[rows])
 
 
@@ -302,27 +396,39 @@ def test_gemm_mx_identity():
     assert np.array_equal(C, deq)
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
-def test_gemm_mx_brute_force_rationals(fmt):
+def _random_finite_codes(fmt, shape, g):
+    """Random finite codes of a format and the torch / hand value table."""
+    if fmt == oracle.E4M3:
+        vals = _torch_e4m3_table()
+        c = g.integers(0, 256, shape)
+        c[(c & 0x7F) == 0x7F] = 0x3F
+    elif fmt == oracle.E5M2:
+        vals = _torch_e5m2_table()
+        c = g.integers(0, 256, shape)
+        c[(c & 0x7F) >= 0x7C] = 0x3D
+    else:
+        vals = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+        c = g.integers(0, 16, shape)
+    return c, vals
+
+
+@pytest.mark.parametrize("fmt,fmt_b", [
+    (oracle.E4M3, oracle.E4M3), (oracle.E5M2, oracle.E5M2),
+    (oracle.E4M3, oracle.E5M2), (oracle.E5M2, oracle.E4M3),
+    (oracle.E2M1, oracle.E2M1)])
+def test_gemm_mx_brute_force_rationals(fmt, fmt_b):
     """4 x 4 x 64 random codes with extreme scales: float64 oracle vs the
     exact rational sum (element values from torch / the hand table)."""
     g = np.random.default_rng(21)
     M, N, K = 4, 4, 64
-    if fmt == oracle.E4M3:
-        vals = _torch_e4m3_table()
-        codes_a = g.integers(0, 256, (M, K))
-        codes_b = g.integers(0, 256, (N, K))
-        codes_a[(codes_a & 0x7F) == 0x7F] = 0x3F
-        codes_b[(codes_b & 0x7F) == 0x7F] = 0x41
-    else:
-        vals = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
-        codes_a = g.integers(0, 16, (M, K))
-        codes_b = g.integers(0, 16, (N, K))
+    codes_a, vals = _random_finite_codes(fmt, (M, K), g)
+    codes_b, vals_b = _random_finite_codes(fmt_b, (N, K), g)
     sa = g.integers(0, 255, (M, K // 32))
     sb = g.integers(0, 255, (N, K // 32))
     sa[0, 0], sb[1, 1], sa[2, 1], sb[3, 0] = 0, 254, 1, 253
     C, S = oracle.gemm_mx(codes_a.astype(np.uint8), sa.astype(np.uint8),
-                          codes_b.astype(np.uint8), sb.astype(np.uint8), fmt)
+                          codes_b.astype(np.uint8), sb.astype(np.uint8), fmt,
+                          fmt_b=fmt_b)
     for i in range(M):
         for j in range(N):
             exact = Fraction(0)
@@ -330,7 +436,7 @@ def test_gemm_mx_brute_force_rationals(fmt):
             for k in range(K):
                 a = Fraction(float(vals[codes_a[i, k]])) * \
                     Fraction(2) ** (int(sa[i, k // 32]) - 127)
-                b = Fraction(float(vals[codes_b[j, k]])) * \
+                b = Fraction(float(vals_b[codes_b[j, k]])) * \
                     Fraction(2) ** (int(sb[j, k // 32]) - 127)
                 exact += a * b
                 eabs += abs(a * b)
