@@ -38,7 +38,17 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # nominal dense ratios to bf16: fp8 2x, fp4 6x (2.25 / 4.5 / 13.5 PFLOP/s)
-NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0}
+# dense tensor rate of each kind relative to bf16; an E2M1 operand beside an
+# 8-bit one runs at the FP8 rate
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0,
+                 "mxfp8_e5m2": 2.0, "w4a8": 2.0}
+DTYPE_NAME = {"mxfp8": "e4m3", "mxfp4": "e2m1", "mxfp8_e5m2": "e5m2",
+              "w4a8": "e4m3 x e2m1"}
+
+
+def ws_format(fa, fb):
+    """The format mx_gemm_workspace_bytes takes for an operand pair."""
+    return fa if fa == fb else 1
 
 
 def peaks():
@@ -156,12 +166,13 @@ def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
     dA, dB = A.to(dev), B.to(dev)
     out_dt = torch.bfloat16 if c.out == "bf16" else torch.float32
     C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
-    if c.kind in ("mxfp8", "mxfp4"):
-        fmt = mx.E4M3 if c.kind == "mxfp8" else mx.E2M1
-        qa = mx.mx_quantize(dA, fmt)
-        qb = mx.mx_quantize(dB, fmt, k_strided=True)
+    if workloads.is_mx(c):
+        fa, fb = workloads.formats(c)
+        qa = mx.mx_quantize(dA, fa)
+        qb = mx.mx_quantize(dB, fb, k_strided=True)
         del dA, dB
-        nb = mx.mx_gemm_workspace_bytes(fmt, c.M, c.N, c.K) if splitk else 0
+        nb = (mx.mx_gemm_workspace_bytes(ws_format(fa, fb), c.M, c.N, c.K)
+              if splitk else 0)
         ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
         f = lambda: mx.mx_gemm(qa, qb, out_dtype=out_dt, out=C, workspace=ws)  # noqa
     else:
@@ -189,7 +200,7 @@ def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
 
 def quant_bytes(fmt, rows, K):
     """Algorithmic bytes of one mx_quantize: fp32 in, codes + scales out."""
-    code = rows * K if fmt == 1 else rows * K / 2
+    code = rows * K / 2 if fmt == 2 else rows * K           # E2M1: 4 bits
     return 4.0 * rows * K + code + rows * K / 32
 
 
@@ -204,15 +215,15 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     A, B = workloads.sources(c)
-    is_mx = c.kind in ("mxfp8", "mxfp4")
-    fmt = {"mxfp8": mx.E4M3, "mxfp4": mx.E2M1}.get(c.kind)
+    is_mx = workloads.is_mx(c)
+    fa, fb = workloads.formats(c) if is_mx else (None, None)
     out_dt = torch.bfloat16 if c.out == "bf16" else torch.float32
     dA, dB = A.to(dev), B.to(dev)
     C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
     if is_mx:
-        qa = mx.empty_mx(fmt, c.M, c.K, dev)
-        qb = mx.empty_mx(fmt, c.N, c.K, dev)
-        ws_bytes = mx.mx_gemm_workspace_bytes(fmt, c.M, c.N, c.K)
+        qa = mx.empty_mx(fa, c.M, c.K, dev)
+        qb = mx.empty_mx(fb, c.N, c.K, dev)
+        ws_bytes = mx.mx_gemm_workspace_bytes(ws_format(fa, fb), c.M, c.N, c.K)
     else:
         ws_bytes = mx.gemm_f16_workspace_bytes(c.M, c.N, c.K)
     # scratch for the K-split of the last wave of tiles (allocated here,
@@ -226,10 +237,10 @@ def run_ours(args, rank, world, local_rank):
         if is_mx:
             if ev is not None:
                 ev[0].record(stream)
-            mx.mx_quantize(dA, fmt, out=qa)
+            mx.mx_quantize(dA, fa, out=qa)
             if ev is not None:
                 ev[1].record(stream)
-            mx.mx_quantize(dB, fmt, k_strided=True, out=qb)
+            mx.mx_quantize(dB, fb, k_strided=True, out=qb)
             if ev is not None:
                 ev[2].record(stream)
             mx.mx_gemm(qa, qb, out_dtype=out_dt, out=C, workspace=ws)
@@ -297,8 +308,8 @@ def run_ours(args, rank, world, local_rank):
         qb_ms = statistics.mean(per_kernel[1])
         extra["quantize_a_ms"] = qa_ms
         extra["quantize_b_ms"] = qb_ms
-        extra["quantize_a_gbs"] = quant_bytes(fmt, c.M, c.K) / qa_ms / 1e6
-        extra["quantize_b_gbs"] = quant_bytes(fmt, c.N, c.K) / qb_ms / 1e6
+        extra["quantize_a_gbs"] = quant_bytes(fa, c.M, c.K) / qa_ms / 1e6
+        extra["quantize_b_gbs"] = quant_bytes(fb, c.N, c.K) / qb_ms / 1e6
         extra["quantize_a_frac_hbm"] = extra["quantize_a_gbs"] / hbm
         extra["quantize_b_frac_hbm"] = extra["quantize_b_gbs"] / hbm
 
@@ -334,8 +345,8 @@ def run_ours(args, rank, world, local_rank):
             s_cmp.wait_event(ev["in"][b])
             s_cmp.wait_event(ev["out"][b])       # step i-2's C[b] is copied out
             if is_mx:
-                mx.mx_quantize(dAs[b], fmt, out=qa, stream=s_cmp)
-                mx.mx_quantize(dBs[b], fmt, k_strided=True, out=qb, stream=s_cmp)
+                mx.mx_quantize(dAs[b], fa, out=qa, stream=s_cmp)
+                mx.mx_quantize(dBs[b], fb, k_strided=True, out=qb, stream=s_cmp)
                 ev["used"][b].record(s_cmp)
                 mx.mx_gemm(qa, qb, out_dtype=out_dt, out=Cs[b], workspace=ws,
                            stream=s_cmp)
@@ -394,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
         "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"mxfp8": "e4m3", "mxfp4": "e2m1"}.get(c.kind, c.kind),
+        "dtype": DTYPE_NAME.get(c.kind, c.kind),
         "data": "synthetic (seeded)",
         "config": {"workload": c.name, "M": c.M, "N": c.N, "K": c.K,
                    "out": c.out, "dist": c.dist_a,
@@ -435,14 +446,14 @@ def oracle_sample(c, budget_s: float):
             if time.perf_counter() - t0 > budget_s:
                 break
     else:
-        fmt = oracle.E4M3 if c.kind == "mxfp8" else oracle.E2M1
-        cb, sb = oracle.quantize(B.numpy(), fmt, k_axis=0)
+        fa, fb = workloads.formats(c)
+        cb, sb = oracle.quantize(B.numpy(), fb, k_axis=0)
         An = A.numpy()
         rows = 0
         chunk = 16
         while rows < c.M:
-            ca, sa = oracle.quantize(An[rows:rows + chunk], fmt, k_axis=1)
-            oracle.gemm_mx(ca, sa, cb, sb, fmt)
+            ca, sa = oracle.quantize(An[rows:rows + chunk], fa, k_axis=1)
+            oracle.gemm_mx(ca, sa, cb, sb, fa, fmt_b=fb)
             rows += ca.shape[0]
             if time.perf_counter() - t0 > budget_s:
                 break
@@ -465,7 +476,7 @@ def run_reference(args):
     rows, thr, dt = last
     sample = ("rows of C computed from the fp32 sources: quantize all of B, "
               "then %d rows of A quantized and multiplied (%.1f s per step)"
-              % (rows, dt)) if c.kind in ("mxfp8", "mxfp4") else \
+              % (rows, dt)) if workloads.is_mx(c) else \
         ("%d rows of C (%.1f s per step)" % (rows, dt))
     return {
         "impl": "reference",
@@ -497,6 +508,7 @@ def parse_args(argv=None):
                     help="total seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--others", default="mxfp8_4096,mxfp4_8192,mxfp4_4096,"
+                    "mxfp8_e5m2_8192,w4a8_8192,"
                     "bf16_4096,f16_4096,bf16_2048,bf16_1024,proj_qkv,proj_out,"
                     "proj_up,proj_down,mx256",
                     help="workloads whose GEMM alone is also timed (L2 "

@@ -22,6 +22,7 @@ from . import _build
 
 E4M3 = 1
 E2M1 = 2
+E5M2 = 3
 DT_F32, DT_BF16, DT_F16 = 0, 1, 2
 SRC_K_CONTIGUOUS, SRC_K_STRIDED = 0, 1
 
@@ -188,8 +189,8 @@ def gemm_f16_workspace_bytes(M: int, N: int, K: int) -> int:
 def mx_gemm(A: MXTensor, B: MXTensor, out_dtype=torch.bfloat16,
             out: torch.Tensor | None = None, stream=None,
             workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """C = A * B for MX tensors A (M x K) and B (quantized from K x N).
-    With a workspace (a CUDA tensor of at least mx_gemm_workspace_bytes()
+    """C = A * B for MX tensors A (M x K) and B (quantized from K x N); the
+    two may hold different element formats.  With a workspace (a CUDA tensor of at least mx_gemm_workspace_bytes()
     bytes) the K-split entry point is used."""
     dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
     if out is None:

@@ -35,9 +35,22 @@ mx_status check_device() {
 
 mx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
+// A and B of one product: equal K; an E2M1 operand beside an 8-bit one is
+// unpacked by TMA, which needs K % 128 == 0 and a 32-byte aligned plane.
+mx_status check_pair(const mx_tensor* A, const mx_tensor* B) {
+  if (A->K != B->K) return MX_ERR_SHAPE;
+  if ((A->fmt == MX_FMT_E2M1) == (B->fmt == MX_FMT_E2M1)) return MX_OK;
+  if (A->outer == 0 || B->outer == 0 || A->K == 0) return MX_OK;
+  if (A->K % 128) return MX_ERR_SHAPE;
+  const mx_tensor* f4 = (A->fmt == MX_FMT_E2M1) ? A : B;
+  if (reinterpret_cast<uintptr_t>(f4->data) % 32) return MX_ERR_ALIGN;
+  return MX_OK;
+}
+
 mx_status check_tensor(const mx_tensor* t) {
   if (!t) return MX_ERR_INVALID_ARG;
-  if (t->fmt != MX_FMT_E4M3 && t->fmt != MX_FMT_E2M1) return MX_ERR_INVALID_ARG;
+  if (t->fmt != MX_FMT_E4M3 && t->fmt != MX_FMT_E5M2 && t->fmt != MX_FMT_E2M1)
+    return MX_ERR_INVALID_ARG;
   if (t->outer < 0 || t->K < 0 || t->outer > kMaxDim || t->K > kMaxDim) return MX_ERR_SHAPE;
   if (t->K % 32) return MX_ERR_SHAPE;
   if (t->outer > 0 && t->K > 0) {
@@ -54,7 +67,8 @@ extern "C" {
 
 size_t mx_data_bytes(int32_t fmt, int64_t outer, int64_t K) {
   if (outer < 0 || K < 0 || K % 32) return 0;
-  if (fmt == MX_FMT_E4M3) return static_cast<size_t>(outer) * static_cast<size_t>(K);
+  if (fmt == MX_FMT_E4M3 || fmt == MX_FMT_E5M2)
+    return static_cast<size_t>(outer) * static_cast<size_t>(K);
   if (fmt == MX_FMT_E2M1) return static_cast<size_t>(outer) * static_cast<size_t>(K) / 2;
   return 0;
 }
@@ -90,7 +104,7 @@ mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dty
   mx_status s;
   if ((s = check_tensor(A)) != MX_OK) return s;
   if ((s = check_tensor(B)) != MX_OK) return s;
-  if (A->fmt != B->fmt || A->K != B->K) return MX_ERR_SHAPE;
+  if ((s = check_pair(A, B)) != MX_OK) return s;
   if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
   const int64_t M = A->outer, N = B->outer, K = A->K;
   if (M == 0 || N == 0) return MX_OK;
@@ -99,13 +113,14 @@ mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dty
   if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
   if (!aligned16(C)) return MX_ERR_ALIGN;
   if ((s = check_device()) != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_mx(A->fmt, A->data, A->scales, B->data, B->scales, C,
+  return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data,
+                                       B->scales, C,
                                        c_dtype, ldc, M, N, K, nullptr, 0,
                                        static_cast<cudaStream_t>(stream)));
 }
 
 size_t mx_gemm_workspace_bytes(int32_t fmt, int64_t M, int64_t N, int64_t K) {
-  if (fmt != MX_FMT_E4M3 && fmt != MX_FMT_E2M1) return 0;
+  if (fmt != MX_FMT_E4M3 && fmt != MX_FMT_E5M2 && fmt != MX_FMT_E2M1) return 0;
   if (M <= 0 || N <= 0 || K <= 0 || K % 32 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return 0;
   if (check_device() != MX_OK) return 0;
@@ -117,7 +132,7 @@ mx_status mx_gemm_splitk(const mx_tensor* A, const mx_tensor* B, void* C, int32_
   mx_status s;
   if ((s = check_tensor(A)) != MX_OK) return s;
   if ((s = check_tensor(B)) != MX_OK) return s;
-  if (A->fmt != B->fmt || A->K != B->K) return MX_ERR_SHAPE;
+  if ((s = check_pair(A, B)) != MX_OK) return s;
   if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
   const int64_t M = A->outer, N = B->outer, K = A->K;
   if (M == 0 || N == 0) return MX_OK;
@@ -126,7 +141,8 @@ mx_status mx_gemm_splitk(const mx_tensor* A, const mx_tensor* B, void* C, int32_
   if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
   if (!aligned16(C) || (workspace && !aligned16(workspace))) return MX_ERR_ALIGN;
   if ((s = check_device()) != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_mx(A->fmt, A->data, A->scales, B->data, B->scales, C,
+  return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data,
+                                       B->scales, C,
                                        c_dtype, ldc, M, N, K, workspace, workspace_bytes,
                                        static_cast<cudaStream_t>(stream)));
 }

@@ -8,7 +8,7 @@
 
 namespace mxk {
 
-enum Format : int { FMT_E4M3 = 1, FMT_E2M1 = 2 };
+enum Format : int { FMT_E4M3 = 1, FMT_E2M1 = 2, FMT_E5M2 = 3 };
 enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 
 // Status word bits recorded by kernels (the host maps any non-zero word to
@@ -48,7 +48,8 @@ cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt
 // mx GEMM: A data outer=M, B data outer=N, both K-major; C row-major.
 // ws: workspace for the fp32 partials of K-split tiles (nullptr, or fewer
 // than gemm_workspace_bytes() bytes: no splitting).
-cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
+// fmt_a / fmt_b: the element formats of A and B (FMT_*).
+cudaError_t launch_gemm_mx(int fmt_a, int fmt_b, const void* a_data, const uint8_t* a_sf,
                            const void* b_data, const uint8_t* b_sf, void* C,
                            int c_dtype, int64_t ldc, int64_t M, int64_t N,
                            int64_t K, void* ws, size_t ws_bytes, cudaStream_t st);
@@ -59,7 +60,8 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
                             cudaStream_t st);
 
 // Workspace bytes the K-split needs (0: the problem is not split).
-// kind: FMT_E4M3, FMT_E2M1, or 0 for the 16-bit GEMM.
+// kind: FMT_E4M3 / FMT_E5M2 (the FP8-rate kernel, also for mixed formats),
+// FMT_E2M1 (both operands E2M1), or 0 for the 16-bit GEMM.
 size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K);
 
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc,

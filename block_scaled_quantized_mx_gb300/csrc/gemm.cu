@@ -1,6 +1,8 @@
 // gemm.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a:
-//   kind::f16 (fp16 / bf16 operands), kind::mxf8f6f4 block-scaled E4M3 and
-//   kind::mxf4 block-scaled packed E2M1, fp32 accumulation in tensor memory.
+//   kind::f16 (fp16 / bf16 operands), kind::mxf8f6f4 block-scaled E4M3 / E5M2
+//   (either operand may instead be E2M1, which TMA unpacks into the 8-bit
+//   shared-memory layout) and kind::mxf4 block-scaled packed E2M1 on both
+//   sides, fp32 accumulation in tensor memory.
 //
 // What is computed: C = A * B with fp32 accumulation (dicastech tutorial
 // "Treinar LLM em Swift", Passo 4-6: tiled matmul, FP16 variant); for the MX
@@ -107,9 +109,10 @@ __host__ __device__ constexpr uint32_t idesc_f16() {
          (static_cast<uint32_t>((BM * CG) >> 4) << 24);
 }
 
-// Instruction descriptor, block-scaled kinds: A/B format (E4M3 = 0 for
-// mxf8f6f4, E2M1 = 1 for mxf4), both K-major, N>>3 at bit 17, scale type
-// UE8M0 (bit 23), M>>4 at bit 24; the scale-factor byte selectors (bits 4-5
+// Instruction descriptor, block-scaled kinds: both operands K-major, N>>3 at
+// bit 17, scale type UE8M0 (bit 23), M>>4 at bit 24.  The A / B element
+// formats (bits 7-9 / 10-12) are E2M1 = 1 for mxf4; for mxf8f6f4 they are a
+// launch argument (fmt_field), and the scale-factor byte selectors (bits 4-5
 // for B, 29-30 for A) are filled in per MMA.
 template <int KIND, int CG>
 __host__ __device__ constexpr uint32_t idesc_mx() {
@@ -180,7 +183,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const __grid_constant__ CUtensorMap tmSFA,
             const __grid_constant__ CUtensorMap tmSFB, void* __restrict__ Cptr,
             int64_t ldc, int M, int N, int K, float* __restrict__ ws, int full_tiles,
-            int split) {
+            int split, uint32_t ab_fmt) {
   using T = KT<KIND, KSUB>;
   using L = Smem<KIND, CG, STAGES, KSUB>;
   extern __shared__ uint8_t smem_raw[];
@@ -246,6 +249,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
+      // Bytes one stage's copies complete on the full barrier.  TMA counts an
+      // E2M1 operand that it unpacks for the FP8-rate kernel at its packed
+      // size, half of what it occupies in shared memory.
+      uint32_t stage_tx = L::STAGE_TX;
+      if (KIND == KIND_MXF8) {
+        if (((ab_fmt >> 7) & 7u) == 5u) stage_tx -= L::A_BYTES / 2;
+        if (((ab_fmt >> 10) & 7u) == 5u) stage_tx -= L::B_BYTES / 2;
+      }
       for (int w = cluster_id; w < work.total && ok; w += num_clusters) {
         int mb, nb, kb0, kb1, unit;
         work.item(w, mb, nb, kb0, kb1, unit);
@@ -257,7 +268,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, CG * L::STAGE_TX);
+          if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, CG * stage_tx);
           const uint32_t full = full0 + 8 * s;
           const uint32_t a_dst = base + L::A_OFF + s * L::A_BYTES;
           const uint32_t b_dst = base + L::B_OFF + s * L::B_BYTES;
@@ -362,7 +373,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 // one scale atom (4 blocks) per sub-tile; byte mm of it
                 constexpr uint32_t ID = idesc_mx<KIND, CG>();
                 mma_mxf8_cg<CG>(tmem_base, ad, bd,
-                                ID | (static_cast<uint32_t>(mm) << 4) |
+                                ID | ab_fmt | (static_cast<uint32_t>(mm) << 4) |
                                     (static_cast<uint32_t>(mm) << 29),
                                 sfa_t + 4 * u, sfb_t + u * 4 * (BN / 128), acc);
               } else {
@@ -652,7 +663,7 @@ SplitPlan plan_split(int64_t M, int64_t N, int64_t K, int kps, bool use_split) {
 template <int KIND, int CG, int STAGES, int KSUB, int OUT_BF16>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                 const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
-                const SplitPlan& plan, float* ws, cudaStream_t st) {
+                const SplitPlan& plan, float* ws, uint32_t ab_fmt, cudaStream_t st) {
   using L = Smem<KIND, CG, STAGES, KSUB>;
   auto kern = gemm_kernel<KIND, CG, STAGES, KSUB, OUT_BF16>;
   static bool attr_set[64] = {};
@@ -677,7 +688,7 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, C, ldc, M, N, K, ws, plan.full_tiles,
-                         plan.split);
+                         plan.split, ab_fmt);
   if (e != cudaSuccess || plan.split < 2) return e;
   WorkList work;
   work.init((M + BM * CG - 1) / (BM * CG), (N + BN - 1) / BN,
@@ -697,12 +708,12 @@ constexpr int STAGES_CG1 = 4;
 template <int KIND, int OUT_BF16>
 cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                      const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
-                     const SplitPlan& plan, float* ws, cudaStream_t st) {
+                     const SplitPlan& plan, float* ws, uint32_t ab_fmt, cudaStream_t st) {
   if (M > BM)
     return run<KIND, 2, STAGES_CG2, KSUB_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K,
-                                                       plan, ws, st);
+                                                       plan, ws, ab_fmt, st);
   return run<KIND, 1, STAGES_CG1, KSUB_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, plan,
-                                                     ws, st);
+                                                     ws, ab_fmt, st);
 }
 
 // K elements per stage of each kind (KSUB is the same for both CTA groups)
@@ -717,45 +728,78 @@ int stage_k(int kind) {
 
 size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  const int k = (kind == FMT_E4M3) ? KIND_MXF8 : (kind == FMT_E2M1) ? KIND_MXF4 : KIND_F16;
+  const int k = (kind == FMT_E4M3 || kind == FMT_E5M2) ? KIND_MXF8
+                : (kind == FMT_E2M1)                  ? KIND_MXF4
+                                                      : KIND_F16;
   return plan_split(M, N, K, stage_k(k), true).ws_bytes;
 }
 
-cudaError_t launch_gemm_mx(int fmt, const void* a_data, const uint8_t* a_sf,
+namespace {
+
+// The tensor map of one operand's data plane: rows x K codes, a box of 128 K
+// by box_rows rows.  8-bit codes are copied as bytes.  Packed E2M1 codes for
+// the FP4-rate kernel are copied as bytes too (128 bytes = 256 codes); for
+// the FP8-rate kernel TMA unpacks them (16U4_ALIGN16B) into the 8-bit
+// layout, 16 codes in 8 bytes followed by an 8-byte gap, so that the tile in
+// shared memory is laid out exactly as an E4M3 tile is.
+bool make_data_tmap(CUtensorMap* m, const void* data, int fmt, bool fp4_kind, int64_t rows,
+                    int64_t K, uint32_t box_rows) {
+  if (fmt != FMT_E2M1)
+    return make_tmap(m, data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, rows, K, 128, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (fp4_kind)
+    return make_tmap(m, data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, K / 2, 128,
+                     box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(data), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Element-format field of the mxf8f6f4 instruction descriptor.
+uint32_t f8f6f4_code(int fmt) { return fmt == FMT_E5M2 ? 1u : fmt == FMT_E2M1 ? 5u : 0u; }
+
+}  // namespace
+
+cudaError_t launch_gemm_mx(int fmt_a, int fmt_b, const void* a_data, const uint8_t* a_sf,
                            const void* b_data, const uint8_t* b_sf, void* C,
                            int c_dtype, int64_t ldc, int64_t M, int64_t N,
                            int64_t K, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   const int eb = (c_dtype == DT_BF16) ? 2 : 4;
   if (K == 0) return launch_zero_fill(C, M, N, ldc, eb, st);
-  const int kind = (fmt == FMT_E4M3) ? KIND_MXF8 : KIND_MXF4;
+  const bool fp4 = (fmt_a == FMT_E2M1 && fmt_b == FMT_E2M1);
+  const int kind = fp4 ? KIND_MXF4 : KIND_MXF8;
   SplitPlan plan = plan_split(M, N, K, stage_k(kind), ws != nullptr);
   if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = plan_split(M, N, K, stage_k(kind), false);
-  const uint64_t kbytes = (fmt == FMT_E4M3) ? K : K / 2;
   // scale atoms per stage of the configuration dispatch() picks
   const bool pair = M > BM;
-  const int ck = (fmt == FMT_E4M3)
-                     ? (pair ? KT<KIND_MXF8, KSUB_CG2>::CK : KT<KIND_MXF8, KSUB_CG1>::CK)
-                     : (pair ? KT<KIND_MXF4, KSUB_CG2>::CK : KT<KIND_MXF4, KSUB_CG1>::CK);
+  const int ck = !fp4 ? (pair ? KT<KIND_MXF8, KSUB_CG2>::CK : KT<KIND_MXF8, KSUB_CG1>::CK)
+                      : (pair ? KT<KIND_MXF4, KSUB_CG2>::CK : KT<KIND_MXF4, KSUB_CG1>::CK);
   // one TMA box of B is this CTA's half of the N tile when M > BM
   const uint32_t b_rows = pair ? BN / 2 : BN;
   CUtensorMap ta, tb, tsa, tsb;
-  if (!make_tmap(&ta, a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, M, kbytes, 128, BM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tb, b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kbytes, N, kbytes, 128, b_rows,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!make_data_tmap(&ta, a_data, fmt_a, fp4, M, K, BM) ||
+      !make_data_tmap(&tb, b_data, fmt_b, fp4, N, K, b_rows) ||
       !make_sf_tmap(&tsa, a_sf, M, K, ck) || !make_sf_tmap(&tsb, b_sf, N, K, ck))
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   float* w = static_cast<float*>(ws);
-  if (fmt == FMT_E4M3) {
+  if (!fp4) {
+    const uint32_t f = (f8f6f4_code(fmt_a) << 7) | (f8f6f4_code(fmt_b) << 10);
     if (c_dtype == DT_BF16)
-      return dispatch<KIND_MXF8, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
-    return dispatch<KIND_MXF8, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
+      return dispatch<KIND_MXF8, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, st);
+    return dispatch<KIND_MXF8, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, st);
   }
   if (c_dtype == DT_BF16)
-    return dispatch<KIND_MXF4, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
-  return dispatch<KIND_MXF4, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, st);
+    return dispatch<KIND_MXF4, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, st);
+  return dispatch<KIND_MXF4, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, st);
 }
 
 cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
@@ -777,8 +821,8 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
   float* w = static_cast<float*>(ws);
   // the scale maps are unused by the 16-bit kinds
   if (ab_dtype == DT_BF16)
-    return dispatch<KIND_BF16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, st);
-  return dispatch<KIND_F16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, st);
+    return dispatch<KIND_BF16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, 0u, st);
+  return dispatch<KIND_F16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, 0u, st);
 }
 
 unsigned fetch_and_clear_status_gemm(cudaError_t* err) {

@@ -57,8 +57,11 @@ extern "C" {
 mx_status mx_gemm_splitk_noalloc(const mx_tensor* A, const mx_tensor* B, void* C,
                                  int32_t c_dtype, int64_t ldc, void* stream) {
   if (!A || !B) return MX_ERR_INVALID_ARG;
-  if (A->fmt == B->fmt && A->K == B->K && A->outer > 0 && B->outer > 0 && A->K > 0) {
-    const size_t need = mx_gemm_workspace_bytes(A->fmt, A->outer, B->outer, A->K);
+  if (A->K == B->K && A->outer > 0 && B->outer > 0 && A->K > 0) {
+    // the FP8-rate kernel unless both operands are E2M1
+    const int32_t kind = (A->fmt == MX_FMT_E2M1 && B->fmt == MX_FMT_E2M1) ? MX_FMT_E2M1
+                                                                          : MX_FMT_E4M3;
+    const size_t need = mx_gemm_workspace_bytes(kind, A->outer, B->outer, A->K);
     if (need > kScratchBytes) return MX_ERR_SHAPE;
   }
   void* scratch = nullptr;

@@ -377,6 +377,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two floats -> two E5M2 codes (lo in the low byte), RNE, saturating to
+// +-57344 instead of overflowing to infinity.
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Two floats -> one byte of two E2M1 codes (lo in the low nibble), RNE,
 // saturating.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {

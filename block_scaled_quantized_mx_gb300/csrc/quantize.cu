@@ -1,4 +1,4 @@
-// quantize.cu -- OCP MX quantization, fp32 -> E4M3 / E2M1 data plane plus
+// quantize.cu -- OCP MX quantization, fp32 -> E4M3 / E5M2 / E2M1 data plane plus
 // UE8M0 scale plane in the tensor-core scale-factor layout.
 //
 // The rule (OCP Microscaling v1.0 conversion; block of 32 along the
@@ -8,11 +8,12 @@
 //   e    = floor(log2 amax), read off the fp32 exponent field (for a subnormal
 //          amax, from the position of its leading one) -- never via a log
 //          function, which can round up just below a power of two
-//   X    = 2^clamp(e - emax, -127, 127), emax = 8 (E4M3) / 2 (E2M1)
+//   X    = 2^clamp(e - emax, -127, 127), emax = 8 (E4M3) / 15 (E5M2) / 2 (E2M1)
 //   code = e_s + 127 (UE8M0); all-zero block -> 0; NaN/Inf in block -> 0xFF
 //   q_i  = RNE-saturate(x_i / X) to the element format.
 // x / X is a multiplication by a power of two in fp32; it is exact except when
-// the product is an fp32 subnormal, which both formats round to +-0 anyway.
+// the product is an fp32 subnormal, which every element format rounds to +-0
+// anyway (the smallest E5M2 subnormal is 2^-16).
 //
 // Both kernels are HBM-streaming passes: each CTA owns one 128-row x 128-K
 // region, i.e. exactly one 512-byte scale atom, which it assembles in shared
@@ -32,8 +33,19 @@ __device__ __forceinline__ uint32_t abs_bits(float x) {
   return __float_as_uint(x) & 0x7FFFFFFFu;
 }
 
+template <int FMT>
+constexpr int emax_of() {
+  return FMT == FMT_E4M3 ? 8 : FMT == FMT_E5M2 ? 15 : 2;
+}
+
+// Two scaled values -> two 8-bit codes (lo in the low byte).
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt8x2(float lo, float hi) {
+  return FMT == FMT_E5M2 ? cvt_e5m2x2(lo, hi) : cvt_e4m3x2(lo, hi);
+}
+
 // Scale code and the multiplier 1/X for a block whose largest |x| has the bit
-// pattern amax (sign cleared).  emax: 8 for E4M3, 2 for E2M1.
+// pattern amax (sign cleared).  emax: 8 for E4M3, 15 for E5M2, 2 for E2M1.
 __device__ __forceinline__ void block_scale(uint32_t amax, int emax,
                                             uint32_t& code, float& inv_x) {
   if (amax >= 0x7F800000u) {          // Inf or NaN somewhere in the block
@@ -52,7 +64,7 @@ __device__ __forceinline__ void block_scale(uint32_t amax, int emax,
   }
   code = static_cast<uint32_t>(es + 127);
   // 2^-es as an fp32: biased exponent 127 - es lies in [2, 254] because
-  // e <= 127 bounds es above by 119 (E4M3) / 125 (E2M1).
+  // e <= 127 bounds es above by 119 (E4M3) / 112 (E5M2) / 125 (E2M1).
   inv_x = __uint_as_float(static_cast<uint32_t>(127 - es) << 23);
 }
 
@@ -60,13 +72,13 @@ __device__ __forceinline__ void block_scale(uint32_t amax, int emax,
 // Source outer x K, K contiguous.  CTA = (K chunk kc, row group rg); each warp
 // owns 16 rows; for one row a warp reads the chunk's 128 floats as 32 float4,
 // lane l covering k = 4l..4l+3 of block l/8.  The block amax is a max over 8
-// lanes (shuffles), the 4 codes of a lane are one 32-bit (E4M3) or 16-bit
-// (E2M1) store, so a warp stores 128 (64) contiguous bytes per row.
+// lanes (shuffles), the 4 codes of a lane are one 32-bit (8-bit formats) or
+// 16-bit (E2M1) store, so a warp stores 128 (64) contiguous bytes per row.
 template <int FMT>
 __global__ void __launch_bounds__(QT_THREADS)
 quantize_kcontig(const float* __restrict__ src, int64_t ld, int64_t outer,
                  int64_t K, uint8_t* __restrict__ data, uint8_t* __restrict__ sf) {
-  constexpr int EMAX = (FMT == FMT_E4M3) ? 8 : 2;
+  constexpr int EMAX = emax_of<FMT>();
   constexpr int ROWS_PER_WARP = 16;
   constexpr int BATCH = 8;
   __shared__ __align__(16) uint8_t atom[SF_ATOM_BYTES];
@@ -110,9 +122,9 @@ quantize_kcontig(const float* __restrict__ src, int64_t ld, int64_t outer,
       block_scale(a, EMAX, code, s);
       if (r < outer && kvalid) {
         if ((lane & 7) == 0) atom[sf_in_atom(rl, j)] = static_cast<uint8_t>(code);
-        if (FMT == FMT_E4M3) {
-          const uint32_t lo = cvt_e4m3x2(v[i].x * s, v[i].y * s);
-          const uint32_t hi = cvt_e4m3x2(v[i].z * s, v[i].w * s);
+        if (FMT != FMT_E2M1) {
+          const uint32_t lo = cvt8x2<FMT>(v[i].x * s, v[i].y * s);
+          const uint32_t hi = cvt8x2<FMT>(v[i].z * s, v[i].w * s);
           *reinterpret_cast<uint32_t*>(data + r * K + k) = lo | (hi << 16);
         } else {
           const uint32_t lo = cvt_e2m1x2(v[i].x * s, v[i].y * s);
@@ -143,7 +155,7 @@ template <int FMT>
 __global__ void __launch_bounds__(128)
 quantize_kstrided(const float* __restrict__ src, int64_t ld, int64_t outer,
                   int64_t K, uint8_t* __restrict__ data, uint8_t* __restrict__ sf) {
-  constexpr int EMAX = (FMT == FMT_E4M3) ? 8 : 2;
+  constexpr int EMAX = emax_of<FMT>();
   __shared__ __align__(16) uint8_t atom[SF_ATOM_BYTES];
 
   const int lane = threadIdx.x & 31;
@@ -186,12 +198,12 @@ quantize_kstrided(const float* __restrict__ src, int64_t ld, int64_t outer,
       float s;
       block_scale(a, EMAX, code, s);
       atom[sf_in_atom(4 * lane + c, w)] = static_cast<uint8_t>(code);
-      if (FMT == FMT_E4M3) {
+      if (FMT != FMT_E2M1) {
         uint32_t q[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          q[i] = cvt_e4m3x2(x[4 * i] * s, x[4 * i + 1] * s) |
-                 (cvt_e4m3x2(x[4 * i + 2] * s, x[4 * i + 3] * s) << 16);
+          q[i] = cvt8x2<FMT>(x[4 * i] * s, x[4 * i + 1] * s) |
+                 (cvt8x2<FMT>(x[4 * i + 2] * s, x[4 * i + 3] * s) << 16);
         uint4* dst = reinterpret_cast<uint4*>(data + (n + c) * K + kb);
         dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
         dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
@@ -238,6 +250,7 @@ cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt
   if (outer == 0 || K == 0) return cudaSuccess;
   uint8_t* d = static_cast<uint8_t*>(data);
   if (fmt == FMT_E4M3) return launch_fmt<FMT_E4M3>(src, ld, k_strided, outer, K, d, scales, st);
+  if (fmt == FMT_E5M2) return launch_fmt<FMT_E5M2>(src, ld, k_strided, outer, K, d, scales, st);
   return launch_fmt<FMT_E2M1>(src, ld, k_strided, outer, K, d, scales, st);
 }
 

@@ -4,8 +4,8 @@
  *
  * Three operations, all launched asynchronously on the caller's CUDA stream:
  *
- *   mx_quantize  fp32 matrix -> MX tensor (E4M3 or E2M1 data plane plus a
- *                UE8M0 scale plane, one scale per 32 consecutive K elements)
+ *   mx_quantize  fp32 matrix -> MX tensor (E4M3, E5M2 or E2M1 data plane plus
+ *                a UE8M0 scale plane, one scale per 32 consecutive K elements)
  *   mx_gemm      C = A * B on two MX tensors, fp32 accumulation, dequantize
  *                inside the tensor-core matmul, fp32 or bf16 C
  *   gemm_f16     C = A * B on row-major fp16 or bf16 matrices, fp32
@@ -59,9 +59,15 @@ typedef enum mx_status {
 typedef enum mx_format {
   MX_FMT_E4M3 = 1, /* MXFP8: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
                       one code per byte; no infinity; max 448            */
-  MX_FMT_E2M1 = 2  /* MXFP4: 1 sign, 2 exponent (bias 1), 1 mantissa bit;
+  MX_FMT_E2M1 = 2, /* MXFP4: 1 sign, 2 exponent (bias 1), 1 mantissa bit;
                       two codes per byte, the element with even k in the
                       low nibble; max 6                                   */
+  MX_FMT_E5M2 = 3  /* MXFP8 with a wider range: 1 sign, 5 exponent (bias
+                      15), 2 mantissa bits; one code per byte; max 57344;
+                      0x7C / 0xFC are +-infinity (mx_quantize never writes
+                      them, mx_gemm propagates them), 0x7D-0x7F NaN.  The
+                      RIGEL summary, Main findings section 3, names E5M2
+                      beside E4M3 and notes that it has infinities.       */
 } mx_format;
 
 /* Element type of a plain matrix. */
@@ -100,8 +106,8 @@ typedef struct mx_tensor {
   int64_t K;
 } mx_tensor;
 
-/* Bytes of the data plane: outer*K (E4M3) or outer*K/2 (E2M1); 0 on bad
- * arguments. */
+/* Bytes of the data plane: outer*K (E4M3, E5M2) or outer*K/2 (E2M1); 0 on
+ * bad arguments. */
 size_t mx_data_bytes(int32_t fmt, int64_t outer, int64_t K);
 
 /* Bytes of the scale plane: ceil(outer/128) * ceil(K/128) * 512; 0 on bad
@@ -114,9 +120,11 @@ size_t mx_scale_bytes(int64_t outer, int64_t K);
  *
  * For every row r of out and every block j of 32 consecutive K elements:
  *   amax = max |x| over the block; e = floor(log2(amax)) from the fp32
- *   exponent; X = 2^clamp(e - emax, -127, 127) with emax = 8 (E4M3) or 2
- *   (E2M1); the scale code is log2(X) + 127; each element is x / X rounded
- *   to nearest-even and saturated to the format's largest finite value.
+ *   exponent; X = 2^clamp(e - emax, -127, 127) with emax = 8 (E4M3), 15
+ *   (E5M2) or 2 (E2M1); the scale code is log2(X) + 127; each element is
+ *   x / X rounded to nearest-even and saturated to the format's largest
+ *   finite value (for E5M2 too: a block's own maximum, up to 1.99 * 2^15
+ *   after scaling, becomes 57344, never an infinity).
  *   An all-zero block gets scale code 0; a block holding a NaN or an
  *   infinity gets scale code 0xFF (its element codes are then unspecified).
  *
@@ -138,7 +146,12 @@ mx_status mx_quantize(const float* src, int64_t ld, int32_t src_layout,
  * from, with fp32 accumulation:
  *   C[i][j] = sum_k (a_ik * Xa_i,k/32) * (b_jk * Xb_j,k/32).
  *
- *   A, B     MX tensors of the same fmt and K (A->outer = M, B->outer = N)
+ *   A, B     MX tensors of the same K (A->outer = M, B->outer = N).  Their
+ *            formats may differ: any two of E4M3, E5M2 and E2M1.  A pair
+ *            of E2M1 tensors runs at the FP4 tensor rate; every other pair
+ *            runs at the FP8 rate, and a pair mixing E2M1 with an 8-bit
+ *            format needs K a multiple of 128 and the E2M1 data plane
+ *            32-byte aligned (MX_ERR_SHAPE / MX_ERR_ALIGN otherwise).
  *   C        device, M x N row-major, element type c_dtype (MX_DT_F32 or
  *            MX_DT_BF16, rounded to nearest-even); 16-byte aligned
  *   ldc      leading dimension of C in elements, >= N; ldc * element size
@@ -180,6 +193,8 @@ mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype,
  * *_workspace_bytes returns 0 when the problem is not split (or on bad
  * arguments, or without a compute capability 10.3 device).
  */
+/* fmt: the element format of both operands; for operands of different
+ * formats pass MX_FMT_E4M3. */
 size_t mx_gemm_workspace_bytes(int32_t fmt, int64_t M, int64_t N, int64_t K);
 mx_status mx_gemm_splitk(const mx_tensor* A, const mx_tensor* B, void* C,
                          int32_t c_dtype, int64_t ldc, void* workspace,

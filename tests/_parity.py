@@ -57,8 +57,19 @@ def sample_rows(M: int, n_random: int = 24, seed: int = 0):
     return sorted(r for r in fixed | rnd if 0 <= r < M)
 
 
-def fmt_code(kind: str) -> int:
-    return oracle.E4M3 if kind == "mxfp8" else oracle.E2M1
+def mx_quantize_both(A32: torch.Tensor, B32: torch.Tensor, fa: int, fb: int):
+    """Library quantization of A (M x K) and of B (K x N, K-strided)."""
+    a = mx.mx_quantize(A32.cuda(), fa)
+    b = mx.mx_quantize(B32.cuda(), fb, k_strided=True)
+    return a, b
+
+
+def oracle_mx_product(A32: torch.Tensor, B32: torch.Tensor, fa: int, fb: int,
+                      rows=None):
+    """Oracle quantization of both sources and the float64 product."""
+    ca, sa = oracle.quantize(A32.numpy(), fa, k_axis=1)
+    cb, sb = oracle.quantize(B32.numpy(), fb, k_axis=0)
+    return oracle.gemm_mx(ca, sa, cb, sb, fa, rows=rows, fmt_b=fb)
 
 
 def lib_quantize_to_oracle_form(q: mx.MXTensor):
@@ -66,7 +77,7 @@ def lib_quantize_to_oracle_form(q: mx.MXTensor):
     the oracle's plain form, using the oracle's own layout restatement."""
     data = q.data.cpu().numpy()
     sc = q.scales.cpu().numpy()
-    if q.fmt == mx.E4M3:
+    if q.fmt != mx.E2M1:
         codes = data.reshape(q.outer, q.K)
     else:
         codes = layout.unpack_e2m1(data.reshape(q.outer, q.K // 2))
@@ -77,7 +88,7 @@ def planes_from_codes(codes: np.ndarray, scales: np.ndarray, fmt: int,
                       device="cuda") -> mx.MXTensor:
     """Build library-format device planes from oracle-form codes."""
     outer, K = codes.shape
-    if fmt == oracle.E4M3:
+    if fmt != oracle.E2M1:
         data = codes.reshape(-1)
     else:
         data = layout.pack_e2m1(codes).reshape(-1)

@@ -48,6 +48,7 @@ def test_status_strings_and_version(L):
                                      (8192, 8192), (16384, 2048)])
 def test_plane_sizes(L, outer, K):
     assert mx.data_bytes(mx.E4M3, outer, K) == outer * K
+    assert mx.data_bytes(mx.E5M2, outer, K) == outer * K
     assert mx.data_bytes(mx.E2M1, outer, K) == outer * K // 2
     assert mx.scale_bytes(outer, K) == layout.scale_plane_bytes(outer, K)
 
@@ -76,7 +77,8 @@ def test_host_validation_without_launch(L):
     byref = ctypes.byref
     # mx_quantize
     assert L.mx_quantize(P, 128, 0, None, None) == 1
-    assert L.mx_quantize(P, 128, 0, byref(_t(fmt=3)), None) == 1
+    assert L.mx_quantize(P, 128, 0, byref(_t(fmt=4)), None) == 1
+    assert L.mx_quantize(P, 128, 0, byref(_t(fmt=0)), None) == 1
     assert L.mx_quantize(P, 128, 5, byref(_t()), None) == 1
     assert L.mx_quantize(None, 128, 0, byref(_t()), None) == 1
     assert L.mx_quantize(P, 128, 0, byref(_t(K=100)), None) == 2
@@ -93,8 +95,20 @@ def test_host_validation_without_launch(L):
     # mx_gemm
     a, b = _t(), _t(outer=256)
     assert L.mx_gemm(None, byref(b), P, 1, 256, None) == 1
-    assert L.mx_gemm(byref(a), byref(_t(fmt=2, outer=256)), P, 1, 256,
-                     None) == 2
+    # an E2M1 operand beside an 8-bit one: K % 128 and a 32-byte aligned
+    # E2M1 plane (TMA unpacks it); either order, E4M3 or E5M2
+    for f8 in (mx.E4M3, mx.E5M2):
+        for fa, fb in ((f8, mx.E2M1), (mx.E2M1, f8)):
+            assert L.mx_gemm(byref(_t(fmt=fa, K=96)),
+                             byref(_t(fmt=fb, outer=256, K=96)), P, 1, 256,
+                             None) == 2
+            bad = dict(data=0x1010)
+            ta = _t(fmt=fa, **(bad if fa == mx.E2M1 else {}))
+            tb = _t(fmt=fb, outer=256, **(bad if fb == mx.E2M1 else {}))
+            assert L.mx_gemm(byref(ta), byref(tb), P, 1, 256, None) == 3
+            assert L.mx_gemm_splitk(byref(ta), byref(tb), P, 1, 256, None, 0,
+                                    None) == 3
+    assert L.mx_gemm(byref(_t(fmt=4)), byref(b), P, 1, 256, None) == 1
     assert L.mx_gemm(byref(a), byref(_t(outer=256, K=256)), P, 1, 256,
                      None) == 2
     assert L.mx_gemm(byref(a), byref(b), P, 2, 256, None) == 1   # f16 out

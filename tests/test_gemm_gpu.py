@@ -16,8 +16,8 @@ import torch
 import block_scaled_quantized_mx_gb300 as mx
 import oracle
 import workloads
-from tests._parity import (check_close, f16_bits, fmt_code, nan_like,
-                           planes_from_codes, sample_rows)
+from tests._parity import (check_close, f16_bits, mx_quantize_both, nan_like,
+                           oracle_mx_product, planes_from_codes, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,34 +34,43 @@ def _out_dtype(out):
     return torch.bfloat16 if out == "bf16" else torch.float32
 
 
-def _mx_run(A32, B32, fmt, out):
+def _mx_run(A32, B32, fmt, out, fmt_b=None):
     """quantize A (M x K) and B (K x N) on the GPU, multiply, return C."""
-    a = mx.mx_quantize(A32.cuda(), fmt)
-    b = mx.mx_quantize(B32.cuda(), fmt, k_strided=True)
+    a, b = mx_quantize_both(A32, B32, fmt, fmt if fmt_b is None else fmt_b)
     C = nan_like((a.outer, b.outer), _out_dtype(out))
     mx.mx_gemm(a, b, out_dtype=_out_dtype(out), out=C)
     assert mx.mx_last_error() == 0
     return C.float().cpu().numpy()
 
 
-def _mx_ref(A32, B32, fmt, rows=None):
-    ca, sa = oracle.quantize(A32.numpy(), fmt, k_axis=1)
-    cb, sb = oracle.quantize(B32.numpy(), fmt, k_axis=0)
-    return oracle.gemm_mx(ca, sa, cb, sb, fmt, rows=rows)
+def _mx_ref(A32, B32, fmt, rows=None, fmt_b=None):
+    return oracle_mx_product(A32, B32, fmt, fmt if fmt_b is None else fmt_b,
+                             rows=rows)
 
 
 # ---------------------------------------------------------------- exact cases
 
-@pytest.mark.parametrize("fmt,values", [
-    (oracle.E4M3, np.arange(-14, 15)),
-    (oracle.E2M1, np.array([0, 1, 2, 3, 4, 6, -1, -2, -3, -4, -6]))])
+INTS = {oracle.E4M3: np.arange(-14, 15),
+        oracle.E2M1: np.array([0, 1, 2, 3, 4, 6, -1, -2, -3, -4, -6]),
+        # E5M2 holds 3 significant bits: m * 2^e with m <= 7
+        oracle.E5M2: np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 14, 16,
+                               -1, -2, -3, -5, -6, -7, -12, -16])}
+
+FORMAT_PAIRS = [(oracle.E4M3, oracle.E4M3), (oracle.E2M1, oracle.E2M1),
+                (oracle.E5M2, oracle.E5M2), (oracle.E4M3, oracle.E5M2),
+                (oracle.E5M2, oracle.E4M3), (oracle.E4M3, oracle.E2M1),
+                (oracle.E2M1, oracle.E4M3), (oracle.E5M2, oracle.E2M1),
+                (oracle.E2M1, oracle.E5M2)]
+
+
+@pytest.mark.parametrize("fmt,fmt_b", FORMAT_PAIRS)
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_integer_matrices_exact(fmt, values, out):
+def test_integer_matrices_exact(fmt, fmt_b, out):
     g = np.random.default_rng(17)
     M, N, K = 256, 384, 512
-    A = torch.from_numpy(g.choice(values, (M, K)).astype(np.float32))
-    B = torch.from_numpy(g.choice(values, (K, N)).astype(np.float32))
-    C = _mx_run(A, B, fmt, out)
+    A = torch.from_numpy(g.choice(INTS[fmt], (M, K)).astype(np.float32))
+    B = torch.from_numpy(g.choice(INTS[fmt_b], (K, N)).astype(np.float32))
+    C = _mx_run(A, B, fmt, out, fmt_b=fmt_b)
     want = (A.numpy().astype(np.int64) @ B.numpy().astype(np.int64))
     if out == "f32":
         assert np.array_equal(C, want.astype(np.float64))
@@ -125,7 +134,7 @@ def test_gemm_random_codes(fmt, M, N, K, out):
     check_close(C.float().cpu().numpy(), Cr, S, out, f"{fmt} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.E2M1])
 def test_gemm_extreme_scales(fmt):
     """Scale codes across the whole finite range, per block."""
     M = N = 256
@@ -142,6 +151,50 @@ def test_gemm_extreme_scales(fmt):
     ok = (S < 1e37) & (S > 1e-30)
     Cg = C.cpu().numpy().astype(np.float64)
     check_close(np.where(ok, Cg, Cr), Cr, S, "f32", "extreme scales")
+
+
+@pytest.mark.parametrize("fmt,fmt_b", FORMAT_PAIRS[3:])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (200, 296, 256),
+                                   (129, 136, 384), (1000, 520, 1152),
+                                   (384, 768, 4096)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_gemm_random_codes_mixed(fmt, fmt_b, M, N, K, out):
+    """Operands of different element formats (K a multiple of 128, as an
+    E2M1 operand beside an 8-bit one needs), ragged M and N tails."""
+    ca, sa = workloads.random_codes((M, K), fmt, seed=3 * M + K + fmt)
+    cb, sb = workloads.random_codes((N, K), fmt_b, seed=5 * N + K + fmt_b)
+    a = planes_from_codes(ca, sa, fmt)
+    b = planes_from_codes(cb, sb, fmt_b)
+    C = nan_like((M, N), _out_dtype(out))
+    mx.mx_gemm(a, b, out_dtype=_out_dtype(out), out=C)
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt, fmt_b=fmt_b)
+    check_close(C.float().cpu().numpy(), Cr, S, out,
+                f"{fmt}x{fmt_b} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt_b", [oracle.E5M2, oracle.E4M3])
+def test_e5m2_infinity_propagates(fmt_b):
+    """An E5M2 infinity code in A gives +-infinity in every element of its
+    row of C, with the sign of the partner element of B, as the oracle's
+    float64 sum does; the other rows stay finite and within tolerance."""
+    M, N, K = 256, 256, 256
+    ca, sa = workloads.random_codes((M, K), oracle.E5M2, 61)
+    cb, sb = workloads.random_codes((N, K), fmt_b, 62)
+    zero_b = (cb & 0x7F) == 0
+    cb[zero_b] |= 0x38                       # no zero partners: inf * 0
+    ca[3, 5] = 0x7C                          # +inf
+    ca[200, 77] = 0xFC                       # -inf
+    a = planes_from_codes(ca, sa, oracle.E5M2)
+    b = planes_from_codes(cb, sb, fmt_b)
+    C = mx.mx_gemm(a, b, out_dtype=torch.float32).cpu().numpy()
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, oracle.E5M2, fmt_b=fmt_b)
+    inf_rows = [3, 200]
+    assert np.isinf(Cr[inf_rows]).all()
+    assert np.array_equal(C[inf_rows], Cr[inf_rows])
+    rest = np.setdiff1d(np.arange(M), inf_rows)
+    check_close(C[rest], Cr[rest], S[rest], "f32", "finite rows")
 
 
 def test_k_zero_writes_zero():
@@ -210,9 +263,9 @@ def _case_check(c, rows=None):
                                 oracle.F16 if c.kind == "f16" else oracle.BF16,
                                 rows=rows)
     else:
-        fmt = fmt_code(c.kind)
-        Cg = _mx_run(A, B, fmt, c.out)
-        Cr, S = _mx_ref(A, B, fmt, rows=rows)
+        fa, fb = workloads.formats(c)
+        Cg = _mx_run(A, B, fa, c.out, fmt_b=fb)
+        Cr, S = _mx_ref(A, B, fa, rows=rows, fmt_b=fb)
     if rows is not None:
         Cg = Cg[rows]
     return check_close(Cg, Cr, S, c.out, c.name)
@@ -220,8 +273,9 @@ def _case_check(c, rows=None):
 
 SMALL = ["mx256", "f16_1024", "bf16_1024", "mxfp8_2048"]
 LARGE = ["f16_2048", "bf16_2048", "f16_4096", "bf16_4096", "mxfp8_4096",
-         "mxfp8_8192", "mxfp4_4096", "mxfp4_8192", "proj_qkv", "proj_out",
-         "proj_up", "proj_down"]
+         "mxfp8_8192", "mxfp4_4096", "mxfp4_8192", "mxfp8_e5m2_8192",
+         "w4a8_2048", "w4a8_8192", "proj_qkv", "proj_out", "proj_up",
+         "proj_down"]
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -235,7 +289,8 @@ def test_workload_sampled_rows(name):
     _case_check(c, rows=sample_rows(c.M, seed=c.seed_a))
 
 
-@pytest.mark.parametrize("name", ["mxfp8_4096", "bf16_2048", "mxfp4_4096"])
+@pytest.mark.parametrize("name", ["mxfp8_4096", "bf16_2048", "mxfp4_4096",
+                                  "w4a8_2048"])
 def test_deterministic(name):
     c = workloads.case(name)
     A, B = workloads.sources(c)
@@ -243,9 +298,7 @@ def test_deterministic(name):
         A, B = A.cuda(), B.cuda()
         C1, C2 = mx.gemm_f16(A, B), mx.gemm_f16(A, B)
     else:
-        fmt = fmt_code(c.kind)
-        a = mx.mx_quantize(A.cuda(), fmt)
-        b = mx.mx_quantize(B.cuda(), fmt, k_strided=True)
+        a, b = mx_quantize_both(A, B, *workloads.formats(c))
         C1 = mx.mx_gemm(a, b)
         C2 = mx.mx_gemm(a, b)
     assert torch.equal(C1.view(torch.uint8), C2.view(torch.uint8))

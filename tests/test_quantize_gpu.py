@@ -1,6 +1,6 @@
 """mx_quantize on the GPU vs the oracle: bit-exact data codes and scale codes
 (scale plane compared through the oracle's own layout restatement), padding
-bytes zero, both source orientations, both formats, the full-size sources of
+bytes zero, both source orientations, all three formats, the full-size sources of
 the benchmark workloads, ragged shapes and adversarial blocks."""
 import numpy as np
 import pytest
@@ -14,7 +14,7 @@ from tests._parity import lib_quantize_to_oracle_form
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [oracle.E4M3, oracle.E2M1]
+FMTS = [oracle.E4M3, oracle.E5M2, oracle.E2M1]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -105,6 +105,8 @@ def _adversarial_blocks():
         [1.0, 2.0 ** -10, -2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -11],
         [6.0, 5.0, 2.5, 0.25, 0.75, -1.25, 1.75, 3.5],   # E2M1 ties
         [2.0 ** -130, -2.0 ** -140, 2.0 ** -149],         # subnormal block
+        [1.875, 1.0], [1.8125, -1.5], [-1.96875],          # E5M2 top binade
+        [1.0, 2.0 ** -32, 3 * 2.0 ** -32, -2.0 ** -31, 2.0 ** -33],  # E5M2 ties
         list(2.0 ** np.arange(-15, 17, dtype=np.float64)),
         list(-(2.0 ** np.arange(-20, 12, dtype=np.float64))),
         [float("nan"), 1.0], [float("inf")], [-float("inf"), 3.0],
@@ -127,14 +129,15 @@ def test_quantize_adversarial_blocks(fmt, k_strided):
 
 
 @pytest.mark.parametrize("name", ["mx256", "mxfp8_8192", "mxfp4_8192",
+                                  "mxfp8_e5m2_8192", "w4a8_8192",
                                   "proj_down"])
 def test_quantize_full_size_sources(name):
     """The full-size sources the benchmark quantizes, bit for bit."""
     c = workloads.case(name)
     A, B = workloads.sources(c)
-    fmt = oracle.E4M3 if c.kind == "mxfp8" else oracle.E2M1
-    _compare(A, fmt, False)
-    _compare(B, fmt, True)
+    fa, fb = workloads.formats(c)
+    _compare(A, fa, False)
+    _compare(B, fb, True)
 
 
 def test_quantize_is_deterministic():

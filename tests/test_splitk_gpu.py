@@ -14,8 +14,8 @@ import torch
 import block_scaled_quantized_mx_gb300 as mx
 import oracle
 import workloads
-from tests._parity import (check_close, f16_bits, nan_like, planes_from_codes,
-                           sample_rows)
+from tests._parity import (check_close, f16_bits, mx_quantize_both, nan_like,
+                           oracle_mx_product, planes_from_codes, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -90,7 +90,7 @@ def test_f16_splitk(dt, M, N, K):
 
 
 @pytest.mark.parametrize("name", ["mxfp8_8192", "mxfp4_4096", "bf16_4096",
-                                  "proj_out"])
+                                  "proj_out", "w4a8_2048"])
 def test_workloads_splitk_sampled(name):
     c = workloads.case(name)
     A, B = workloads.sources(c)
@@ -103,15 +103,14 @@ def test_workloads_splitk_sampled(name):
                                 oracle.F16 if c.kind == "f16" else oracle.BF16,
                                 rows=rows)
     else:
-        fmt = oracle.E4M3 if c.kind == "mxfp8" else oracle.E2M1
-        nbytes = mx.mx_gemm_workspace_bytes(fmt, c.M, c.N, c.K)
-        a = mx.mx_quantize(A.cuda(), fmt)
-        b = mx.mx_quantize(B.cuda(), fmt, k_strided=True)
+        fa, fb = workloads.formats(c)
+        # both E2M1: the FP4-rate kernel; any other pair: the FP8-rate one
+        wfmt = fa if fa == fb else oracle.E4M3
+        nbytes = mx.mx_gemm_workspace_bytes(wfmt, c.M, c.N, c.K)
+        a, b = mx_quantize_both(A, B, fa, fb)
         odt = torch.bfloat16 if c.out == "bf16" else torch.float32
         C = nan_like((c.M, c.N), odt)
         mx.mx_gemm(a, b, out_dtype=odt, out=C, workspace=_ws(nbytes))
-        ca, sa = oracle.quantize(A.numpy(), fmt, k_axis=1)
-        cb, sb = oracle.quantize(B.numpy(), fmt, k_axis=0)
-        Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt, rows=rows)
+        Cr, S = oracle_mx_product(A, B, fa, fb, rows=rows)
     assert mx.mx_last_error() == 0
     check_close(C.float().cpu().numpy()[rows], Cr, S, c.out, name)

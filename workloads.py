@@ -15,6 +15,10 @@ Workloads (sizes and value recipes):
              entries (Bernoulli(0.01), drawn from the same generator)
              multiplied by 100, bf16 output
   mxfp4      MXFP4, M=N=K in {4096, 8192}, N(0,1), bf16 output
+  mxfp8_e5m2 MXFP8 with E5M2 elements on both sides, M=N=K=8192, the
+             mxfp8 recipe, bf16 output
+  w4a8       mixed MX formats: E4M3 activations (A, the mxfp8 recipe) times
+             E2M1 weights (B, N(0, 0.02)), M=N=K in {2048, 8192}, bf16 output
   proj       transformer projections of a 1B-parameter model at 32 x 512
              tokens (M=16384), hidden 2048, FFN 8192: qkv (K=2048, N=6144),
              out (K=2048, N=2048), up (K=2048, N=8192), down (K=8192,
@@ -29,10 +33,16 @@ from dataclasses import dataclass
 import torch
 
 
+# Element formats (A, B) of the MX kinds, as the library's format codes:
+# 1 = E4M3, 2 = E2M1, 3 = E5M2.
+MX_FORMATS = {"mxfp8": (1, 1), "mxfp4": (2, 2), "mxfp8_e5m2": (3, 3),
+              "w4a8": (1, 2)}
+
+
 @dataclass(frozen=True)
 class GemmCase:
     name: str
-    kind: str          # "mxfp8" | "mxfp4" | "f16" | "bf16"
+    kind: str          # an MX_FORMATS key | "f16" | "bf16"
     M: int
     N: int
     K: int
@@ -82,6 +92,26 @@ def mxfp4_cases():
     return out
 
 
+def format_cases():
+    sa, sb = _seeds(5, 13)
+    out = [GemmCase("mxfp8_e5m2_8192", "mxfp8_e5m2", 8192, 8192, 8192, "bf16",
+                    "outlier", "outlier", sa, sb)]
+    for n in (2048, 8192):
+        sa, sb = _seeds(6, int(math.log2(n)))
+        out.append(GemmCase(f"w4a8_{n}", "w4a8", n, n, n, "bf16", "outlier",
+                            "weight", sa, sb))
+    return out
+
+
+def is_mx(c: GemmCase) -> bool:
+    return c.kind in MX_FORMATS
+
+
+def formats(c: GemmCase):
+    """(format of A, format of B) of an MX case."""
+    return MX_FORMATS[c.kind]
+
+
 PROJ_SHAPES = (("qkv", 2048, 6144), ("out", 2048, 2048), ("up", 2048, 8192),
                ("down", 8192, 2048))
 
@@ -97,7 +127,7 @@ def proj_cases():
 
 def all_cases():
     return [mx256()] + f16_cases() + mxfp8_cases() + mxfp4_cases() + \
-        proj_cases()
+        format_cases() + proj_cases()
 
 
 def case(name: str) -> GemmCase:
@@ -145,12 +175,13 @@ def random_codes(shape, fmt: int, seed: int, scale_lo: int = 112,
     [scale_lo, scale_hi].  Returns (codes outer x K, scales outer x K/32)."""
     outer, K = shape
     g = torch.Generator().manual_seed(int(seed))
-    if fmt == 1:
+    if fmt in (1, 3):
         codes = torch.randint(0, 256, (outer, K), generator=g,
                               dtype=torch.int32)
-        # 0x7F and 0xFF are NaN in E4M3: redraw them as zeros
-        codes = torch.where((codes & 0x7F) == 0x7F, torch.zeros_like(codes),
-                            codes)
+        # redraw the non-finite codes as zeros: 0x7F / 0xFF in E4M3,
+        # 0x7C-0x7F / 0xFC-0xFF in E5M2
+        bad = (codes & 0x7F) >= (0x7F if fmt == 1 else 0x7C)
+        codes = torch.where(bad, torch.zeros_like(codes), codes)
     else:
         codes = torch.randint(0, 16, (outer, K), generator=g,
                               dtype=torch.int32)
