@@ -19,6 +19,7 @@ cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -37,13 +38,47 @@ import workloads  # noqa: E402
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# nominal dense ratios to bf16: fp8 2x, fp4 6x (2.25 / 4.5 / 13.5 PFLOP/s)
-# dense tensor rate of each kind relative to bf16; an E2M1 operand beside an
-# 8-bit one runs at the FP8 rate
+# nominal dense tensor rate of each kind relative to bf16 (2.25 / 4.5 / 13.5
+# PFLOP/s for bf16 / fp8 / fp4); an E2M1 operand beside an 8-bit one runs at
+# the FP8 rate
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0,
                  "mxfp8_e5m2": 2.0, "w4a8": 2.0}
 DTYPE_NAME = {"mxfp8": "e4m3", "mxfp4": "e2m1", "mxfp8_e5m2": "e5m2",
               "w4a8": "e4m3 x e2m1"}
+
+
+PROFILES = os.path.join(ROOT, "profiles")
+GEMM_SOURCES = [os.path.join(ROOT, "block_scaled_quantized_mx_gb300", "csrc", f)
+                for f in ("gemm.cu", "ptx.cuh", "common.cuh")]
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the GEMM kernel on this workload, from the
+    traffic record of a committed ncu summary under profiles/, or None when
+    there is none or the kernel's sources changed since it was taken."""
+    want = gemm_source_hash()
+    try:
+        names = sorted(os.listdir(PROFILES))
+    except OSError:
+        return None
+    for name in names:
+        with open(os.path.join(PROFILES, name)) as f:
+            for line in f:
+                line = line.strip()
+                if not line.startswith("traffic-record:"):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split()[1:])
+                if kv.get("workload") == workload and kv.get("sources") == want:
+                    return int(kv["bytes_per_launch"])
+    return None
 
 
 def ws_format(fa, fb):
@@ -396,7 +431,11 @@ def run_ours(args, rank, world, local_rank):
 
     roofline = {"bound": "tensor", "kernel": "mx_gemm" if is_mx else "gemm_f16",
                 "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
-                "frac": gemm_tf / peak, "traffic": None,
+                "frac": gemm_tf / peak,
+                "traffic": profiled_traffic(c.name) if is_mx else None,
+                "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum "
+                                  "per launch, ncu capture summarised in "
+                                  "profiles/ (null once the kernel changed)",
                 "peak_source": "%s bf16 burst x nominal %s/bf16 ratio %g" %
                 (peak_src, c.kind, NOMINAL_RATIO[c.kind])}
     line = {
