@@ -17,6 +17,9 @@ What each function follows:
     quantized bytes (RIGEL technical summary, "Metodologia", checksum gate),
     returning C and S = sum_k |a_ik * b_kj| for the per-element tolerance
     |C_gpu - C| <= tol * S.
+  * ``epilogue`` -- bias and GELU on the product, the fused GEMM + bias +
+    GELU kernel of the RIGEL summary (Main findings section 4); GELU is
+    x * Phi(x) (through erfc), or its tanh approximation.
 """
 from __future__ import annotations
 
@@ -32,6 +35,9 @@ E2M1 = 2
 E5M2 = 3
 F16 = 2
 BF16 = 1
+ACT_NONE = 0
+ACT_GELU = 1
+ACT_GELU_TANH = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mx_oracle.c")
@@ -91,6 +97,12 @@ def _load():
                                     i64, p, p]
         lib.mxo_gemm_f16.restype = None
         lib.mxo_gemm_f16.argtypes = [p, p, i64, i64, i64, i32, p, i64, p, p]
+        lib.mxo_gelu.restype = dbl
+        lib.mxo_gelu.argtypes = [dbl]
+        lib.mxo_gelu_tanh.restype = dbl
+        lib.mxo_gelu_tanh.argtypes = [dbl]
+        lib.mxo_epilogue.restype = None
+        lib.mxo_epilogue.argtypes = [p, i64, i64, p, i32]
         lib.mxo_num_threads.restype = i32
         lib.mxo_num_threads.argtypes = []
         _lib = lib
@@ -153,6 +165,29 @@ def decode_table(fmt: int) -> np.ndarray:
     if fmt == E5M2:
         return np.array([decode_e5m2(c) for c in range(256)])
     return np.array([decode_e2m1(c) for c in range(16)])
+
+
+def gelu(x: float) -> float:
+    return float(_load().mxo_gelu(float(x)))
+
+
+def gelu_tanh(x: float) -> float:
+    return float(_load().mxo_gelu_tanh(float(x)))
+
+
+def epilogue(C, bias=None, act: int = ACT_NONE) -> np.ndarray:
+    """float64 act(C + bias) of a float64 rows x N product (bias: N values
+    added to every row, or None)."""
+    Y = np.array(C, dtype=np.float64, order="C", copy=True)
+    rows, N = Y.shape
+    b = None
+    if bias is not None:
+        b = np.ascontiguousarray(bias, dtype=np.float64)
+        if b.shape != (N,):
+            raise ValueError("bias must hold N values")
+    _load().mxo_epilogue(_ptr(Y), rows, N, None if b is None else _ptr(b),
+                         int(act))
+    return Y
 
 
 def num_threads() -> int:

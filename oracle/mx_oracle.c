@@ -30,6 +30,7 @@
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC mx_oracle.c -o liboracle.so -lm
  */
+#define _DEFAULT_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -41,6 +42,9 @@
 #define MXO_E5M2 3
 #define MXO_F16 2
 #define MXO_BF16 1
+#define MXO_ACT_NONE 0
+#define MXO_ACT_GELU 1
+#define MXO_ACT_GELU_TANH 2
 
 /* ------------------------------------------------------------------------ */
 /* Decoding (closed form from the bit fields).                               */
@@ -350,6 +354,42 @@ void mxo_gemm_f16(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N,
         }
     }
     free(tab);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused epilogue: bias and activation on the product.                       */
+/* ------------------------------------------------------------------------ */
+
+/* GELU(x) = x * Phi(x), Phi the standard normal CDF, written through erfc so
+ * that the negative tail keeps its relative accuracy:
+ * Phi(x) = erfc(-x / sqrt(2)) / 2. */
+double mxo_gelu(double x)
+{
+    return 0.5 * x * erfc(-x / sqrt(2.0));
+}
+
+/* The tanh approximation of GELU (Hendrycks and Gimpel, "Gaussian Error
+ * Linear Units"): 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))). */
+double mxo_gelu_tanh(double x)
+{
+    const double k = sqrt(2.0 / M_PI);
+    return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+}
+
+/* The epilogue of the fused GEMM + bias + GELU kernel (RIGEL summary, Main
+ * findings section 4): Y[i][j] = act(C[i][j] + bias[j]) for an rows x N
+ * matrix C; bias may be NULL (no bias).  In place. */
+void mxo_epilogue(double* C, int64_t rows, int64_t N, const double* bias, int act)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double x = C[i * N + j] + (bias ? bias[j] : 0.0);
+            if (act == MXO_ACT_GELU) x = mxo_gelu(x);
+            else if (act == MXO_ACT_GELU_TANH) x = mxo_gelu_tanh(x);
+            C[i * N + j] = x;
+        }
+    }
 }
 
 int mxo_num_threads(void)

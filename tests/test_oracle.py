@@ -520,3 +520,53 @@ def test_e2m1_pack_roundtrip():
     assert p.shape == (5, 32)
     assert p[0, 0] == (c[0, 0] | (c[0, 1] << 4))
     assert np.array_equal(layout.unpack_e2m1(p), c)
+
+
+# ---------------------------------------------------------------- epilogue
+
+def test_gelu_textbook_values_and_identity():
+    # GELU(x) = x * Phi(x); Phi(1) = 0.8413447460685429 and
+    # Phi(-1) = 0.15865525393145707 (standard normal table)
+    assert oracle.gelu(1.0) == pytest.approx(0.8413447460685429, rel=1e-15)
+    assert oracle.gelu(-1.0) == pytest.approx(-0.15865525393145707, rel=1e-15)
+    assert oracle.gelu(0.0) == 0.0
+    for x in (0.3, 1.7, 4.0, 9.0, 30.0):
+        # x Phi(x) - (-x) Phi(-x) = x (Phi(x) + Phi(-x)) = x
+        assert oracle.gelu(x) - oracle.gelu(-x) == pytest.approx(x, rel=1e-15)
+    assert oracle.gelu(40.0) == 40.0
+    # deep negative tail: -x Phi(-x) keeps its relative accuracy
+    assert oracle.gelu(-10.0) == pytest.approx(-10.0 * 7.61985302416047e-24,
+                                               rel=1e-12)
+
+
+def test_gelu_matches_scipy_and_torch():
+    sp = pytest.importorskip("scipy.special")
+    x = np.concatenate([np.linspace(-12, 12, 4001),
+                        np.random.default_rng(5).standard_normal(2000) * 3])
+    ours = np.array([oracle.gelu(v) for v in x])
+    ref = x * sp.ndtr(x)
+    assert np.allclose(ours, ref, rtol=1e-13, atol=1e-300)
+    tx = torch.from_numpy(x)
+    ref_t = torch.nn.functional.gelu(tx).numpy()
+    assert np.allclose(ours, ref_t, rtol=1e-13, atol=1e-15)
+    ours_t = np.array([oracle.gelu_tanh(v) for v in x])
+    ref_tt = torch.nn.functional.gelu(tx, approximate="tanh").numpy()
+    assert np.allclose(ours_t, ref_tt, rtol=1e-13, atol=1e-15)
+    # the two forms differ (by up to ~1e-3 near |x| ~ 2), so a swapped
+    # activation code would show
+    assert np.abs(ours - ours_t).max() > 1e-4
+
+
+def test_epilogue_bias_runs_along_columns():
+    g = np.random.default_rng(8)
+    C = g.standard_normal((7, 5))
+    bias = np.array([1.0, -2.0, 0.5, 3.0, -0.25])
+    Y = oracle.epilogue(C, bias, oracle.ACT_NONE)
+    assert np.array_equal(Y, C + bias[None, :])
+    assert np.array_equal(oracle.epilogue(C, None, oracle.ACT_NONE), C)
+    sp = pytest.importorskip("scipy.special")
+    Yg = oracle.epilogue(C, bias, oracle.ACT_GELU)
+    x = C + bias[None, :]
+    assert np.allclose(Yg, x * sp.ndtr(x), rtol=1e-13, atol=1e-300)
+    with pytest.raises(ValueError):
+        oracle.epilogue(C, bias[:4], oracle.ACT_GELU)
