@@ -193,6 +193,27 @@ class L2Flusher:
         self.buf.fill_(1.0)
 
 
+def event_time(f, iters=20, flusher=None):
+    """Mean CUDA-event time (ms) of f() on the current stream, after 3
+    untimed calls; L2 flushed (untimed) before every call when a flusher is
+    given."""
+    for _ in range(3):
+        f()
+    stream = torch.cuda.current_stream()
+    tot = 0.0
+    for _ in range(iters):
+        if flusher is not None:
+            flusher()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        f()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    return tot / iters
+
+
 def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
     """CUDA-event time of the GEMM kernel alone on pre-quantized operands
     (mean over iters; L2 flushed before every launch when a flusher is
@@ -214,23 +235,61 @@ def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
         nb = mx.gemm_f16_workspace_bytes(c.M, c.N, c.K) if splitk else 0
         ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
         f = lambda: mx.gemm_f16(dA, dB, out=C, workspace=ws)  # noqa
-    for _ in range(3):
-        f()
-    stream = torch.cuda.current_stream()
-    tot = 0.0
-    for _ in range(iters):
-        if flusher is not None:
-            flusher()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        f()
-        e1.record(stream)
-        e1.synchronize()
-        tot += e0.elapsed_time(e1)
+    ms = event_time(f, iters, flusher)
     assert mx.mx_last_error() == 0
-    ms = tot / iters
     return ms, flops_of(c) / (ms * 1e-3) / 1e12
+
+
+def time_fused(mx, c, dev, flusher):
+    """The fused epilogue against the decomposed path on one MX workload
+    (the RIGEL summary's fused GEMM + bias + GELU, Main findings section 4):
+      gemm             mx_gemm, bf16 C (no epilogue work)
+      fused            mx_gemm_fused, bias + GELU, bf16 C
+      decomposed       mx_gemm fp32 C, then bias + GELU as a separate
+                       elementwise pass (torch), bf16 result
+      fused_quantize   mx_gemm_fused_quantize, bias + GELU, C as E4M3 MX
+      two_step_quantize  mx_gemm_fused fp32 C, then mx_quantize
+    Every launch starts with L2 flushed.  Returns milliseconds and the gains
+    of the fused forms."""
+    fa, fb = workloads.formats(c)
+    A, B = workloads.sources(c)
+    qa = mx.mx_quantize(A.to(dev), fa)
+    qb = mx.mx_quantize(B.to(dev), fb, k_strided=True)
+    bias = (torch.randn(c.N, generator=torch.Generator().manual_seed(9)) *
+            0.5).to(dev)
+    Cb = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    Cf = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
+    q = mx.empty_mx(mx.E4M3, c.M, c.N, dev)
+    gelu = torch.nn.functional.gelu
+
+    def decomposed():
+        mx.mx_gemm(qa, qb, out_dtype=torch.float32, out=Cf)
+        Cb.copy_(gelu(Cf + bias))
+
+    def two_step():
+        mx.mx_gemm_fused(qa, qb, bias, mx.ACT_GELU, out_dtype=torch.float32,
+                         out=Cf)
+        mx.mx_quantize(Cf, mx.E4M3, out=q)
+
+    t = {
+        "gemm": event_time(lambda: mx.mx_gemm(qa, qb, out=Cb), flusher=flusher),
+        "fused": event_time(lambda: mx.mx_gemm_fused(qa, qb, bias, mx.ACT_GELU,
+                                                     out=Cb), flusher=flusher),
+        "decomposed": event_time(decomposed, flusher=flusher),
+        "fused_quantize": event_time(
+            lambda: mx.mx_gemm_fused_quantize(qa, qb, mx.E4M3, bias,
+                                              mx.ACT_GELU, out=q),
+            flusher=flusher),
+        "two_step_quantize": event_time(two_step, flusher=flusher),
+    }
+    assert mx.mx_last_error() == 0
+    out = {k + "_ms": v for k, v in t.items()}
+    out["fused_gain_vs_decomposed"] = t["decomposed"] / t["fused"] - 1.0
+    out["fused_cost_vs_gemm"] = t["fused"] / t["gemm"] - 1.0
+    out["fused_quantize_gain_vs_two_step"] = \
+        t["two_step_quantize"] / t["fused_quantize"] - 1.0
+    out["fused_tflops"] = flops_of(c) / (t["fused"] * 1e-3) / 1e12
+    return out
 
 
 def quant_bytes(fmt, rows, K):
@@ -428,6 +487,13 @@ def run_ours(args, rank, world, local_rank):
             others[name] = {"gemm_ms": ms_o, "tflops": tf_o,
                             "frac_of_peak": tf_o / (bf16 * NOMINAL_RATIO[oc.kind])}
         del fl
+    fused = {}
+    if not args.no_fused and rank == 0:
+        fl = L2Flusher(dev)
+        for name in args.fused.split(","):
+            if name:
+                fused[name] = time_fused(mx, workloads.case(name), dev, fl)
+        del fl
 
     roofline = {"bound": "tensor", "kernel": "mx_gemm" if is_mx else "gemm_f16",
                 "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
@@ -457,6 +523,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "breakdown": extra,
         "gemm_only_other_workloads": others,
+        "fused_epilogue": fused,
         "e2e": e2e,
         "clocks": clk,
     }
@@ -553,6 +620,10 @@ def parse_args(argv=None):
                     help="workloads whose GEMM alone is also timed (L2 "
                          "flushed before each launch)")
     ap.add_argument("--no-others", action="store_true")
+    ap.add_argument("--fused", default="proj_up,mxfp8_4096",
+                    help="MX workloads on which the fused bias + GELU epilogue "
+                         "is timed against the decomposed path")
+    ap.add_argument("--no-fused", action="store_true")
     ap.add_argument("--splitk", action="store_true",
                     help="use the K-split GEMM entry points (with a workspace)")
     return ap.parse_args(argv)

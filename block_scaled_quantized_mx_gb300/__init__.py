@@ -25,13 +25,15 @@ E2M1 = 2
 E5M2 = 3
 DT_F32, DT_BF16, DT_F16 = 0, 1, 2
 SRC_K_CONTIGUOUS, SRC_K_STRIDED = 0, 1
+ACT_NONE, ACT_GELU, ACT_GELU_TANH = 0, 1, 2
 
 STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
           3: "MX_ERR_ALIGN", 4: "MX_ERR_UNSUPPORTED", 5: "MX_ERR_CUDA",
           6: "MX_ERR_TIMEOUT"}
 
 EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
-           "gemm_f16", "mx_gemm_workspace_bytes", "mx_gemm_splitk",
+           "gemm_f16", "mx_gemm_fused", "mx_gemm_fused_quantize",
+           "gemm_f16_fused", "mx_gemm_workspace_bytes", "mx_gemm_splitk",
            "gemm_f16_workspace_bytes", "gemm_f16_splitk",
            "mx_gemm_splitk_noalloc", "mx_last_error",
            "mx_selftest_wait_timeout", "mx_scales_to_rowmajor",
@@ -49,6 +51,11 @@ class CMXTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("fmt", ctypes.c_int32), ("outer", ctypes.c_int64),
                 ("K", ctypes.c_int64)]
+
+
+class CEpilogue(ctypes.Structure):
+    """Mirror of struct mx_epilogue."""
+    _fields_ = [("bias", ctypes.c_void_p), ("act", ctypes.c_int32)]
 
 
 _lib = None
@@ -86,6 +93,14 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm.argtypes = [pt, pt, p, i32, i64, p]
     L.gemm_f16.restype = i32
     L.gemm_f16.argtypes = [p, p, p, i32, i64, i64, i64, i64, i64, i64, p]
+    pe = ctypes.POINTER(CEpilogue)
+    L.mx_gemm_fused.restype = i32
+    L.mx_gemm_fused.argtypes = [pt, pt, pe, p, i32, i64, p]
+    L.mx_gemm_fused_quantize.restype = i32
+    L.mx_gemm_fused_quantize.argtypes = [pt, pt, pe, pt, p]
+    L.gemm_f16_fused.restype = i32
+    L.gemm_f16_fused.argtypes = [p, p, pe, p, i32, i64, i64, i64, i64, i64,
+                                 i64, p]
     L.mx_gemm_workspace_bytes.restype = sz
     L.mx_gemm_workspace_bytes.argtypes = [i32, i64, i64, i64]
     L.mx_gemm_splitk.restype = i32
@@ -234,6 +249,79 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
             *args, workspace.data_ptr() if workspace.numel() else None,
             workspace.numel() * workspace.element_size(), _stream(stream)),
             "gemm_f16_splitk")
+    return out
+
+
+def _epilogue(bias, act) -> CEpilogue:
+    if bias is not None:
+        if (bias.dtype != torch.float32 or bias.dim() != 1 or not bias.is_cuda
+                or not bias.is_contiguous()):
+            raise ValueError("bias must be a contiguous 1-D float32 CUDA tensor")
+    return CEpilogue(bias.data_ptr() if bias is not None and bias.numel() else
+                     None, int(act))
+
+
+def _check_bias(bias, N):
+    if bias is not None and bias.numel() != N:
+        raise ValueError("bias must hold N values")
+
+
+def mx_gemm_fused(A: MXTensor, B: MXTensor, bias: torch.Tensor | None = None,
+                  act: int = ACT_NONE, out_dtype=torch.bfloat16,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C = act(A * B + bias) with the bias and activation applied to the
+    fp32 accumulator inside the GEMM epilogue."""
+    _check_bias(bias, B.outer)
+    dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    if out is None:
+        out = torch.empty((A.outer, B.outer), dtype=out_dtype,
+                          device=A.data.device)
+    ca, cb, ep = A.c(), B.c(), _epilogue(bias, act)
+    ldc = out.stride(0) if out.dim() == 2 else B.outer
+    _check(lib().mx_gemm_fused(ctypes.byref(ca), ctypes.byref(cb),
+                               ctypes.byref(ep),
+                               out.data_ptr() if out.numel() else None, dt,
+                               ldc, _stream(stream)), "mx_gemm_fused")
+    return out
+
+
+def mx_gemm_fused_quantize(A: MXTensor, B: MXTensor, fmt: int,
+                           bias: torch.Tensor | None = None,
+                           act: int = ACT_NONE, out: MXTensor | None = None,
+                           stream=None) -> MXTensor:
+    """act(A * B + bias) quantized in the GEMM epilogue to an M x N MX
+    tensor (blocks of 32 along N) of element format fmt."""
+    _check_bias(bias, B.outer)
+    if out is None:
+        out = empty_mx(fmt, A.outer, B.outer, A.data.device)
+    ca, cb, cc, ep = A.c(), B.c(), out.c(), _epilogue(bias, act)
+    _check(lib().mx_gemm_fused_quantize(ctypes.byref(ca), ctypes.byref(cb),
+                                        ctypes.byref(ep), ctypes.byref(cc),
+                                        _stream(stream)),
+           "mx_gemm_fused_quantize")
+    return out
+
+
+def gemm_f16_fused(A: torch.Tensor, B: torch.Tensor,
+                   bias: torch.Tensor | None = None, act: int = ACT_NONE,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C (fp32) = act(A * B + bias) for row-major fp16 or bf16 tensors."""
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("A and B must both be fp16 or both bf16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    _check_bias(bias, N)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    dt = DT_F16 if A.dtype == torch.float16 else DT_BF16
+    ep = _epilogue(bias, act)
+    _check(lib().gemm_f16_fused(
+        A.data_ptr() if A.numel() else None,
+        B.data_ptr() if B.numel() else None, ctypes.byref(ep),
+        out.data_ptr() if out.numel() else None, dt, M, N, K, A.stride(0),
+        B.stride(0), out.stride(0), _stream(stream)), "gemm_f16_fused")
     return out
 
 

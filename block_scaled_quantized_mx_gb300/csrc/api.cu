@@ -60,6 +60,70 @@ mx_status check_tensor(const mx_tensor* t) {
   return MX_OK;
 }
 
+// The optional epilogue argument: NULL means none.  The bias must be
+// 16-byte aligned (it is read as float4).
+mx_status epilogue_from(const mx_epilogue* epi, mxk::Epilogue* out) {
+  *out = mxk::Epilogue{};
+  if (!epi) return MX_OK;
+  if (epi->act != MX_ACT_NONE && epi->act != MX_ACT_GELU && epi->act != MX_ACT_GELU_TANH)
+    return MX_ERR_INVALID_ARG;
+  if (epi->bias && !aligned16(epi->bias)) return MX_ERR_ALIGN;
+  out->bias = epi->bias;
+  out->act = epi->act;
+  return MX_OK;
+}
+
+bool has_work(const mxk::Epilogue& e) { return e.bias != nullptr || e.act != MX_ACT_NONE; }
+
+// mx_gemm, mx_gemm_splitk and mx_gemm_fused: checks, then one launch.
+mx_status mx_product(const mx_tensor* A, const mx_tensor* B, const mx_epilogue* epi, void* C,
+                     int32_t c_dtype, int64_t ldc, void* ws, size_t ws_bytes, void* stream) {
+  mx_status s;
+  if ((s = check_tensor(A)) != MX_OK) return s;
+  if ((s = check_tensor(B)) != MX_OK) return s;
+  if ((s = check_pair(A, B)) != MX_OK) return s;
+  if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  mxk::Epilogue e;
+  if ((s = epilogue_from(epi, &e)) != MX_OK) return s;
+  const int64_t M = A->outer, N = B->outer, K = A->K;
+  if (M == 0 || N == 0) return MX_OK;
+  if (!C) return MX_ERR_INVALID_ARG;
+  const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
+  if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
+  if (!aligned16(C)) return MX_ERR_ALIGN;
+  if (K == 0 && has_work(e)) return MX_ERR_SHAPE;
+  if ((s = check_device()) != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data, B->scales,
+                                       C, c_dtype, ldc, M, N, K, ws, ws_bytes, e,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+// gemm_f16, gemm_f16_splitk and gemm_f16_fused.
+mx_status f16_product(const void* A, const void* B, const mx_epilogue* epi, float* C,
+                      int32_t ab_dtype, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int64_t ldc, void* ws, size_t ws_bytes, void* stream) {
+  if (ab_dtype != MX_DT_F16 && ab_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MX_ERR_SHAPE;
+  mxk::Epilogue e;
+  mx_status s = epilogue_from(epi, &e);
+  if (s != MX_OK) return s;
+  if (M == 0 || N == 0) return MX_OK;
+  if (!C) return MX_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 4) return MX_ERR_SHAPE;
+  if (!aligned16(C)) return MX_ERR_ALIGN;
+  if (K > 0) {
+    if (!A || !B) return MX_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || lda % 8 || ldb % 8) return MX_ERR_SHAPE;
+    if (!aligned16(A) || !aligned16(B)) return MX_ERR_ALIGN;
+  } else if (has_work(e)) {
+    return MX_ERR_SHAPE;
+  }
+  if ((s = check_device()) != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc, ws,
+                                        ws_bytes, e, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 #pragma GCC visibility push(default)
@@ -101,22 +165,7 @@ mx_status mx_quantize(const float* src, int64_t ld, int32_t src_layout, const mx
 
 mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dtype,
                   int64_t ldc, void* stream) {
-  mx_status s;
-  if ((s = check_tensor(A)) != MX_OK) return s;
-  if ((s = check_tensor(B)) != MX_OK) return s;
-  if ((s = check_pair(A, B)) != MX_OK) return s;
-  if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
-  const int64_t M = A->outer, N = B->outer, K = A->K;
-  if (M == 0 || N == 0) return MX_OK;
-  if (!C) return MX_ERR_INVALID_ARG;
-  const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
-  if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
-  if (!aligned16(C)) return MX_ERR_ALIGN;
-  if ((s = check_device()) != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data,
-                                       B->scales, C,
-                                       c_dtype, ldc, M, N, K, nullptr, 0,
-                                       static_cast<cudaStream_t>(stream)));
+  return mx_product(A, B, nullptr, C, c_dtype, ldc, nullptr, 0, stream);
 }
 
 size_t mx_gemm_workspace_bytes(int32_t fmt, int64_t M, int64_t N, int64_t K) {
@@ -129,43 +178,40 @@ size_t mx_gemm_workspace_bytes(int32_t fmt, int64_t M, int64_t N, int64_t K) {
 
 mx_status mx_gemm_splitk(const mx_tensor* A, const mx_tensor* B, void* C, int32_t c_dtype,
                          int64_t ldc, void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace && !aligned16(workspace)) return MX_ERR_ALIGN;
+  return mx_product(A, B, nullptr, C, c_dtype, ldc, workspace, workspace_bytes, stream);
+}
+
+mx_status mx_gemm_fused(const mx_tensor* A, const mx_tensor* B, const mx_epilogue* epi,
+                        void* C, int32_t c_dtype, int64_t ldc, void* stream) {
+  return mx_product(A, B, epi, C, c_dtype, ldc, nullptr, 0, stream);
+}
+
+mx_status mx_gemm_fused_quantize(const mx_tensor* A, const mx_tensor* B,
+                                 const mx_epilogue* epi, const mx_tensor* C, void* stream) {
   mx_status s;
   if ((s = check_tensor(A)) != MX_OK) return s;
   if ((s = check_tensor(B)) != MX_OK) return s;
   if ((s = check_pair(A, B)) != MX_OK) return s;
-  if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if ((s = check_tensor(C)) != MX_OK) return s;
   const int64_t M = A->outer, N = B->outer, K = A->K;
+  if (C->outer != M || C->K != N) return MX_ERR_SHAPE;
+  mxk::Epilogue e;
+  if ((s = epilogue_from(epi, &e)) != MX_OK) return s;
   if (M == 0 || N == 0) return MX_OK;
-  if (!C) return MX_ERR_INVALID_ARG;
-  const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
-  if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
-  if (!aligned16(C) || (workspace && !aligned16(workspace))) return MX_ERR_ALIGN;
+  if (K == 0) return MX_ERR_SHAPE;
   if ((s = check_device()) != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data,
-                                       B->scales, C,
-                                       c_dtype, ldc, M, N, K, workspace, workspace_bytes,
+  e.q_fmt = C->fmt;
+  e.q_sf = C->scales;
+  return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data, B->scales,
+                                       C->data, MX_DT_F32, N, M, N, K, nullptr, 0, e,
                                        static_cast<cudaStream_t>(stream)));
 }
 
 mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,
                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                    void* stream) {
-  if (ab_dtype != MX_DT_F16 && ab_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-    return MX_ERR_SHAPE;
-  if (M == 0 || N == 0) return MX_OK;
-  if (!C) return MX_ERR_INVALID_ARG;
-  if (ldc < N || ldc % 4) return MX_ERR_SHAPE;
-  if (!aligned16(C)) return MX_ERR_ALIGN;
-  if (K > 0) {
-    if (!A || !B) return MX_ERR_INVALID_ARG;
-    if (lda < K || ldb < N || lda % 8 || ldb % 8) return MX_ERR_SHAPE;
-    if (!aligned16(A) || !aligned16(B)) return MX_ERR_ALIGN;
-  }
-  mx_status s = check_device();
-  if (s != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc, nullptr,
-                                        0, static_cast<cudaStream_t>(stream)));
+  return f16_product(A, B, nullptr, C, ab_dtype, M, N, K, lda, ldb, ldc, nullptr, 0, stream);
 }
 
 size_t gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -177,22 +223,15 @@ size_t gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 mx_status gemm_f16_splitk(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,
                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                           void* workspace, size_t workspace_bytes, void* stream) {
-  if (ab_dtype != MX_DT_F16 && ab_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-    return MX_ERR_SHAPE;
-  if (M == 0 || N == 0) return MX_OK;
-  if (!C) return MX_ERR_INVALID_ARG;
-  if (ldc < N || ldc % 4) return MX_ERR_SHAPE;
-  if (!aligned16(C) || (workspace && !aligned16(workspace))) return MX_ERR_ALIGN;
-  if (K > 0) {
-    if (!A || !B) return MX_ERR_INVALID_ARG;
-    if (lda < K || ldb < N || lda % 8 || ldb % 8) return MX_ERR_SHAPE;
-    if (!aligned16(A) || !aligned16(B)) return MX_ERR_ALIGN;
-  }
-  mx_status s = check_device();
-  if (s != MX_OK) return s;
-  return from_cuda(mxk::launch_gemm_f16(ab_dtype, A, B, C, M, N, K, lda, ldb, ldc, workspace,
-                                        workspace_bytes, static_cast<cudaStream_t>(stream)));
+  if (workspace && !aligned16(workspace)) return MX_ERR_ALIGN;
+  return f16_product(A, B, nullptr, C, ab_dtype, M, N, K, lda, ldb, ldc, workspace,
+                     workspace_bytes, stream);
+}
+
+mx_status gemm_f16_fused(const void* A, const void* B, const mx_epilogue* epi, float* C,
+                         int32_t ab_dtype, int64_t M, int64_t N, int64_t K, int64_t lda,
+                         int64_t ldb, int64_t ldc, void* stream) {
+  return f16_product(A, B, epi, C, ab_dtype, M, N, K, lda, ldb, ldc, nullptr, 0, stream);
 }
 
 mx_status mx_last_error(void* stream) {

@@ -10,6 +10,19 @@ namespace mxk {
 
 enum Format : int { FMT_E4M3 = 1, FMT_E2M1 = 2, FMT_E5M2 = 3 };
 enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+enum Act : int { ACT_NONE = 0, ACT_GELU = 1, ACT_GELU_TANH = 2 };
+
+// What the GEMM epilogue does between the fp32 accumulator and the store of
+// C: add bias[j] to column j (bias may be null), apply the activation, and
+// store C plain (q_fmt = 0: fp32 or bf16 by c_dtype) or as an MX tensor of
+// element format q_fmt whose blocks of 32 run along the columns of C (C is
+// then the data plane and q_sf its scale plane).
+struct Epilogue {
+  const float* bias = nullptr;
+  int act = ACT_NONE;
+  int q_fmt = 0;
+  uint8_t* q_sf = nullptr;
+};
 
 // Status word bits recorded by kernels (the host maps any non-zero word to
 // MX_ERR_TIMEOUT; the low byte says which wait gave up).
@@ -52,12 +65,13 @@ cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt
 cudaError_t launch_gemm_mx(int fmt_a, int fmt_b, const void* a_data, const uint8_t* a_sf,
                            const void* b_data, const uint8_t* b_sf, void* C,
                            int c_dtype, int64_t ldc, int64_t M, int64_t N,
-                           int64_t K, void* ws, size_t ws_bytes, cudaStream_t st);
+                           int64_t K, void* ws, size_t ws_bytes, const Epilogue& epi,
+                           cudaStream_t st);
 
 cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
                             int64_t M, int64_t N, int64_t K, int64_t lda,
                             int64_t ldb, int64_t ldc, void* ws, size_t ws_bytes,
-                            cudaStream_t st);
+                            const Epilogue& epi, cudaStream_t st);
 
 // Workspace bytes the K-split needs (0: the problem is not split).
 // kind: FMT_E4M3 / FMT_E5M2 (the FP8-rate kernel, also for mixed formats),

@@ -28,8 +28,11 @@
 //     epilogues;
 //   * warps 2..9: epilogue -- each warp drains 128 accumulator columns of its
 //     32-lane quarter into registers, hands the accumulator back to the MMA
-//     issuer at once, then converts (fp32, or bf16 RNE) and stores while the
-//     next tile's main loop runs.
+//     issuer at once, then, while the next tile's main loop runs, adds the
+//     bias and applies the activation when asked (the fused GEMM + bias +
+//     GELU kernel of the RIGEL summary, Main findings section 4) and stores
+//     fp32, bf16 (RNE), or C quantized to an MX tensor for the next layer:
+//     one thread holds one row's 128 columns, i.e. four whole 32-blocks.
 // Tensor memory: accumulator in columns [0, BN); per-stage scales from 256.
 //
 // Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records a
@@ -37,6 +40,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "mx_rule.cuh"
 #include "ptx.cuh"
 
 namespace mxk {
@@ -46,6 +50,8 @@ namespace {
 __device__ unsigned int g_status_gemm = 0;
 
 enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_MXF8 = 2, KIND_MXF4 = 3 };
+// the form in which the epilogue stores C
+enum Out : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_MX8 = 2, OUT_MX4 = 3 };
 
 constexpr int BM = 128;              // rows of A per CTA
 constexpr int BN = 256;              // columns of C per tile
@@ -177,13 +183,127 @@ __device__ __forceinline__ void record_timeout(volatile int* abort, unsigned sit
   atomicOr(&g_status_gemm, STATUS_TIMEOUT | site);
 }
 
-template <int KIND, int CG, int STAGES, int KSUB, int OUT_BF16>
+// Kernel-side form of Epilogue (plus the geometry of an MX output's scale
+// plane).
+struct EpiArgs {
+  const float* bias;
+  int act;
+  int q_fmt;
+  uint8_t* q_sf;
+  int64_t q_k_atoms;     // atoms along the columns of C
+  int64_t q_row_atoms;   // atoms along the rows of C
+};
+
+// GELU(x) = x * Phi(x) = x (1 + erf(x / sqrt 2)) / 2.  Inlined, so that the
+// 128 evaluations of one thread interleave.  Where 1 + erf cancels (x below
+// about -4) the result keeps an absolute error near 2^-24 |x| instead of its
+// relative accuracy, far below the product's own accumulation error.
+__device__ __forceinline__ float gelu_exact(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
+}
+
+// The tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+
+// Bias and activation on one thread's EPI_COLS accumulator values of one row
+// of C, columns col0 .. col0 + EPI_COLS - 1 (bias is read below N only).
+template <int NC>
+__device__ __forceinline__ void apply_bias_act(uint32_t (&r)[NC], const EpiArgs& e, int col0,
+                                               int N) {
+  if (e.bias != nullptr) {
+#pragma unroll
+    for (int v = 0; v < NC / 4; ++v) {
+      const int c = col0 + 4 * v;
+      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c + 3 < N) {
+        b = __ldg(reinterpret_cast<const float4*>(e.bias + c));
+      } else {
+        if (c < N) b.x = __ldg(e.bias + c);
+        if (c + 1 < N) b.y = __ldg(e.bias + c + 1);
+        if (c + 2 < N) b.z = __ldg(e.bias + c + 2);
+      }
+      r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + b.x);
+      r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + b.y);
+      r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + b.z);
+      r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + b.w);
+    }
+  }
+  if (e.act == ACT_GELU) {
+#pragma unroll
+    for (int i = 0; i < NC; ++i) r[i] = __float_as_uint(gelu_exact(__uint_as_float(r[i])));
+  } else if (e.act == ACT_GELU_TANH) {
+#pragma unroll
+    for (int i = 0; i < NC; ++i) r[i] = __float_as_uint(gelu_tanh(__uint_as_float(r[i])));
+  }
+}
+
+// Store one row's EPI_COLS values of C as an MX tensor (blocks of 32 along the
+// row, the next layer's K): the OCP rule per block, codes to the data plane
+// (row stride N codes), the row's four scale codes -- one 32-bit word, as
+// col0 is a multiple of 128 -- to the scale plane.  Rows beyond M inside the
+// last row atom and blocks beyond N get scale code 0 (the plane's padding).
+template <int OUT, int NC>
+__device__ __forceinline__ void store_mx_row(const uint32_t (&r)[NC], const EpiArgs& e,
+                                             uint8_t* data, int64_t row, int col0, int M,
+                                             int N) {
+  static_assert(NC == 4 * 32, "one thread stores four whole blocks");
+  if (col0 >= N || (row >> 7) >= e.q_row_atoms) return;
+  uint32_t sf = 0;
+  if (row < M) {
+    const int emax = emax_of_fmt(e.q_fmt);
+    const bool e5 = (e.q_fmt == FMT_E5M2);
+#pragma unroll
+    for (int b = 0; b < NC / 32; ++b) {
+      const int c = col0 + 32 * b;
+      if (c >= N) break;
+      uint32_t a = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a = max(a, r[32 * b + i] & 0x7FFFFFFFu);
+      uint32_t code;
+      float s;
+      block_scale(a, emax, code, s);
+      sf |= code << (8 * b);
+      const uint32_t* x = r + 32 * b;
+      if (OUT == OUT_MX8) {
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float x0 = __uint_as_float(x[4 * i]) * s, x1 = __uint_as_float(x[4 * i + 1]) * s;
+          const float x2 = __uint_as_float(x[4 * i + 2]) * s, x3 = __uint_as_float(x[4 * i + 3]) * s;
+          q[i] = e5 ? (cvt_e5m2x2(x0, x1) | (cvt_e5m2x2(x2, x3) << 16))
+                    : (cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(data + row * N + c);
+        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      } else {
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t* y = x + 8 * i;
+          q[i] = cvt_e2m1x2(__uint_as_float(y[0]) * s, __uint_as_float(y[1]) * s) |
+                 (cvt_e2m1x2(__uint_as_float(y[2]) * s, __uint_as_float(y[3]) * s) << 8) |
+                 (cvt_e2m1x2(__uint_as_float(y[4]) * s, __uint_as_float(y[5]) * s) << 16) |
+                 (cvt_e2m1x2(__uint_as_float(y[6]) * s, __uint_as_float(y[7]) * s) << 24);
+        }
+        *reinterpret_cast<uint4*>(data + (row * N + c) / 2) = make_uint4(q[0], q[1], q[2], q[3]);
+      }
+    }
+  }
+  *reinterpret_cast<uint32_t*>(e.q_sf + ((row >> 7) * e.q_k_atoms + (col0 >> 7)) * SF_ATOM_BYTES +
+                               sf_in_atom(static_cast<int>(row & 127), 0)) = sf;
+}
+
+template <int KIND, int CG, int STAGES, int KSUB, int OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmSFA,
             const __grid_constant__ CUtensorMap tmSFB, void* __restrict__ Cptr,
             int64_t ldc, int M, int N, int K, float* __restrict__ ws, int full_tiles,
-            int split, uint32_t ab_fmt) {
+            int split, uint32_t ab_fmt, EpiArgs epi) {
   using T = KT<KIND, KSUB>;
   using L = Smem<KIND, CG, STAGES, KSUB>;
   extern __shared__ uint8_t smem_raw[];
@@ -441,8 +561,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       }
       const int64_t row = static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q + lane;
       const int col0 = nb * BN + cg_ * EPI_COLS;
+      if (epi.bias != nullptr || epi.act != ACT_NONE) apply_bias_act(r, epi, col0, N);
+      if (OUT == OUT_MX8 || OUT == OUT_MX4) {
+        store_mx_row<OUT>(r, epi, static_cast<uint8_t*>(Cptr), row, col0, M, N);
+        continue;
+      }
       if (row < M) {
-        if (OUT_BF16) {
+        if (OUT == OUT_BF16) {
           uint16_t* crow = reinterpret_cast<uint16_t*>(Cptr) + row * ldc;
 #pragma unroll
           for (int v = 0; v < EPI_COLS / 8; ++v) {    // 8 columns per vector
@@ -536,7 +661,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 // Sum the `split` fp32 partials of each split tile in a fixed order (so the
 // result does not depend on timing) and write C.  CTA = (split tile r,
 // group of 4 tile rows); each thread owns 4 consecutive columns.
-template <int OUT_BF16>
+template <int OUT>
 __global__ void __launch_bounds__(256)
 reduce_partials_kernel(const float* __restrict__ ws, void* __restrict__ Cptr, int64_t ldc,
                        int M, int N, WorkList work, int tile_rows) {
@@ -558,7 +683,7 @@ reduce_partials_kernel(const float* __restrict__ ws, void* __restrict__ Cptr, in
     acc.w += v.w;
   }
   const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-  if (OUT_BF16) {
+  if (OUT == OUT_BF16) {
     uint16_t* crow = reinterpret_cast<uint16_t*>(Cptr) + row * ldc;
     const uint32_t lo = cvt_bf16x2(a[0], a[1]), hi = cvt_bf16x2(a[2], a[3]);
     if (col + 3 < N) {
@@ -660,12 +785,13 @@ SplitPlan plan_split(int64_t M, int64_t N, int64_t K, int kps, bool use_split) {
   return p;
 }
 
-template <int KIND, int CG, int STAGES, int KSUB, int OUT_BF16>
+template <int KIND, int CG, int STAGES, int KSUB, int OUT>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                 const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
-                const SplitPlan& plan, float* ws, uint32_t ab_fmt, cudaStream_t st) {
+                const SplitPlan& plan, float* ws, uint32_t ab_fmt, const EpiArgs& epi,
+                cudaStream_t st) {
   using L = Smem<KIND, CG, STAGES, KSUB>;
-  auto kern = gemm_kernel<KIND, CG, STAGES, KSUB, OUT_BF16>;
+  auto kern = gemm_kernel<KIND, CG, STAGES, KSUB, OUT>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -688,13 +814,15 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, C, ldc, M, N, K, ws, plan.full_tiles,
-                         plan.split, ab_fmt);
-  if (e != cudaSuccess || plan.split < 2) return e;
+                         plan.split, ab_fmt, epi);
+  // a split problem is a plain one (no epilogue work, fp32 or bf16 C)
+  if (e != cudaSuccess || plan.split < 2 || OUT == OUT_MX8 || OUT == OUT_MX4) return e;
   WorkList work;
   work.init((M + BM * CG - 1) / (BM * CG), (N + BN - 1) / BN,
             (K + KT<KIND, KSUB>::KPS - 1) / KT<KIND, KSUB>::KPS, plan.full_tiles, plan.split);
   dim3 grid(static_cast<unsigned>(plan.rem), BM * CG / 4);
-  reduce_partials_kernel<OUT_BF16><<<grid, 256, 0, st>>>(ws, C, ldc, M, N, work, BM * CG);
+  constexpr int ROUT = (OUT == OUT_BF16) ? OUT_BF16 : OUT_F32;
+  reduce_partials_kernel<ROUT><<<grid, 256, 0, st>>>(ws, C, ldc, M, N, work, BM * CG);
   return cudaGetLastError();
 }
 
@@ -705,15 +833,31 @@ constexpr int STAGES_CG2 = 6 / KSUB_CG2;
 constexpr int KSUB_CG1 = 1;
 constexpr int STAGES_CG1 = 4;
 
-template <int KIND, int OUT_BF16>
+template <int KIND, int OUT>
 cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                      const CUtensorMap& tsb, void* C, int64_t ldc, int M, int N, int K,
-                     const SplitPlan& plan, float* ws, uint32_t ab_fmt, cudaStream_t st) {
+                     const SplitPlan& plan, float* ws, uint32_t ab_fmt, const EpiArgs& epi,
+                     cudaStream_t st) {
   if (M > BM)
-    return run<KIND, 2, STAGES_CG2, KSUB_CG2, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K,
-                                                       plan, ws, ab_fmt, st);
-  return run<KIND, 1, STAGES_CG1, KSUB_CG1, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, M, N, K, plan,
-                                                     ws, ab_fmt, st);
+    return run<KIND, 2, STAGES_CG2, KSUB_CG2, OUT>(ta, tb, tsa, tsb, C, ldc, M, N, K, plan, ws,
+                                                  ab_fmt, epi, st);
+  return run<KIND, 1, STAGES_CG1, KSUB_CG1, OUT>(ta, tb, tsa, tsb, C, ldc, M, N, K, plan, ws,
+                                                ab_fmt, epi, st);
+}
+
+EpiArgs epi_args(const Epilogue& e, int64_t M, int64_t N) {
+  EpiArgs a;
+  a.bias = e.bias;
+  a.act = e.act;
+  a.q_fmt = e.q_fmt;
+  a.q_sf = e.q_sf;
+  a.q_k_atoms = sf_k_atoms(N);
+  a.q_row_atoms = sf_row_atoms(M);
+  return a;
+}
+
+bool plain_epilogue(const Epilogue& e) {
+  return e.bias == nullptr && e.act == ACT_NONE && e.q_fmt == 0;
 }
 
 // K elements per stage of each kind (KSUB is the same for both CTA groups)
@@ -770,13 +914,20 @@ uint32_t f8f6f4_code(int fmt) { return fmt == FMT_E5M2 ? 1u : fmt == FMT_E2M1 ? 
 cudaError_t launch_gemm_mx(int fmt_a, int fmt_b, const void* a_data, const uint8_t* a_sf,
                            const void* b_data, const uint8_t* b_sf, void* C,
                            int c_dtype, int64_t ldc, int64_t M, int64_t N,
-                           int64_t K, void* ws, size_t ws_bytes, cudaStream_t st) {
+                           int64_t K, void* ws, size_t ws_bytes, const Epilogue& epi,
+                           cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
+  const bool plain = plain_epilogue(epi);
   const int eb = (c_dtype == DT_BF16) ? 2 : 4;
-  if (K == 0) return launch_zero_fill(C, M, N, ldc, eb, st);
+  if (K == 0) {
+    if (!plain) return cudaErrorInvalidValue;   // the fused calls need K > 0
+    return launch_zero_fill(C, M, N, ldc, eb, st);
+  }
   const bool fp4 = (fmt_a == FMT_E2M1 && fmt_b == FMT_E2M1);
   const int kind = fp4 ? KIND_MXF4 : KIND_MXF8;
-  SplitPlan plan = plan_split(M, N, K, stage_k(kind), ws != nullptr);
+  // the K-split is for plain products only: the partials' reduction has no
+  // epilogue
+  SplitPlan plan = plan_split(M, N, K, stage_k(kind), ws != nullptr && plain);
   if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = plan_split(M, N, K, stage_k(kind), false);
   // scale atoms per stage of the configuration dispatch() picks
   const bool pair = M > BM;
@@ -791,24 +942,48 @@ cudaError_t launch_gemm_mx(int fmt_a, int fmt_b, const void* a_data, const uint8
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   float* w = static_cast<float*>(ws);
+  const EpiArgs ea = epi_args(epi, M, N);
+  const int out = epi.q_fmt == FMT_E2M1 ? OUT_MX4
+                  : epi.q_fmt != 0      ? OUT_MX8
+                  : c_dtype == DT_BF16  ? OUT_BF16
+                                        : OUT_F32;
   if (!fp4) {
     const uint32_t f = (f8f6f4_code(fmt_a) << 7) | (f8f6f4_code(fmt_b) << 10);
-    if (c_dtype == DT_BF16)
-      return dispatch<KIND_MXF8, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, st);
-    return dispatch<KIND_MXF8, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, st);
+    switch (out) {
+      case OUT_BF16:
+        return dispatch<KIND_MXF8, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, ea, st);
+      case OUT_MX8:
+        return dispatch<KIND_MXF8, OUT_MX8>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, ea, st);
+      case OUT_MX4:
+        return dispatch<KIND_MXF8, OUT_MX4>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, ea, st);
+      default:
+        return dispatch<KIND_MXF8, OUT_F32>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, f, ea, st);
+    }
   }
-  if (c_dtype == DT_BF16)
-    return dispatch<KIND_MXF4, 1>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, st);
-  return dispatch<KIND_MXF4, 0>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, st);
+  switch (out) {
+    case OUT_BF16:
+      return dispatch<KIND_MXF4, OUT_BF16>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, ea, st);
+    case OUT_MX8:
+      return dispatch<KIND_MXF4, OUT_MX8>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, ea, st);
+    case OUT_MX4:
+      return dispatch<KIND_MXF4, OUT_MX4>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, ea, st);
+    default:
+      return dispatch<KIND_MXF4, OUT_F32>(ta, tb, tsa, tsb, C, ldc, m, n, k, plan, w, 0u, ea, st);
+  }
 }
 
 cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C,
                             int64_t M, int64_t N, int64_t K, int64_t lda,
                             int64_t ldb, int64_t ldc, void* ws, size_t ws_bytes,
-                            cudaStream_t st) {
+                            const Epilogue& epi, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
-  if (K == 0) return launch_zero_fill(C, M, N, ldc, 4, st);
-  SplitPlan plan = plan_split(M, N, K, stage_k(KIND_F16), ws != nullptr);
+  const bool plain = plain_epilogue(epi);
+  if (epi.q_fmt != 0) return cudaErrorInvalidValue;     // fp32 C only
+  if (K == 0) {
+    if (!plain) return cudaErrorInvalidValue;
+    return launch_zero_fill(C, M, N, ldc, 4, st);
+  }
+  SplitPlan plan = plan_split(M, N, K, stage_k(KIND_F16), ws != nullptr && plain);
   if (plan.split > 1 && ws_bytes < plan.ws_bytes)
     plan = plan_split(M, N, K, stage_k(KIND_F16), false);
   const CUtensorMapDataType dt = (ab_dtype == DT_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -819,10 +994,11 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
     return cudaErrorInvalidValue;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   float* w = static_cast<float*>(ws);
+  const EpiArgs ea = epi_args(epi, M, N);
   // the scale maps are unused by the 16-bit kinds
   if (ab_dtype == DT_BF16)
-    return dispatch<KIND_BF16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, 0u, st);
-  return dispatch<KIND_F16, 0>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, 0u, st);
+    return dispatch<KIND_BF16, OUT_F32>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, 0u, ea, st);
+  return dispatch<KIND_F16, OUT_F32>(ta, tb, ta, tb, C, ldc, m, n, k, plan, w, 0u, ea, st);
 }
 
 unsigned fetch_and_clear_status_gemm(cudaError_t* err) {

@@ -10,6 +10,9 @@
  *                inside the tensor-core matmul, fp32 or bf16 C
  *   gemm_f16     C = A * B on row-major fp16 or bf16 matrices, fp32
  *                accumulation, fp32 C
+ *   *_fused      the same products with bias and GELU applied to the fp32
+ *                accumulator in the epilogue, and mx_gemm_fused_quantize,
+ *                which also quantizes C to an MX tensor for the next layer
  *
  * Where these come from.  The quantized tensor as one object holding a data
  * plane and a scale plane, the scale format ("FP8 E8M0") and the block of 32
@@ -72,6 +75,14 @@ typedef enum mx_format {
 
 /* Element type of a plain matrix. */
 typedef enum mx_dtype { MX_DT_F32 = 0, MX_DT_BF16 = 1, MX_DT_F16 = 2 } mx_dtype;
+
+/* Activation of a fused epilogue. */
+typedef enum mx_activation {
+  MX_ACT_NONE = 0,
+  MX_ACT_GELU = 1,      /* GELU(x) = x * Phi(x), Phi the standard normal CDF  */
+  MX_ACT_GELU_TANH = 2  /* its tanh approximation:
+                           0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))   */
+} mx_activation;
 
 /* Orientation of mx_quantize's fp32 source. */
 typedef enum mx_src_layout {
@@ -175,6 +186,53 @@ mx_status mx_gemm(const mx_tensor* A, const mx_tensor* B, void* C,
 mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype,
                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                    int64_t ldc, void* stream);
+
+/*
+ * Fused epilogue -- the GEMM + bias + GELU kernel of the RIGEL summary (Main
+ * findings section 4: fusing the epilogue in registers saves the O(n^2)
+ * round trip of C through memory).  Each element of the fp32 accumulator
+ * becomes
+ *   y[i][j] = act(acc[i][j] + bias[j])
+ * in fp32 before C is stored.
+ *
+ *   bias  device, N fp32 values (bias[j] is added to column j), 16-byte
+ *         aligned; NULL: no bias
+ *   act   mx_activation
+ * A NULL mx_epilogue pointer means no bias and MX_ACT_NONE.
+ */
+typedef struct mx_epilogue {
+  const float* bias;
+  int32_t act;
+} mx_epilogue;
+
+/* mx_gemm with the fused epilogue.  K = 0 is rejected (MX_ERR_SHAPE) when
+ * the epilogue does anything; other arguments as for mx_gemm. */
+mx_status mx_gemm_fused(const mx_tensor* A, const mx_tensor* B,
+                        const mx_epilogue* epi, void* C, int32_t c_dtype,
+                        int64_t ldc, void* stream);
+
+/*
+ * mx_gemm_fused_quantize -- y = act(A * B + bias) as above, then quantized
+ * in the epilogue into the MX tensor C (C->outer = M, C->K = N: blocks of 32
+ * consecutive columns of y share a scale, so C is ready to be the A operand
+ * of a next product whose contraction runs over those N columns).  The
+ * result is what mx_quantize (MX_SRC_K_CONTIGUOUS) would make of the fp32
+ * output of mx_gemm_fused, without the fp32 round trip through memory.
+ *
+ *   C       any mx_format; N a multiple of 32; its planes must not overlap
+ *           A's or B's
+ * K > 0 is required (MX_ERR_SHAPE otherwise).
+ */
+mx_status mx_gemm_fused_quantize(const mx_tensor* A, const mx_tensor* B,
+                                 const mx_epilogue* epi, const mx_tensor* C,
+                                 void* stream);
+
+/* gemm_f16 with the fused epilogue (fp32 C); K = 0 is rejected when the
+ * epilogue does anything. */
+mx_status gemm_f16_fused(const void* A, const void* B, const mx_epilogue* epi,
+                         float* C, int32_t ab_dtype, int64_t M, int64_t N,
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                         void* stream);
 
 /*
  * K-split variants.  When a problem's tiles leave clusters of SMs idle (a last,

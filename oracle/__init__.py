@@ -88,6 +88,8 @@ def _load():
         lib.mxo_encode_e4m3.argtypes = [dbl]
         lib.mxo_encode_e2m1.restype = u8
         lib.mxo_encode_e2m1.argtypes = [dbl]
+        lib.mxo_encode_array.restype = None
+        lib.mxo_encode_array.argtypes = [p, i64, i32, p]
         lib.mxo_floor_log2_f32.restype = i32
         lib.mxo_floor_log2_f32.argtypes = [ctypes.c_float]
         lib.mxo_quantize.restype = None
@@ -151,6 +153,15 @@ def encode_e4m3(v: float) -> int:
 
 def encode_e2m1(v: float) -> int:
     return int(_load().mxo_encode_e2m1(float(v)))
+
+
+def encode_array(values, fmt: int) -> np.ndarray:
+    """Codes (uint8, one per element, same shape) of float64 values:
+    round to nearest, ties to even, saturating, as the scalar encoders."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().mxo_encode_array(_ptr(v), v.size, int(fmt), _ptr(out))
+    return out
 
 
 def floor_log2_f32(a: float) -> int:

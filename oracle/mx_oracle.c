@@ -193,6 +193,15 @@ uint8_t mxo_encode_e2m1(double v)
     return (uint8_t)(c | (neg << 3));
 }
 
+/* Encode n values into codes of an element format (one code per byte). */
+void mxo_encode_array(const double* v, int64_t n, int fmt, uint8_t* out)
+{
+    build_tables();
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (fmt == MXO_E4M3) ? mxo_encode_e4m3(v[i])
+                 : (fmt == MXO_E5M2) ? mxo_encode_e5m2(v[i]) : mxo_encode_e2m1(v[i]);
+}
+
 /* ------------------------------------------------------------------------ */
 /* MX quantizer (OCP MX rule), one 32-element block at a time.               */
 /* ------------------------------------------------------------------------ */

@@ -107,3 +107,88 @@ def f16_bits(t: torch.Tensor) -> np.ndarray:
 
 def is_pow2(x: int) -> bool:
     return x > 0 and (x & (x - 1)) == 0 and math.log2(x) == int(math.log2(x))
+
+
+# ---------------------------------------------------------------- epilogue
+
+# max |d/dx GELU(x)| = 1.1289 (at x ~ 1.41); the tanh form's is the same to
+# three digits
+GELU_SLOPE = 1.13
+
+
+def epilogue_tolerance(C_ref, S, bias, act, Y_ref):
+    """Bound on |y_gpu - y_ref| for y = act(acc + bias).
+
+    The accumulator is within REL_TOL * S of C_ref; the fp32 bias add rounds
+    by at most 2^-24 |pre| (pre = C_ref + bias); the activation moves the
+    error by at most its slope and adds a few ulp of its own: 2^-21 |y|
+    covers erff / tanhf and the products around them; where 1 + erf or
+    1 + tanh cancels in fp32 (the negative tail) the absolute error stays
+    near 2^-24 |pre|, inside the slope * 2^-23 |pre| term."""
+    pre = C_ref + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+    slope = 1.0 if act == oracle.ACT_NONE else GELU_SLOPE
+    return slope * (REL_TOL * S + 2.0 ** -23 * np.abs(pre)) + \
+        2.0 ** -21 * np.abs(Y_ref)
+
+
+def check_epilogue_close(Y_gpu, C_ref, S, bias, act, out, what=""):
+    """Y_gpu (fp32 or bf16 output of a fused call) vs the oracle's
+    act(C_ref + bias)."""
+    Y_gpu = np.asarray(Y_gpu, dtype=np.float64)
+    Y_ref = oracle.epilogue(C_ref, bias, act)
+    assert Y_gpu.shape == Y_ref.shape
+    assert np.isfinite(Y_gpu).all(), f"{what}: non-finite output"
+    bound = epilogue_tolerance(C_ref, S, bias, act, Y_ref)
+    if out == "bf16":
+        bound = bound + ulp_bf16(Y_ref)
+    err = np.abs(Y_gpu - Y_ref)
+    bad = err > bound
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} out of "
+                             f"tolerance; first at {i}: gpu {Y_gpu[i]!r} ref "
+                             f"{Y_ref[i]!r} bound {bound[i]!r}")
+    return Y_ref, bound
+
+
+EMAX = {oracle.E4M3: 8, oracle.E5M2: 15, oracle.E2M1: 2}
+
+
+def _scale_codes(amax, emax):
+    """UE8M0 code of the OCP rule for float64 block maxima (0 for 0)."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))     # a = m 2^e, m in [0.5, 1)
+    es = np.clip(e - 1 - emax, -127, 127)
+    return np.where(a > 0, es + 127, 0).astype(np.int64)
+
+
+def check_mx_output(codes, scales, Y_ref, tol, fmt, what=""):
+    """The GPU quantized y = act(acc + bias) itself, and its fp32 y is known
+    only to lie within Y_ref +- tol.  Checks, from the oracle's side only:
+    every block's scale code is one the OCP rule gives for some block
+    maximum in the allowed interval, and, under that scale, every element
+    code is the oracle's encoding of some value in its allowed interval
+    (encoding is monotone, so the codes between those of the interval's
+    ends).  Returns the fraction of elements whose code the interval fixes
+    uniquely (compared exactly)."""
+    rows, N = Y_ref.shape
+    nb = N // 32
+    lo_abs = np.maximum(np.abs(Y_ref) - tol, 0.0).reshape(rows, nb, 32)
+    hi_abs = (np.abs(Y_ref) + tol).reshape(rows, nb, 32)
+    s_lo = _scale_codes(lo_abs.max(axis=2), EMAX[fmt])
+    s_hi = _scale_codes(hi_abs.max(axis=2), EMAX[fmt])
+    sc = scales.astype(np.int64)
+    bad = (sc < s_lo) | (sc > s_hi)
+    assert not bad.any(), (f"{what}: scale code outside the allowed range at "
+                           f"{np.argwhere(bad)[:3].tolist()}")
+    X = np.repeat(2.0 ** (sc - 127).astype(np.float64), 32, axis=1)
+    c_lo = oracle.encode_array((Y_ref - tol) / X, fmt)
+    c_hi = oracle.encode_array((Y_ref + tol) / X, fmt)
+    tab = oracle.decode_table(fmt)
+    v_lo, v_hi, v = tab[c_lo], tab[c_hi], tab[codes]
+    bad = ~((v >= v_lo) & (v <= v_hi))
+    assert not bad.any(), (
+        f"{what}: {bad.sum()} codes outside the allowed interval; first at "
+        f"{tuple(np.argwhere(bad)[0])}")
+    unique = (c_lo == c_hi) & np.repeat(s_lo == s_hi, 32, axis=1)
+    return float(unique.mean())

@@ -117,6 +117,42 @@ def test_host_validation_without_launch(L):
     assert L.mx_gemm(byref(a), byref(b), P, 1, 260, None) == 2   # ldc*2 % 16
     assert L.mx_gemm(byref(a), byref(b), P + 8, 1, 256, None) == 3
     assert L.mx_gemm(byref(_t(outer=0)), byref(b), None, 1, 256, None) == 0
+    # fused epilogue
+    ep = lambda bias=None, act=0: byref(mx.CEpilogue(bias, act))  # noqa
+    assert L.mx_gemm_fused(byref(a), byref(b), ep(act=3), P, 1, 256,
+                           None) == 1
+    assert L.mx_gemm_fused(byref(a), byref(b), ep(act=-1), P, 1, 256,
+                           None) == 1
+    assert L.mx_gemm_fused(byref(a), byref(b), ep(bias=P + 4), P, 1, 256,
+                           None) == 3
+    assert L.mx_gemm_fused(byref(_t(K=0, data=None, scales=None)),
+                           byref(_t(outer=256, K=0, data=None, scales=None)),
+                           ep(act=1), P, 1, 256, None) == 2
+    cq = _t(outer=128, K=256)                       # M x N output tensor
+    assert L.mx_gemm_fused_quantize(byref(a), byref(b), None, None,
+                                    None) == 1
+    assert L.mx_gemm_fused_quantize(byref(a), byref(b), None,
+                                    byref(_t(outer=64, K=256)), None) == 2
+    assert L.mx_gemm_fused_quantize(byref(a), byref(b), None,
+                                    byref(_t(outer=128, K=224)), None) == 2
+    assert L.mx_gemm_fused_quantize(byref(a), byref(b), None,
+                                    byref(_t(fmt=9, outer=128, K=256)),
+                                    None) == 1
+    assert L.mx_gemm_fused_quantize(byref(a), byref(b), ep(act=4),
+                                    byref(cq), None) == 1
+    assert L.mx_gemm_fused_quantize(byref(a), byref(b), None,
+                                    byref(_t(outer=128, K=256, data=0x1008)),
+                                    None) == 3
+    assert L.mx_gemm_fused_quantize(
+        byref(_t(K=0, data=None, scales=None)),
+        byref(_t(outer=256, K=0, data=None, scales=None)), None,
+        byref(cq), None) == 2
+    assert L.gemm_f16_fused(P, P, ep(act=7), P, 2, 128, 128, 128, 128, 128,
+                            128, None) == 1
+    assert L.gemm_f16_fused(P, P, ep(bias=P + 8), P, 2, 128, 128, 128, 128,
+                            128, 128, None) == 3
+    assert L.gemm_f16_fused(P, P, ep(act=1), P, 2, 128, 128, 0, 128, 128,
+                            128, None) == 2
     # gemm_f16
     assert L.gemm_f16(P, P, P, 0, 128, 128, 128, 128, 128, 128, None) == 1
     assert L.gemm_f16(P, P, P, 2, -1, 128, 128, 128, 128, 128, None) == 2

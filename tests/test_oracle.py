@@ -207,6 +207,19 @@ def test_encode_e5m2_saturates_and_roundtrips():
     assert oracle.encode_e5m2(3 * 2.0 ** -17) == 0x02
 
 
+def test_encode_array_matches_scalar_encoders():
+    g = np.random.default_rng(13)
+    v = np.concatenate([g.standard_normal(3000) * 100, [0.0, -0.0, 1e9,
+                                                          -1e9, 2.0 ** -20]])
+    for fmt, enc in ((oracle.E4M3, oracle.encode_e4m3),
+                     (oracle.E5M2, oracle.encode_e5m2),
+                     (oracle.E2M1, oracle.encode_e2m1)):
+        got = oracle.encode_array(v.reshape(-1, 5), fmt)
+        assert got.shape == (len(v) // 5, 5)
+        assert np.array_equal(got.reshape(-1),
+                              np.array([enc(x) for x in v], dtype=np.uint8))
+
+
 def test_encode_e2m1_hand_values():
     cases = {6.9: 0x7, 100.0: 0x7, 0.25: 0x0, 0.75: 0x2, 2.5: 0x4,
              5.0: 0x6, 1.25: 0x2, 1.75: 0x4, 3.5: 0x6, 0.2: 0x0,
