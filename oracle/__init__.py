@@ -33,6 +33,10 @@ import numpy as np
 E4M3 = 1
 E2M1 = 2
 E5M2 = 3
+INT8 = 4
+INT4 = 5
+INT2 = 6
+INT_BITS = {INT8: 8, INT4: 4, INT2: 2}
 F16 = 2
 BF16 = 1
 ACT_NONE = 0
@@ -76,6 +80,13 @@ def _load():
         lib.mxo_decode_e5m2.argtypes = [u8]
         lib.mxo_encode_e5m2.restype = u8
         lib.mxo_encode_e5m2.argtypes = [dbl]
+        lib.mxo_decode_int.restype = dbl
+        lib.mxo_decode_int.argtypes = [u8, i32]
+        lib.mxo_encode_int.restype = u8
+        lib.mxo_encode_int.argtypes = [dbl, i32]
+        lib.mxo_gemm_a16_bmx.restype = None
+        lib.mxo_gemm_a16_bmx.argtypes = [p, i32, p, p, i32, i64, i64, i64, p,
+                                         i64, p, p]
         lib.mxo_decode_e2m1.restype = dbl
         lib.mxo_decode_e2m1.argtypes = [u8]
         lib.mxo_decode_ue8m0.restype = dbl
@@ -131,6 +142,14 @@ def encode_e5m2(v: float) -> int:
     return int(_load().mxo_encode_e5m2(float(v)))
 
 
+def decode_int(code: int, bits: int) -> float:
+    return _load().mxo_decode_int(int(code) & 0xFF, int(bits))
+
+
+def encode_int(v: float, bits: int) -> int:
+    return int(_load().mxo_encode_int(float(v), int(bits)))
+
+
 def decode_e2m1(code: int) -> float:
     return _load().mxo_decode_e2m1(int(code) & 0xF)
 
@@ -170,7 +189,10 @@ def floor_log2_f32(a: float) -> int:
 
 def decode_table(fmt: int) -> np.ndarray:
     """float64 value of every code: 256 entries for E4M3 / E5M2, 16 for
-    E2M1."""
+    E2M1, 2^bits for the integer formats."""
+    if fmt in INT_BITS:
+        b = INT_BITS[fmt]
+        return np.array([decode_int(c, b) for c in range(1 << b)])
     if fmt == E4M3:
         return np.array([decode_e4m3(c) for c in range(256)])
     if fmt == E5M2:
@@ -269,6 +291,26 @@ def gemm_mx(codesA, scalesA, codesB, scalesB, fmt: int, rows=None,
     lib.mxo_gemm_mx(_ptr(cA), _ptr(sA), _ptr(cB), _ptr(sB), M, N, K, fmt,
                     fmt if fmt_b is None else fmt_b,
                     None if r is None else _ptr(r), nr, _ptr(C), _ptr(S))
+    return C, S
+
+
+def gemm_a16_bmx(A_bits, dtype: int, codesB, scalesB, fmt_b: int, rows=None):
+    """float64 C = A * B_mx^T for a row-major fp16 / bf16 A (uint16 bit
+    patterns, M x K) and an MX tensor B (codes N x K, scales N x K/32) of
+    any element format; also S = sum |products|."""
+    lib = _load()
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    cB = np.ascontiguousarray(codesB, dtype=np.uint8)
+    sB = np.ascontiguousarray(scalesB, dtype=np.uint8)
+    M, K = A.shape
+    N, K2 = cB.shape
+    if K != K2 or sB.shape != (N, K // 32):
+        raise ValueError("shape mismatch")
+    r, nr = _rows_arg(rows, M)
+    C = np.empty((nr, N), dtype=np.float64)
+    S = np.empty((nr, N), dtype=np.float64)
+    lib.mxo_gemm_a16_bmx(_ptr(A), dtype, _ptr(cB), _ptr(sB), fmt_b, M, N, K,
+                         None if r is None else _ptr(r), nr, _ptr(C), _ptr(S))
     return C, S
 
 

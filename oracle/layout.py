@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY.  The oracle itself works on plain arrays: one code
 per byte (outer x K) and a row-major scale matrix (outer x K/32).  The CUDA
 library stores an MX tensor as
 
-  * a data plane, outer x K, K contiguous: E4M3 one code per byte; E2M1 two
-    codes per byte, the element with even k in the low nibble;
+  * a data plane, outer x K, K contiguous: E4M3, E5M2 and int8 one code per
+    byte; E2M1 and int4 two codes per byte, the element with even k in the
+    low nibble; int2 four codes per byte, element k at bits 2*(k % 4);
   * a scale plane in the tensor-core scale-factor layout: the (padded)
     outer x K/32 scale matrix is cut into atoms of 128 rows x 4 scale columns
     (128 K elements); each atom is 512 contiguous bytes in which the scale of
@@ -34,8 +35,13 @@ def scale_plane_bytes(outer: int, K: int) -> int:
     return row_atoms * k_atoms * ATOM_BYTES
 
 
+# bits per element code of each format (1 E4M3, 2 E2M1, 3 E5M2, 4 int8,
+# 5 int4, 6 int2)
+CODE_BITS = {1: 8, 2: 4, 3: 8, 4: 8, 5: 4, 6: 2}
+
+
 def data_plane_bytes(fmt: int, outer: int, K: int) -> int:
-    return outer * K if fmt == 1 else outer * K // 2
+    return outer * K * CODE_BITS[fmt] // 8
 
 
 def _scale_offsets(outer: int, K: int) -> np.ndarray:
@@ -74,6 +80,34 @@ def pack_e2m1(codes: np.ndarray) -> np.ndarray:
     """outer x K nibble codes -> outer x K/2 bytes, even k in the low nibble."""
     c = np.asarray(codes, dtype=np.uint8) & 0xF
     return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def pack_codes(codes: np.ndarray, fmt: int) -> np.ndarray:
+    """outer x K codes (one per byte) -> the library's data plane rows."""
+    bits = CODE_BITS[fmt]
+    c = np.asarray(codes, dtype=np.uint8)
+    if bits == 8:
+        return c.copy()
+    if bits == 4:
+        return pack_e2m1(c)
+    c = c & 0x3
+    return (c[:, 0::4] | (c[:, 1::4] << 2) | (c[:, 2::4] << 4) |
+            (c[:, 3::4] << 6)).astype(np.uint8)
+
+
+def unpack_codes(packed: np.ndarray, fmt: int, K: int) -> np.ndarray:
+    """The library's data plane rows -> outer x K codes (one per byte)."""
+    bits = CODE_BITS[fmt]
+    p = np.asarray(packed, dtype=np.uint8)
+    p = p.reshape(p.shape[0] if p.ndim > 1 else -1, K * bits // 8)
+    if bits == 8:
+        return p.copy()
+    if bits == 4:
+        return unpack_e2m1(p)
+    out = np.empty((p.shape[0], K), dtype=np.uint8)
+    for i in range(4):
+        out[:, i::4] = (p >> (2 * i)) & 0x3
+    return out
 
 
 def unpack_e2m1(packed: np.ndarray) -> np.ndarray:

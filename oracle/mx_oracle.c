@@ -17,6 +17,10 @@
  *    tensor is an E4M3 data plane plus a UE8M0 ("FP8 E8M0") scale plane with
  *    block factors {32, 1}: one scale per 32 consecutive elements of the
  *    innermost (K) dimension.
+ *  - WWDC26 session 330, "Quantized data types" and the custom-format
+ *    passage of "Quantized matrix multiplication": 8-, 4- and 2-bit integer
+ *    element types with the same E8M0 block scales, and a matmul that
+ *    dequantizes one operand to f16 before multiplying.
  *  - The OCP Microscaling (MX) v1.0 definitions of E4M3, E5M2, E2M1 and UE8M0
  *    and of the conversion rule: X = 2^(floor(log2(amax)) - emax_elem),
  *    elements rounded to nearest-even and saturated (E5M2 included: an MX
@@ -40,6 +44,9 @@
 #define MXO_E4M3 1
 #define MXO_E2M1 2
 #define MXO_E5M2 3
+#define MXO_INT8 4
+#define MXO_INT4 5
+#define MXO_INT2 6
 #define MXO_F16 2
 #define MXO_BF16 1
 #define MXO_ACT_NONE 0
@@ -91,6 +98,17 @@ double mxo_decode_e2m1(uint8_t b)
     else
         mag = ldexp(1.0 + m / 2.0, e - 1);
     return s ? -mag : mag;
+}
+
+/* Integer element formats: the low `bits` bits of c as a two's-complement
+ * integer (int8 -128..127, int4 -8..7, int2 -2..1). */
+static int int_bits(int fmt) { return fmt == MXO_INT8 ? 8 : fmt == MXO_INT4 ? 4 : 2; }
+
+double mxo_decode_int(uint8_t c, int bits)
+{
+    int v = c & ((1 << bits) - 1);
+    if (v >= (1 << (bits - 1))) v -= (1 << bits);
+    return (double)v;
 }
 
 /* UE8M0: an unsigned 8-bit exponent; value 2^(c-127); 0xFF is NaN. */
@@ -202,6 +220,26 @@ void mxo_encode_array(const double* v, int64_t n, int fmt, uint8_t* out)
                  : (fmt == MXO_E5M2) ? mxo_encode_e5m2(v[i]) : mxo_encode_e2m1(v[i]);
 }
 
+/* Round v to the nearest integer, ties to the even one (written out from the
+ * definition: the two integers around v and their distances), then saturate
+ * to the two's-complement range of `bits` bits; returns the code's low bits. */
+uint8_t mxo_encode_int(double v, int bits)
+{
+    const double lo = -(double)(1 << (bits - 1)), hi = (double)((1 << (bits - 1)) - 1);
+    double q;
+    if (isnan(v)) return 0;
+    if (v <= lo) q = lo;
+    else if (v >= hi) q = hi;
+    else {
+        double f = floor(v), d = v - f;
+        if (d < 0.5) q = f;
+        else if (d > 0.5) q = f + 1.0;
+        else q = (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+        if (q > hi) q = hi;
+    }
+    return (uint8_t)((int)q & ((1 << bits) - 1));
+}
+
 /* ------------------------------------------------------------------------ */
 /* MX quantizer (OCP MX rule), one 32-element block at a time.               */
 /* ------------------------------------------------------------------------ */
@@ -218,14 +256,18 @@ static int floor_log2(double a)
 int mxo_floor_log2_f32(float a) { return floor_log2((double)a); }
 
 /* Quantize one block of 32 values.  emax is the exponent of the element
- * format's largest power of two (8 for E4M3, 15 for E5M2, 2 for E2M1).
+ * format's largest power of two (8 for E4M3, 15 for E5M2, 2 for E2M1, and
+ * bits - 2 for the integer formats: 64, 4 and 1 are the largest powers of two
+ * that int8, int4 and int2 hold, which for int8 is the OCP MXINT8 rule with
+ * its implicit 2^-6 folded into the scale).
  * Writes 32 codes (one per byte, unpacked) and returns the UE8M0 scale code.
  *   amax = 0          -> scale code 0 (2^-127), all elements +-0
  *   NaN/Inf in block  -> scale code 0xFF (NaN); element codes are then
  *                        meaningless and are written as the encoding of 0. */
 static uint8_t quantize_block(const double x[32], int fmt, uint8_t codes[32])
 {
-    int emax = (fmt == MXO_E4M3) ? 8 : (fmt == MXO_E5M2) ? 15 : 2;
+    const int is_int = (fmt == MXO_INT8 || fmt == MXO_INT4 || fmt == MXO_INT2);
+    int emax = (fmt == MXO_E4M3) ? 8 : (fmt == MXO_E5M2) ? 15 : is_int ? int_bits(fmt) - 2 : 2;
     double amax = 0.0;
     int nonfinite = 0;
     for (int i = 0; i < 32; ++i) {
@@ -246,7 +288,8 @@ static uint8_t quantize_block(const double x[32], int fmt, uint8_t codes[32])
     }
     for (int i = 0; i < 32; ++i) {
         double q = ldexp(x[i], -es);            /* exact in double */
-        codes[i] = (fmt == MXO_E4M3) ? mxo_encode_e4m3(q)
+        codes[i] = is_int ? mxo_encode_int(q, int_bits(fmt))
+                   : (fmt == MXO_E4M3) ? mxo_encode_e4m3(q)
                    : (fmt == MXO_E5M2) ? mxo_encode_e5m2(q) : mxo_encode_e2m1(q);
     }
     return (uint8_t)(es + 127);
@@ -281,6 +324,8 @@ void mxo_quantize(const float* src, int64_t rows, int64_t K, int64_t s_row,
 /* Value of code c of an element format (E2M1 codes in the low nibble). */
 static double decode_fmt(int fmt, int c)
 {
+    if (fmt == MXO_INT8 || fmt == MXO_INT4 || fmt == MXO_INT2)
+        return mxo_decode_int((uint8_t)c, int_bits(fmt));
     return (fmt == MXO_E4M3) ? mxo_decode_e4m3((uint8_t)c)
            : (fmt == MXO_E5M2) ? mxo_decode_e5m2((uint8_t)c)
                                : mxo_decode_e2m1((uint8_t)(c & 15));
@@ -321,6 +366,47 @@ void mxo_gemm_mx(const uint8_t* codesA, const uint8_t* scalesA,
                     double xb = mxo_decode_ue8m0(scalesB[j * nb + b]);
                     for (int64_t k = b * 32; k < b * 32 + 32; ++k) {
                         double p = a[k] * (tabb[codesB[j * K + k]] * xb);
+                        c += p;
+                        s += fabs(p);
+                    }
+                }
+                C[ii * N + j] = c;
+                S[ii * N + j] = s;
+            }
+        }
+        free(a);
+    }
+}
+
+/* C = A * B_mx^T for a row-major fp16 / bf16 A (M x K, bit patterns) and an MX
+ * tensor B (codes N x K of format fmt_b, scales N x K/32): the matmul with one
+ * operand in a custom quantized format, dequantized before the multiply
+ * (WWDC26 session 330, "Quantized matrix multiplication", custom formats).
+ * float64, ascending k; rows / nrows as in mxo_gemm_mx. */
+void mxo_gemm_a16_bmx(const uint16_t* A, int dtype, const uint8_t* codesB,
+                      const uint8_t* scalesB, int fmt_b, int64_t M, int64_t N,
+                      int64_t K, const int64_t* rows, int64_t nrows, double* C,
+                      double* S)
+{
+    (void)M;
+    double tab[256];
+    for (int c = 0; c < 256; ++c) tab[c] = decode_fmt(fmt_b, c);
+    int64_t nb = K / 32;
+#pragma omp parallel
+    {
+        double* a = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t ii = 0; ii < nrows; ++ii) {
+            int64_t i = rows ? rows[ii] : ii;
+            for (int64_t k = 0; k < K; ++k)
+                a[k] = (dtype == MXO_BF16) ? mxo_decode_bf16(A[i * K + k])
+                                           : mxo_decode_f16(A[i * K + k]);
+            for (int64_t j = 0; j < N; ++j) {
+                double c = 0.0, s = 0.0;
+                for (int64_t b = 0; b < nb; ++b) {
+                    double xb = mxo_decode_ue8m0(scalesB[j * nb + b]);
+                    for (int64_t k = b * 32; k < b * 32 + 32; ++k) {
+                        double p = a[k] * (tab[codesB[j * K + k]] * xb);
                         c += p;
                         s += fabs(p);
                     }

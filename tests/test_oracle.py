@@ -583,3 +583,124 @@ def test_epilogue_bias_runs_along_columns():
     assert np.allclose(Yg, x * sp.ndtr(x), rtol=1e-13, atol=1e-300)
     with pytest.raises(ValueError):
         oracle.epilogue(C, bias[:4], oracle.ACT_GELU)
+
+
+# ---------------------------------------------------------------- integer formats
+
+INT_FMTS = [oracle.INT8, oracle.INT4, oracle.INT2]
+
+
+def test_int_decode_matches_twos_complement():
+    ref8 = np.arange(256, dtype=np.int64).astype(np.uint8).view(np.int8)
+    assert np.array_equal(oracle.decode_table(oracle.INT8), ref8.astype(float))
+    assert list(oracle.decode_table(oracle.INT4)) == \
+        [0, 1, 2, 3, 4, 5, 6, 7, -8, -7, -6, -5, -4, -3, -2, -1]
+    assert list(oracle.decode_table(oracle.INT2)) == [0, 1, -2, -1]
+
+
+@pytest.mark.parametrize("fmt", INT_FMTS)
+def test_int_encode_matches_numpy_round_half_even(fmt):
+    bits = oracle.INT_BITS[fmt]
+    lo, hi = -(1 << (bits - 1)), (1 << (bits - 1)) - 1
+    g = np.random.default_rng(bits)
+    v = np.concatenate([g.uniform(lo - 3, hi + 3, 4000),
+                        np.arange(lo - 2, hi + 3) + 0.5,          # ties
+                        np.arange(lo - 2, hi + 3).astype(float)])
+    want = np.clip(np.round(v), lo, hi).astype(np.int64) & ((1 << bits) - 1)
+    got = np.array([oracle.encode_int(x, bits) for x in v])
+    assert np.array_equal(got, want)
+
+
+def test_int_scale_rule_hand_values():
+    c, s = _qblock([1.0, -1.0], oracle.INT8)
+    assert s == 121 and c[0] == 64 and c[1] == 0xC0      # 2^(0-6); +-64
+    c, s = _qblock([1.999], oracle.INT8)                  # 127.9 -> 127
+    assert s == 121 and c[0] == 127
+    c, s = _qblock([100.0, 3.0], oracle.INT8)             # X = 2^(6-6) = 1
+    assert s == 127 and c[0] == 100 and c[1] == 3
+    c, s = _qblock([1.0, 0.3], oracle.INT4)               # X = 2^-2
+    assert s == 125 and c[0] == 4 and c[1] == 1           # 1.2 -> 1
+    c, s = _qblock([1.5, -1.5], oracle.INT2)              # X = 1
+    assert s == 127 and c[0] == 1 and c[1] == 2           # 2 -> 1; -2
+    c, s = _qblock([-0.5, 0.5, 1.0], oracle.INT2)         # ties to even 0
+    assert c[0] == 0 and c[1] == 0
+
+
+@pytest.mark.parametrize("fmt", INT_FMTS)
+def test_int_quantize_properties(fmt):
+    bits = oracle.INT_BITS[fmt]
+    emax = bits - 2
+    g = torch.Generator().manual_seed(40 + bits)
+    x = (torch.randn(16, 256, generator=g) *
+         torch.exp(torch.randn(16, 1, generator=g) * 3)).numpy()
+    codes, scales = oracle.quantize(x, fmt)
+    tab = oracle.decode_table(fmt)
+    lo, hi = tab.min(), tab.max()
+    for r in range(x.shape[0]):
+        for b in range(x.shape[1] // 32):
+            blk = x[r, b * 32:(b + 1) * 32].astype(np.float64)
+            X = 2.0 ** (int(scales[r, b]) - 127)
+            assert X * 2 ** emax <= np.abs(blk).max() < X * 2 ** (emax + 1)
+            q = tab[codes[r, b * 32:(b + 1) * 32]]
+            assert np.array_equal(q, np.clip(np.round(blk / X), lo, hi))
+
+
+@pytest.mark.parametrize("fmt,vmax", [(oracle.INT8, 127), (oracle.INT4, 7),
+                                      (oracle.INT2, 1)])
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.F16])
+def test_gemm_a16_bmx_integer_exact(fmt, vmax, dtype):
+    """Integer sources within the format's range quantize without loss, so
+    the product is the integer product (numpy int64), non-square so that a
+    transposed operand shows."""
+    g = np.random.default_rng(fmt + 10 * dtype)
+    M, N, K = 24, 40, 96
+    A = g.integers(-50, 51, (M, K))
+    B = g.integers(-vmax, vmax + 1, (K, N))
+    tdt = torch.bfloat16 if dtype == oracle.BF16 else torch.float16
+    A_bits = torch.from_numpy(A.astype(np.float32)).to(tdt).view(
+        torch.int16).numpy().view(np.uint16)
+    cb, sb = oracle.quantize(B.astype(np.float32), fmt, k_axis=0)
+    C, S = oracle.gemm_a16_bmx(A_bits, dtype, cb, sb, fmt)
+    assert np.array_equal(C, (A @ B).astype(float))
+    assert np.array_equal(S, (np.abs(A) @ np.abs(B)).astype(float))
+    C2, _ = oracle.gemm_a16_bmx(A_bits, dtype, cb, sb, fmt, rows=[3, 0, 23])
+    assert np.array_equal(C2, C[[3, 0, 23]])
+
+
+@pytest.mark.parametrize("fmt", INT_FMTS + [oracle.E4M3, oracle.E2M1])
+def test_gemm_a16_bmx_brute_force_rationals(fmt):
+    g = np.random.default_rng(77 + fmt)
+    M, N, K = 3, 4, 64
+    A = torch.from_numpy(g.standard_normal((M, K)).astype(np.float32) * 8)
+    A_bits = A.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    a_vals = A.to(torch.bfloat16).to(torch.float64).numpy()
+    ncodes = 16 if fmt == oracle.E2M1 else 1 << layout.CODE_BITS[fmt]
+    cb = g.integers(0, ncodes, (N, K))
+    if fmt == oracle.E4M3:
+        cb[(cb & 0x7F) == 0x7F] = 0x11
+    sb = g.integers(60, 190, (N, K // 32))
+    C, S = oracle.gemm_a16_bmx(A_bits, oracle.BF16, cb.astype(np.uint8),
+                               sb.astype(np.uint8), fmt)
+    tab = (_torch_e4m3_table() if fmt == oracle.E4M3 else
+           np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+           if fmt == oracle.E2M1 else oracle.decode_table(fmt))
+    for i in range(M):
+        for j in range(N):
+            exact = sum(Fraction(float(a_vals[i, k])) *
+                        Fraction(float(tab[cb[j, k]])) *
+                        Fraction(2) ** (int(sb[j, k // 32]) - 127)
+                        for k in range(K))
+            tol = Fraction(float(S[i, j]) * K * 2.0 ** -52)
+            assert abs(Fraction(C[i, j]) - exact) <= tol
+
+
+def test_int2_packing_roundtrip():
+    g = np.random.default_rng(4)
+    codes = g.integers(0, 4, (5, 64)).astype(np.uint8)
+    packed = layout.pack_codes(codes, oracle.INT2)
+    assert packed.shape == (5, 16)
+    assert packed[0, 0] == codes[0, 0] | (codes[0, 1] << 2) | \
+        (codes[0, 2] << 4) | (codes[0, 3] << 6)
+    assert np.array_equal(layout.unpack_codes(packed, oracle.INT2, 64), codes)
+    assert layout.data_plane_bytes(oracle.INT2, 5, 64) == 80
+    assert layout.data_plane_bytes(oracle.E5M2, 5, 64) == 320
