@@ -42,14 +42,17 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # PFLOP/s for bf16 / fp8 / fp4); an E2M1 operand beside an 8-bit one runs at
 # the FP8 rate
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0,
-                 "mxfp8_e5m2": 2.0, "w4a8": 2.0}
+                 "mxfp8_e5m2": 2.0, "w4a8": 2.0,
+                 # weight-only: B dequantized to bf16, the bf16 tensor rate
+                 "w8a16": 1.0, "w4a16": 1.0, "w2a16": 1.0}
 DTYPE_NAME = {"mxfp8": "e4m3", "mxfp4": "e2m1", "mxfp8_e5m2": "e5m2",
               "w4a8": "e4m3 x e2m1"}
 
 
 PROFILES = os.path.join(ROOT, "profiles")
 GEMM_SOURCES = [os.path.join(ROOT, "block_scaled_quantized_mx_gb300", "csrc", f)
-                for f in ("gemm.cu", "ptx.cuh", "common.cuh")]
+                for f in ("gemm.cu", "gemm_common.cuh", "mx_rule.cuh", "ptx.cuh",
+                          "common.cuh")]
 
 
 def gemm_source_hash() -> str:
@@ -222,7 +225,10 @@ def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
     dA, dB = A.to(dev), B.to(dev)
     out_dt = torch.bfloat16 if c.out == "bf16" else torch.float32
     C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
-    if workloads.is_mx(c):
+    if workloads.is_dequant(c):
+        qb = mx.mx_quantize(B.to(dev), workloads.formats(c)[1], k_strided=True)
+        f = lambda: mx.gemm_dequant(dA, qb, out_dtype=out_dt, out=C)  # noqa
+    elif workloads.is_mx(c):
         fa, fb = workloads.formats(c)
         qa = mx.mx_quantize(dA, fa)
         qb = mx.mx_quantize(dB, fb, k_strided=True)
@@ -292,6 +298,14 @@ def time_fused(mx, c, dev, flusher):
     return out
 
 
+def dequant_bytes(c):
+    """Algorithmic bytes of one gemm_dequant: bf16 A read, B's codes and
+    scales read, C written."""
+    bits = {4: 8, 5: 4, 6: 2}[workloads.formats(c)[1]]
+    out_b = 2 if c.out == "bf16" else 4
+    return 2.0 * c.M * c.K + c.N * c.K * bits / 8 + c.N * c.K / 32 + out_b * c.M * c.N
+
+
 def quant_bytes(fmt, rows, K):
     """Algorithmic bytes of one mx_quantize: fp32 in, codes + scales out."""
     code = rows * K / 2 if fmt == 2 else rows * K           # E2M1: 4 bits
@@ -305,6 +319,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     c = workloads.case(args.workload)
+    if workloads.is_dequant(c):
+        raise SystemExit("%s is timed in gemm_only_other_workloads; the step "
+                         "workload is an MX or 16-bit case" % c.name)
     hbm, bf16, bf16_sus, peak_src = peaks()
     stream = torch.cuda.current_stream()
 
@@ -486,6 +503,9 @@ def run_ours(args, rank, world, local_rank):
                                         splitk=args.splitk)
             others[name] = {"gemm_ms": ms_o, "tflops": tf_o,
                             "frac_of_peak": tf_o / (bf16 * NOMINAL_RATIO[oc.kind])}
+            if workloads.is_dequant(oc):
+                gbs = dequant_bytes(oc) / ms_o / 1e6
+                others[name].update({"gbs": gbs, "frac_of_hbm": gbs / hbm})
         del fl
     fused = {}
     if not args.no_fused and rank == 0:
@@ -614,7 +634,8 @@ def parse_args(argv=None):
                     help="total seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--others", default="mxfp8_4096,mxfp4_8192,mxfp4_4096,"
-                    "mxfp8_e5m2_8192,w4a8_8192,"
+                    "mxfp8_e5m2_8192,w4a8_8192,w4a16_8192,w2a16_8192,"
+                    "w4a16_decode,"
                     "bf16_4096,f16_4096,bf16_2048,bf16_1024,proj_qkv,proj_out,"
                     "proj_up,proj_down,mx256",
                     help="workloads whose GEMM alone is also timed (L2 "

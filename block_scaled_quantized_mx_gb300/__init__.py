@@ -23,6 +23,9 @@ from . import _build
 E4M3 = 1
 E2M1 = 2
 E5M2 = 3
+INT8 = 4
+INT4 = 5
+INT2 = 6
 DT_F32, DT_BF16, DT_F16 = 0, 1, 2
 SRC_K_CONTIGUOUS, SRC_K_STRIDED = 0, 1
 ACT_NONE, ACT_GELU, ACT_GELU_TANH = 0, 1, 2
@@ -33,7 +36,8 @@ STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
 
 EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
            "gemm_f16", "mx_gemm_fused", "mx_gemm_fused_quantize",
-           "gemm_f16_fused", "mx_gemm_workspace_bytes", "mx_gemm_splitk",
+           "gemm_f16_fused", "gemm_dequant", "mx_gemm_workspace_bytes",
+           "mx_gemm_splitk",
            "gemm_f16_workspace_bytes", "gemm_f16_splitk",
            "mx_gemm_splitk_noalloc", "mx_last_error",
            "mx_selftest_wait_timeout", "mx_scales_to_rowmajor",
@@ -101,6 +105,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_fused.restype = i32
     L.gemm_f16_fused.argtypes = [p, p, pe, p, i32, i64, i64, i64, i64, i64,
                                  i64, p]
+    L.gemm_dequant.restype = i32
+    L.gemm_dequant.argtypes = [p, i32, i64, i64, pt, pe, p, i32, i64, p]
     L.mx_gemm_workspace_bytes.restype = sz
     L.mx_gemm_workspace_bytes.argtypes = [i32, i64, i64, i64]
     L.mx_gemm_splitk.restype = i32
@@ -322,6 +328,34 @@ def gemm_f16_fused(A: torch.Tensor, B: torch.Tensor,
         B.data_ptr() if B.numel() else None, ctypes.byref(ep),
         out.data_ptr() if out.numel() else None, dt, M, N, K, A.stride(0),
         B.stride(0), out.stride(0), _stream(stream)), "gemm_f16_fused")
+    return out
+
+
+def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
+                 act: int = ACT_NONE, out_dtype=torch.float32,
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C = act(A * dequant(B)^T + bias) for a row-major fp16 / bf16 A
+    (M x K) and an MX tensor B of any format (N x K, quantized from a K x N
+    matrix): B is dequantized to A's type in shared memory."""
+    if A.dtype not in (torch.float16, torch.bfloat16) or A.dim() != 2:
+        raise ValueError("A must be a 2-D fp16 or bf16 tensor")
+    if A.stride(1) != 1:
+        raise ValueError("A must have a unit inner stride")
+    M, K = A.shape
+    if K != B.K:
+        raise ValueError("inner dimensions differ")
+    _check_bias(bias, B.outer)
+    dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    if out is None:
+        out = torch.empty((M, B.outer), dtype=out_dtype, device=A.device)
+    cb, ep = B.c(), _epilogue(bias, act)
+    _check(lib().gemm_dequant(
+        A.data_ptr() if A.numel() else None,
+        DT_F16 if A.dtype == torch.float16 else DT_BF16, M, A.stride(0),
+        ctypes.byref(cb), ctypes.byref(ep),
+        out.data_ptr() if out.numel() else None, dt,
+        out.stride(0) if out.dim() == 2 else B.outer, _stream(stream)),
+        "gemm_dequant")
     return out
 
 

@@ -35,9 +35,16 @@ mx_status check_device() {
 
 mx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
+bool is_int_fmt(int32_t fmt) {
+  return fmt == MX_FMT_INT8 || fmt == MX_FMT_INT4 || fmt == MX_FMT_INT2;
+}
+
 // A and B of one product: equal K; an E2M1 operand beside an 8-bit one is
 // unpacked by TMA, which needs K % 128 == 0 and a 32-byte aligned plane.
 mx_status check_pair(const mx_tensor* A, const mx_tensor* B) {
+  // the tensor cores have no block-scaled integer kind: integer tensors are
+  // B operands of gemm_dequant only
+  if (is_int_fmt(A->fmt) || is_int_fmt(B->fmt)) return MX_ERR_INVALID_ARG;
   if (A->K != B->K) return MX_ERR_SHAPE;
   if ((A->fmt == MX_FMT_E2M1) == (B->fmt == MX_FMT_E2M1)) return MX_OK;
   if (A->outer == 0 || B->outer == 0 || A->K == 0) return MX_OK;
@@ -49,8 +56,7 @@ mx_status check_pair(const mx_tensor* A, const mx_tensor* B) {
 
 mx_status check_tensor(const mx_tensor* t) {
   if (!t) return MX_ERR_INVALID_ARG;
-  if (t->fmt != MX_FMT_E4M3 && t->fmt != MX_FMT_E5M2 && t->fmt != MX_FMT_E2M1)
-    return MX_ERR_INVALID_ARG;
+  if (t->fmt < MX_FMT_E4M3 || t->fmt > MX_FMT_INT2) return MX_ERR_INVALID_ARG;
   if (t->outer < 0 || t->K < 0 || t->outer > kMaxDim || t->K > kMaxDim) return MX_ERR_SHAPE;
   if (t->K % 32) return MX_ERR_SHAPE;
   if (t->outer > 0 && t->K > 0) {
@@ -131,10 +137,9 @@ extern "C" {
 
 size_t mx_data_bytes(int32_t fmt, int64_t outer, int64_t K) {
   if (outer < 0 || K < 0 || K % 32) return 0;
-  if (fmt == MX_FMT_E4M3 || fmt == MX_FMT_E5M2)
-    return static_cast<size_t>(outer) * static_cast<size_t>(K);
-  if (fmt == MX_FMT_E2M1) return static_cast<size_t>(outer) * static_cast<size_t>(K) / 2;
-  return 0;
+  if (fmt < MX_FMT_E4M3 || fmt > MX_FMT_INT2) return 0;
+  return static_cast<size_t>(outer) * static_cast<size_t>(K) *
+         static_cast<size_t>(mxk::code_bits(fmt)) / 8;
 }
 
 size_t mx_scale_bytes(int64_t outer, int64_t K) {
@@ -194,6 +199,7 @@ mx_status mx_gemm_fused_quantize(const mx_tensor* A, const mx_tensor* B,
   if ((s = check_tensor(B)) != MX_OK) return s;
   if ((s = check_pair(A, B)) != MX_OK) return s;
   if ((s = check_tensor(C)) != MX_OK) return s;
+  if (is_int_fmt(C->fmt)) return MX_ERR_INVALID_ARG;
   const int64_t M = A->outer, N = B->outer, K = A->K;
   if (C->outer != M || C->K != N) return MX_ERR_SHAPE;
   mxk::Epilogue e;
@@ -206,6 +212,30 @@ mx_status mx_gemm_fused_quantize(const mx_tensor* A, const mx_tensor* B,
   return from_cuda(mxk::launch_gemm_mx(A->fmt, B->fmt, A->data, A->scales, B->data, B->scales,
                                        C->data, MX_DT_F32, N, M, N, K, nullptr, 0, e,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
+                       const mx_tensor* B, const mx_epilogue* epi, void* C, int32_t c_dtype,
+                       int64_t ldc, void* stream) {
+  mx_status s;
+  if (a_dtype != MX_DT_F16 && a_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if ((s = check_tensor(B)) != MX_OK) return s;
+  mxk::Epilogue e;
+  if ((s = epilogue_from(epi, &e)) != MX_OK) return s;
+  if (M < 0 || M > kMaxDim) return MX_ERR_SHAPE;
+  const int64_t N = B->outer, K = B->K;
+  if (M == 0 || N == 0) return MX_OK;
+  if (K == 0 || K % 64) return MX_ERR_SHAPE;
+  if (!A || !C) return MX_ERR_INVALID_ARG;
+  if (lda < K || lda % 8) return MX_ERR_SHAPE;
+  const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
+  if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(C)) return MX_ERR_ALIGN;
+  if ((s = check_device()) != MX_OK) return s;
+  return from_cuda(mxk::launch_gemm_dequant(a_dtype, A, lda, B->fmt, B->data, B->scales, C,
+                                            c_dtype, ldc, M, N, K, e,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,
@@ -240,8 +270,10 @@ mx_status mx_last_error(void* stream) {
   cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
   const unsigned a = mxk::fetch_and_clear_status_quantize(&e1);
   const unsigned b = mxk::fetch_and_clear_status_gemm(&e2);
-  if (e1 != cudaSuccess || e2 != cudaSuccess) return MX_ERR_CUDA;
-  if ((a | b) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
+  cudaError_t e3 = cudaSuccess;
+  const unsigned c = mxk::fetch_and_clear_status_dq(&e3);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return MX_ERR_CUDA;
+  if ((a | b | c) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
   return MX_OK;
 }
 

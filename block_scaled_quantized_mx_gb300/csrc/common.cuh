@@ -8,7 +8,15 @@
 
 namespace mxk {
 
-enum Format : int { FMT_E4M3 = 1, FMT_E2M1 = 2, FMT_E5M2 = 3 };
+enum Format : int {
+  FMT_E4M3 = 1, FMT_E2M1 = 2, FMT_E5M2 = 3,
+  FMT_INT8 = 4, FMT_INT4 = 5, FMT_INT2 = 6   // two's-complement integer codes
+};
+
+// Bits of one element code.
+__host__ __device__ __forceinline__ int code_bits(int fmt) {
+  return fmt == FMT_INT2 ? 2 : (fmt == FMT_E2M1 || fmt == FMT_INT4) ? 4 : 8;
+}
 enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 enum Act : int { ACT_NONE = 0, ACT_GELU = 1, ACT_GELU_TANH = 2 };
 
@@ -73,6 +81,14 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
                             int64_t ldb, int64_t ldc, void* ws, size_t ws_bytes,
                             const Epilogue& epi, cudaStream_t st);
 
+// C = A * dequant(B)^T for a row-major 16-bit A (a_dtype DT_F16 / DT_BF16,
+// M x K, leading dimension lda) and an MX tensor B of any format (N x K);
+// K a multiple of 64.
+cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt_b,
+                                const void* b_data, const uint8_t* b_sf, void* C, int c_dtype,
+                                int64_t ldc, int64_t M, int64_t N, int64_t K, const Epilogue& epi,
+                                cudaStream_t st);
+
 // Workspace bytes the K-split needs (0: the problem is not split).
 // kind: FMT_E4M3 / FMT_E5M2 (the FP8-rate kernel, also for mixed formats),
 // FMT_E2M1 (both operands E2M1), or 0 for the 16-bit GEMM.
@@ -86,5 +102,6 @@ cudaError_t launch_selftest_timeout(long long limit_cycles, cudaStream_t st);
 // Read and clear the device status word of each translation unit.
 unsigned fetch_and_clear_status_quantize(cudaError_t* err);
 unsigned fetch_and_clear_status_gemm(cudaError_t* err);
+unsigned fetch_and_clear_status_dq(cudaError_t* err);
 
 }  // namespace mxk

@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "mx_rule.cuh"
 #include "ptx.cuh"
 
@@ -50,15 +51,10 @@ namespace {
 __device__ unsigned int g_status_gemm = 0;
 
 enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_MXF8 = 2, KIND_MXF4 = 3 };
-// the form in which the epilogue stores C
-enum Out : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_MX8 = 2, OUT_MX4 = 3 };
 
-constexpr int BM = 128;              // rows of A per CTA
-constexpr int BN = 256;              // columns of C per tile
 constexpr int TMEM_COLS = 512;
 constexpr int SF_TMEM_BASE = 256;
 constexpr int MMAS_PER_SUB = 4;      // 4 x 32 bytes of K per 128-byte sub-tile
-constexpr int GROUP_M = 8;           // raster group height in M tiles
 // warp roles
 constexpr int EPI_WARP0 = 2;         // warps 2..9: epilogue, EPI_COLS columns each
 constexpr int NUM_EPI_WARPS = 8;
@@ -127,19 +123,6 @@ __host__ __device__ constexpr uint32_t idesc_mx() {
          (static_cast<uint32_t>((BM * CG) >> 4) << 24);
 }
 
-struct TileSched {
-  int num_m, num_n, total;   // in tiles of (BM*CG) x BN
-  __host__ __device__ __forceinline__ void tile(int t, int& mb, int& nb) const {
-    const int per_group = GROUP_M * num_n;
-    const int g = t / per_group;
-    const int first_m = g * GROUP_M;
-    const int gsz = min(num_m - first_m, GROUP_M);
-    const int r = t - g * per_group;
-    mb = first_m + r % gsz;
-    nb = r / gsz;
-  }
-};
-
 // Work items: [0, full_tiles) are whole tiles in raster order; the remaining
 // tiles (the last, partial wave) are each split into `split` K ranges, one
 // work item per range, whose fp32 partial tiles go to the workspace and are
@@ -181,120 +164,6 @@ struct WorkList {
 __device__ __forceinline__ void record_timeout(volatile int* abort, unsigned site) {
   *abort = 1;
   atomicOr(&g_status_gemm, STATUS_TIMEOUT | site);
-}
-
-// Kernel-side form of Epilogue (plus the geometry of an MX output's scale
-// plane).
-struct EpiArgs {
-  const float* bias;
-  int act;
-  int q_fmt;
-  uint8_t* q_sf;
-  int64_t q_k_atoms;     // atoms along the columns of C
-  int64_t q_row_atoms;   // atoms along the rows of C
-};
-
-// GELU(x) = x * Phi(x) = x (1 + erf(x / sqrt 2)) / 2.  Inlined, so that the
-// 128 evaluations of one thread interleave.  Where 1 + erf cancels (x below
-// about -4) the result keeps an absolute error near 2^-24 |x| instead of its
-// relative accuracy, far below the product's own accumulation error.
-__device__ __forceinline__ float gelu_exact(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
-}
-
-// The tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
-__device__ __forceinline__ float gelu_tanh(float x) {
-  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.0f + tanhf(u));
-}
-
-// Bias and activation on one thread's EPI_COLS accumulator values of one row
-// of C, columns col0 .. col0 + EPI_COLS - 1 (bias is read below N only).
-template <int NC>
-__device__ __forceinline__ void apply_bias_act(uint32_t (&r)[NC], const EpiArgs& e, int col0,
-                                               int N) {
-  if (e.bias != nullptr) {
-#pragma unroll
-    for (int v = 0; v < NC / 4; ++v) {
-      const int c = col0 + 4 * v;
-      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c + 3 < N) {
-        b = __ldg(reinterpret_cast<const float4*>(e.bias + c));
-      } else {
-        if (c < N) b.x = __ldg(e.bias + c);
-        if (c + 1 < N) b.y = __ldg(e.bias + c + 1);
-        if (c + 2 < N) b.z = __ldg(e.bias + c + 2);
-      }
-      r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + b.x);
-      r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + b.y);
-      r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + b.z);
-      r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + b.w);
-    }
-  }
-  if (e.act == ACT_GELU) {
-#pragma unroll
-    for (int i = 0; i < NC; ++i) r[i] = __float_as_uint(gelu_exact(__uint_as_float(r[i])));
-  } else if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-    for (int i = 0; i < NC; ++i) r[i] = __float_as_uint(gelu_tanh(__uint_as_float(r[i])));
-  }
-}
-
-// Store one row's EPI_COLS values of C as an MX tensor (blocks of 32 along the
-// row, the next layer's K): the OCP rule per block, codes to the data plane
-// (row stride N codes), the row's four scale codes -- one 32-bit word, as
-// col0 is a multiple of 128 -- to the scale plane.  Rows beyond M inside the
-// last row atom and blocks beyond N get scale code 0 (the plane's padding).
-template <int OUT, int NC>
-__device__ __forceinline__ void store_mx_row(const uint32_t (&r)[NC], const EpiArgs& e,
-                                             uint8_t* data, int64_t row, int col0, int M,
-                                             int N) {
-  static_assert(NC == 4 * 32, "one thread stores four whole blocks");
-  if (col0 >= N || (row >> 7) >= e.q_row_atoms) return;
-  uint32_t sf = 0;
-  if (row < M) {
-    const int emax = emax_of_fmt(e.q_fmt);
-    const bool e5 = (e.q_fmt == FMT_E5M2);
-#pragma unroll
-    for (int b = 0; b < NC / 32; ++b) {
-      const int c = col0 + 32 * b;
-      if (c >= N) break;
-      uint32_t a = 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a = max(a, r[32 * b + i] & 0x7FFFFFFFu);
-      uint32_t code;
-      float s;
-      block_scale(a, emax, code, s);
-      sf |= code << (8 * b);
-      const uint32_t* x = r + 32 * b;
-      if (OUT == OUT_MX8) {
-        uint32_t q[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float x0 = __uint_as_float(x[4 * i]) * s, x1 = __uint_as_float(x[4 * i + 1]) * s;
-          const float x2 = __uint_as_float(x[4 * i + 2]) * s, x3 = __uint_as_float(x[4 * i + 3]) * s;
-          q[i] = e5 ? (cvt_e5m2x2(x0, x1) | (cvt_e5m2x2(x2, x3) << 16))
-                    : (cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16));
-        }
-        uint4* dst = reinterpret_cast<uint4*>(data + row * N + c);
-        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-      } else {
-        uint32_t q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t* y = x + 8 * i;
-          q[i] = cvt_e2m1x2(__uint_as_float(y[0]) * s, __uint_as_float(y[1]) * s) |
-                 (cvt_e2m1x2(__uint_as_float(y[2]) * s, __uint_as_float(y[3]) * s) << 8) |
-                 (cvt_e2m1x2(__uint_as_float(y[4]) * s, __uint_as_float(y[5]) * s) << 16) |
-                 (cvt_e2m1x2(__uint_as_float(y[6]) * s, __uint_as_float(y[7]) * s) << 24);
-        }
-        *reinterpret_cast<uint4*>(data + (row * N + c) / 2) = make_uint4(q[0], q[1], q[2], q[3]);
-      }
-    }
-  }
-  *reinterpret_cast<uint32_t*>(e.q_sf + ((row >> 7) * e.q_k_atoms + (col0 >> 7)) * SF_ATOM_BYTES +
-                               sf_in_atom(static_cast<int>(row & 127), 0)) = sf;
 }
 
 template <int KIND, int CG, int STAGES, int KSUB, int OUT>
@@ -705,35 +574,6 @@ reduce_partials_kernel(const float* __restrict__ ws, void* __restrict__ Cptr, in
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D tensor map, row-major rows x cols (cols contiguous).
-bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
-               uint64_t cols, uint64_t rows, uint64_t ld_elems, uint32_t box_cols,
-               uint32_t box_rows, CUtensorMapSwizzle swz) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes)};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 // The scale plane as rows of 512-byte atoms (128 x u32); one box = ck atoms.
 bool make_sf_tmap(CUtensorMap* m, const uint8_t* sf, int64_t outer, int64_t K, int ck) {
@@ -869,6 +709,36 @@ int stage_k(int kind) {
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D tensor map, row-major rows x cols (cols contiguous).
+bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
+               uint64_t cols, uint64_t rows, uint64_t ld_elems, uint32_t box_cols,
+               uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes)};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;

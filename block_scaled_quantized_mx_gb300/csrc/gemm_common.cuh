@@ -1,0 +1,212 @@
+// gemm_common.cuh -- pieces shared by the GEMM kernels (gemm.cu: the
+// tensor-core GEMM on MX and 16-bit operands; dqgemm.cu: the GEMM that
+// dequantizes its B operand in shared memory): tile geometry, the raster
+// order of tiles, and the epilogue (bias, activation, the MX quantization of
+// C) applied to accumulator rows held in registers.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+#include "mx_rule.cuh"
+#include "ptx.cuh"
+
+namespace mxk {
+
+constexpr int BM = 128;              // rows of A per CTA
+constexpr int BN = 256;              // columns of C per tile
+constexpr int GROUP_M = 8;           // raster group height in M tiles
+
+// the form in which the epilogue stores C
+enum Out : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_MX8 = 2, OUT_MX4 = 3 };
+
+// Tiles of (BM*CG) x BN walked in groups of GROUP_M tile rows, so that the
+// clusters running at the same time share A and B tiles in L2.
+struct TileSched {
+  int num_m, num_n, total;   // in tiles of (BM*CG) x BN
+  __host__ __device__ __forceinline__ void tile(int t, int& mb, int& nb) const {
+    const int per_group = GROUP_M * num_n;
+    const int g = t / per_group;
+    const int first_m = g * GROUP_M;
+    const int gsz = min(num_m - first_m, GROUP_M);
+    const int r = t - g * per_group;
+    mb = first_m + r % gsz;
+    nb = r / gsz;
+  }
+};
+
+
+// Kernel-side form of Epilogue (plus the geometry of an MX output's scale
+// plane).
+struct EpiArgs {
+  const float* bias;
+  int act;
+  int q_fmt;
+  uint8_t* q_sf;
+  int64_t q_k_atoms;     // atoms along the columns of C
+  int64_t q_row_atoms;   // atoms along the rows of C
+};
+
+// GELU(x) = x * Phi(x) = x (1 + erf(x / sqrt 2)) / 2.  Inlined, so that the
+// 128 evaluations of one thread interleave.  Where 1 + erf cancels (x below
+// about -4) the result keeps an absolute error near 2^-24 |x| instead of its
+// relative accuracy, far below the product's own accumulation error.
+__device__ __forceinline__ float gelu_exact(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
+}
+
+// The tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+
+// Bias and activation on one thread's EPI_COLS accumulator values of one row
+// of C, columns col0 .. col0 + EPI_COLS - 1 (bias is read below N only).
+template <int NC>
+__device__ __forceinline__ void apply_bias_act(uint32_t (&r)[NC], const EpiArgs& e, int col0,
+                                               int N) {
+  if (e.bias != nullptr) {
+#pragma unroll
+    for (int v = 0; v < NC / 4; ++v) {
+      const int c = col0 + 4 * v;
+      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c + 3 < N) {
+        b = __ldg(reinterpret_cast<const float4*>(e.bias + c));
+      } else {
+        if (c < N) b.x = __ldg(e.bias + c);
+        if (c + 1 < N) b.y = __ldg(e.bias + c + 1);
+        if (c + 2 < N) b.z = __ldg(e.bias + c + 2);
+      }
+      r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + b.x);
+      r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + b.y);
+      r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + b.z);
+      r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + b.w);
+    }
+  }
+  if (e.act == ACT_GELU) {
+#pragma unroll
+    for (int i = 0; i < NC; ++i) r[i] = __float_as_uint(gelu_exact(__uint_as_float(r[i])));
+  } else if (e.act == ACT_GELU_TANH) {
+#pragma unroll
+    for (int i = 0; i < NC; ++i) r[i] = __float_as_uint(gelu_tanh(__uint_as_float(r[i])));
+  }
+}
+
+// Quantize one row's 32 values of C (one block: columns c .. c + 31, c < N,
+// N a multiple of 32) by the OCP rule: codes to the MX data plane (row stride
+// N codes), the block's scale code returned.
+template <int OUT>
+__device__ __forceinline__ uint32_t quantize_block_row(const uint32_t (&x)[32], const EpiArgs& e,
+                                                       uint8_t* data, int64_t row, int c, int N) {
+  uint32_t a = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a = max(a, x[i] & 0x7FFFFFFFu);
+  uint32_t code;
+  float s;
+  block_scale(a, emax_of_fmt(e.q_fmt), code, s);
+  if (OUT == OUT_MX8) {
+    const bool e5 = (e.q_fmt == FMT_E5M2);
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float x0 = __uint_as_float(x[4 * i]) * s, x1 = __uint_as_float(x[4 * i + 1]) * s;
+      const float x2 = __uint_as_float(x[4 * i + 2]) * s, x3 = __uint_as_float(x[4 * i + 3]) * s;
+      q[i] = e5 ? (cvt_e5m2x2(x0, x1) | (cvt_e5m2x2(x2, x3) << 16))
+                : (cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16));
+    }
+    uint4* dst = reinterpret_cast<uint4*>(data + row * N + c);
+    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  } else {
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t* y = x + 8 * i;
+      q[i] = cvt_e2m1x2(__uint_as_float(y[0]) * s, __uint_as_float(y[1]) * s) |
+             (cvt_e2m1x2(__uint_as_float(y[2]) * s, __uint_as_float(y[3]) * s) << 8) |
+             (cvt_e2m1x2(__uint_as_float(y[4]) * s, __uint_as_float(y[5]) * s) << 16) |
+             (cvt_e2m1x2(__uint_as_float(y[6]) * s, __uint_as_float(y[7]) * s) << 24);
+    }
+    *reinterpret_cast<uint4*>(data + (row * N + c) / 2) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+  return code;
+}
+
+// One row's four scale codes for columns col0 .. col0 + 127 (col0 a multiple
+// of 128: one 32-bit word of the scale plane).  Rows beyond M inside the last
+// row atom and blocks beyond N carry code 0, the plane's padding.
+__device__ __forceinline__ void store_mx_scales(uint32_t sf_word, const EpiArgs& e, int64_t row,
+                                                int col0, int N) {
+  if (col0 >= N || (row >> 7) >= e.q_row_atoms) return;
+  *reinterpret_cast<uint32_t*>(e.q_sf + ((row >> 7) * e.q_k_atoms + (col0 >> 7)) * SF_ATOM_BYTES +
+                               sf_in_atom(static_cast<int>(row & 127), 0)) = sf_word;
+}
+
+// Store one row's 128 values of C (columns col0 .. col0 + 127) as an MX
+// tensor: four blocks of 32, then the row's scale word.
+template <int OUT, int NC>
+__device__ __forceinline__ void store_mx_row(const uint32_t (&r)[NC], const EpiArgs& e,
+                                             uint8_t* data, int64_t row, int col0, int M,
+                                             int N) {
+  static_assert(NC == 4 * 32, "one thread stores four whole blocks");
+  uint32_t sf = 0;
+  if (row < M) {
+#pragma unroll
+    for (int b = 0; b < NC / 32; ++b) {
+      const int c = col0 + 32 * b;
+      if (c < N)
+        sf |= quantize_block_row<OUT>(*reinterpret_cast<const uint32_t(*)[32]>(r + 32 * b), e,
+                                      data, row, c, N)
+              << (8 * b);
+    }
+  }
+  store_mx_scales(sf, e, row, col0, N);
+}
+
+// One row's 32 values of a plain C (columns c .. c + 31; fp32, or bf16 RNE),
+// clipped at N.
+template <int OUT>
+__device__ __forceinline__ void store_plain_chunk(const uint32_t (&r)[32], void* C, int64_t ldc,
+                                                  int64_t row, int c, int N) {
+  if (OUT == OUT_BF16) {
+    uint16_t* crow = reinterpret_cast<uint16_t*>(C) + row * ldc;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int cc = c + 8 * v;
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = cvt_bf16x2(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]));
+      if (cc + 7 < N) {
+        *reinterpret_cast<uint4*>(crow + cc) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (cc + e < N) crow[cc + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+      }
+    }
+  } else {
+    float* crow = reinterpret_cast<float*>(C) + row * ldc;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const int cc = c + 4 * v;
+      if (cc + 3 < N) {
+        *reinterpret_cast<uint4*>(crow + cc) =
+            make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (cc + e < N) crow[cc + e] = __uint_as_float(r[4 * v + e]);
+      }
+    }
+  }
+}
+
+// Tensor maps (cuTensorMapEncodeTiled, through the driver entry point):
+// a rows x cols matrix of elem_bytes elements, leading dimension ld_elems, a
+// box of box_cols x box_rows.  Returns false when the driver rejects it.
+bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
+               uint64_t cols, uint64_t rows, uint64_t ld_elems, uint32_t box_cols,
+               uint32_t box_rows, CUtensorMapSwizzle swz);
+
+}  // namespace mxk

@@ -194,6 +194,23 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrive on an mbarrier of another CTA of the cluster with the default
+// (release, CTA-scope) ordering: this thread's earlier writes to its own
+// CTA's shared memory are performed before the arrive.  Used after a proxy
+// fence to hand shared-memory operands written by threads to the pair's
+// tensor core.  A release at cluster scope made each such arrive wait
+// ~0.8 us and halved the throughput of the kernel that uses it.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Make this thread's generic-proxy writes to shared memory visible to the
+// async proxy (the tensor core reading operands through descriptors).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Spin (no suspend) until the phase with the given parity completes, within
 // the same bound as mbar_wait; for short waits on the critical path.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
@@ -394,6 +411,54 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
       "cvt.u32.u8 %0, t;\n\t}"
       : "=r"(r)
       : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two 8-bit float codes (lo in the low byte) -> f16x2 (lo in the low half),
+// exact: every E4M3 / E5M2 value is an f16 value.
+__device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint32_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(codes)));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_f16x2_e5m2x2(uint32_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(codes)));
+  return r;
+}
+
+// One byte of two E2M1 codes (lo in the low nibble) -> f16x2, exact.
+__device__ __forceinline__ uint32_t cvt_f16x2_e2m1x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.u8.u32 t, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(byte));
+  return r;
+}
+
+// Packed f16x2 -> two floats, exact.
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+}
+
+// Two floats -> packed f16x2 (lo in the low half), RNE.
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// a * b + c on packed bf16 pairs, one rounding.
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
 

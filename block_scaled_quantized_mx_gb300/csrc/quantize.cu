@@ -1,5 +1,6 @@
-// quantize.cu -- OCP MX quantization, fp32 -> E4M3 / E5M2 / E2M1 data plane plus
-// UE8M0 scale plane in the tensor-core scale-factor layout.
+// quantize.cu -- OCP MX quantization, fp32 -> an E4M3 / E5M2 / E2M1 / int8 /
+// int4 / int2 data plane plus a UE8M0 scale plane in the tensor-core
+// scale-factor layout.
 //
 // The rule (OCP Microscaling v1.0 conversion; block of 32 along the
 // innermost / K axis as in the WWDC26 session 330 "Multi-plane tensors"
@@ -9,8 +10,11 @@
 //          amax, from the position of its leading one) -- never via a log
 //          function, which can round up just below a power of two
 //   X    = 2^clamp(e - emax, -127, 127), emax = 8 (E4M3) / 15 (E5M2) / 2 (E2M1)
+//          / bits - 2 (int8 6, int4 2, int2 0)
 //   code = e_s + 127 (UE8M0); all-zero block -> 0; NaN/Inf in block -> 0xFF
-//   q_i  = RNE-saturate(x_i / X) to the element format.
+//   q_i  = RNE-saturate(x_i / X) to the element format (for the integers: the
+//          nearest integer, ties to even, saturated to the two's-complement
+//          range).
 // x / X is a multiplication by a power of two in fp32; it is exact except when
 // the product is an fp32 subnormal, which every element format rounds to +-0
 // anyway (the smallest E5M2 subnormal is 2^-16).
@@ -84,16 +88,14 @@ quantize_kcontig(const float* __restrict__ src, int64_t ld, int64_t outer,
       block_scale(a, EMAX, code, s);
       if (r < outer && kvalid) {
         if ((lane & 7) == 0) atom[sf_in_atom(rl, j)] = static_cast<uint8_t>(code);
-        if (FMT != FMT_E2M1) {
-          const uint32_t lo = cvt8x2<FMT>(v[i].x * s, v[i].y * s);
-          const uint32_t hi = cvt8x2<FMT>(v[i].z * s, v[i].w * s);
-          *reinterpret_cast<uint32_t*>(data + r * K + k) = lo | (hi << 16);
-        } else {
-          const uint32_t lo = cvt_e2m1x2(v[i].x * s, v[i].y * s);
-          const uint32_t hi = cvt_e2m1x2(v[i].z * s, v[i].w * s);
-          *reinterpret_cast<uint16_t*>(data + (r * K + k) / 2) =
-              static_cast<uint16_t>(lo | (hi << 8));
-        }
+        const uint32_t c4 = codes4<FMT>(v[i].x * s, v[i].y * s, v[i].z * s, v[i].w * s);
+        constexpr int BITS = (FMT == FMT_INT2) ? 2 : (FMT == FMT_E2M1 || FMT == FMT_INT4) ? 4 : 8;
+        if (BITS == 8)
+          *reinterpret_cast<uint32_t*>(data + r * K + k) = c4;
+        else if (BITS == 4)
+          *reinterpret_cast<uint16_t*>(data + (r * K + k) / 2) = static_cast<uint16_t>(c4);
+        else
+          data[(r * K + k) / 4] = static_cast<uint8_t>(c4);
       }
     }
   }
@@ -160,26 +162,23 @@ quantize_kstrided(const float* __restrict__ src, int64_t ld, int64_t outer,
       float s;
       block_scale(a, EMAX, code, s);
       atom[sf_in_atom(4 * lane + c, w)] = static_cast<uint8_t>(code);
-      if (FMT != FMT_E2M1) {
-        uint32_t q[8];
+      uint32_t c4[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          q[i] = cvt8x2<FMT>(x[4 * i] * s, x[4 * i + 1] * s) |
-                 (cvt8x2<FMT>(x[4 * i + 2] * s, x[4 * i + 3] * s) << 16);
+      for (int i = 0; i < 8; ++i)
+        c4[i] = codes4<FMT>(x[4 * i] * s, x[4 * i + 1] * s, x[4 * i + 2] * s, x[4 * i + 3] * s);
+      constexpr int BITS = (FMT == FMT_INT2) ? 2 : (FMT == FMT_E2M1 || FMT == FMT_INT4) ? 4 : 8;
+      if (BITS == 8) {
         uint4* dst = reinterpret_cast<uint4*>(data + (n + c) * K + kb);
-        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-      } else {
-        uint32_t q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float* y = x + 8 * i;
-          q[i] = cvt_e2m1x2(y[0] * s, y[1] * s) | (cvt_e2m1x2(y[2] * s, y[3] * s) << 8) |
-                 (cvt_e2m1x2(y[4] * s, y[5] * s) << 16) |
-                 (cvt_e2m1x2(y[6] * s, y[7] * s) << 24);
-        }
+        dst[0] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+        dst[1] = make_uint4(c4[4], c4[5], c4[6], c4[7]);
+      } else if (BITS == 4) {
         *reinterpret_cast<uint4*>(data + ((n + c) * K + kb) / 2) =
-            make_uint4(q[0], q[1], q[2], q[3]);
+            make_uint4(c4[0] | (c4[1] << 16), c4[2] | (c4[3] << 16), c4[4] | (c4[5] << 16),
+                       c4[6] | (c4[7] << 16));
+      } else {
+        *reinterpret_cast<uint2*>(data + ((n + c) * K + kb) / 4) =
+            make_uint2(c4[0] | (c4[1] << 8) | (c4[2] << 16) | (c4[3] << 24),
+                       c4[4] | (c4[5] << 8) | (c4[6] << 16) | (c4[7] << 24));
       }
     }
   }
@@ -211,9 +210,14 @@ cudaError_t launch_quantize(const float* src, int64_t ld, int k_strided, int fmt
                             cudaStream_t st) {
   if (outer == 0 || K == 0) return cudaSuccess;
   uint8_t* d = static_cast<uint8_t*>(data);
-  if (fmt == FMT_E4M3) return launch_fmt<FMT_E4M3>(src, ld, k_strided, outer, K, d, scales, st);
-  if (fmt == FMT_E5M2) return launch_fmt<FMT_E5M2>(src, ld, k_strided, outer, K, d, scales, st);
-  return launch_fmt<FMT_E2M1>(src, ld, k_strided, outer, K, d, scales, st);
+  switch (fmt) {
+    case FMT_E4M3: return launch_fmt<FMT_E4M3>(src, ld, k_strided, outer, K, d, scales, st);
+    case FMT_E5M2: return launch_fmt<FMT_E5M2>(src, ld, k_strided, outer, K, d, scales, st);
+    case FMT_INT8: return launch_fmt<FMT_INT8>(src, ld, k_strided, outer, K, d, scales, st);
+    case FMT_INT4: return launch_fmt<FMT_INT4>(src, ld, k_strided, outer, K, d, scales, st);
+    case FMT_INT2: return launch_fmt<FMT_INT2>(src, ld, k_strided, outer, K, d, scales, st);
+    default: return launch_fmt<FMT_E2M1>(src, ld, k_strided, outer, K, d, scales, st);
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -65,12 +65,22 @@ typedef enum mx_format {
   MX_FMT_E2M1 = 2, /* MXFP4: 1 sign, 2 exponent (bias 1), 1 mantissa bit;
                       two codes per byte, the element with even k in the
                       low nibble; max 6                                   */
-  MX_FMT_E5M2 = 3  /* MXFP8 with a wider range: 1 sign, 5 exponent (bias
+  MX_FMT_E5M2 = 3, /* MXFP8 with a wider range: 1 sign, 5 exponent (bias
                       15), 2 mantissa bits; one code per byte; max 57344;
                       0x7C / 0xFC are +-infinity (mx_quantize never writes
                       them, mx_gemm propagates them), 0x7D-0x7F NaN.  The
                       RIGEL summary, Main findings section 3, names E5M2
                       beside E4M3 and notes that it has infinities.       */
+  /* Integer elements (WWDC26 session 330, "Quantized data types": 8-, 4- and
+     2-bit integers under the same E8M0 block scales): two's complement, an
+     element's value is q * X.  mx_quantize uses emax = bits - 2 (the OCP
+     MXINT8 rule for int8) and rounds to the nearest integer, ties to even,
+     saturating.  The tensor cores have no block-scaled integer kind:
+     integer tensors are the B operand of gemm_dequant; mx_gemm and its
+     variants reject them (MX_ERR_INVALID_ARG).                            */
+  MX_FMT_INT8 = 4, /* one code per byte, -128..127                          */
+  MX_FMT_INT4 = 5, /* two codes per byte, even k in the low nibble, -8..7   */
+  MX_FMT_INT2 = 6  /* four codes per byte, element k at bits 2*(k%4), -2..1 */
 } mx_format;
 
 /* Element type of a plain matrix. */
@@ -117,8 +127,8 @@ typedef struct mx_tensor {
   int64_t K;
 } mx_tensor;
 
-/* Bytes of the data plane: outer*K (E4M3, E5M2) or outer*K/2 (E2M1); 0 on
- * bad arguments. */
+/* Bytes of the data plane: outer*K (E4M3, E5M2, int8), outer*K/2 (E2M1,
+ * int4) or outer*K/4 (int2); 0 on bad arguments. */
 size_t mx_data_bytes(int32_t fmt, int64_t outer, int64_t K);
 
 /* Bytes of the scale plane: ceil(outer/128) * ceil(K/128) * 512; 0 on bad
@@ -132,7 +142,8 @@ size_t mx_scale_bytes(int64_t outer, int64_t K);
  * For every row r of out and every block j of 32 consecutive K elements:
  *   amax = max |x| over the block; e = floor(log2(amax)) from the fp32
  *   exponent; X = 2^clamp(e - emax, -127, 127) with emax = 8 (E4M3), 15
- *   (E5M2) or 2 (E2M1); the scale code is log2(X) + 127; each element is
+ *   (E5M2), 2 (E2M1) or bits - 2 (the integer formats); the scale code is
+ *   log2(X) + 127; each element is
  *   x / X rounded to nearest-even and saturated to the format's largest
  *   finite value (for E5M2 too: a block's own maximum, up to 1.99 * 2^15
  *   after scaling, becomes 57344, never an infinity).
@@ -233,6 +244,30 @@ mx_status gemm_f16_fused(const void* A, const void* B, const mx_epilogue* epi,
                          float* C, int32_t ab_dtype, int64_t M, int64_t N,
                          int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                          void* stream);
+
+/*
+ * gemm_dequant -- C = A * dequant(B)^T: a row-major fp16 / bf16 A (M x K)
+ * times an MX tensor B (N x K) of any mx_format, with fp32 accumulation.
+ * WWDC26 session 330, "Quantized matrix multiplication": a quantized format
+ * the matmul cannot take directly is loaded in chunks, dequantized to f16 in
+ * threadgroup memory and multiplied.  Here the CTA pair dequantizes B's codes
+ * and scales into shared memory as a_dtype values and runs the 16-bit tensor
+ * cores; weight-only quantization (int4 / int2 / E2M1 weights, 16-bit
+ * activations) is the intended use.
+ *
+ *   A        device, M x K, row-major, element type a_dtype (MX_DT_F16 or
+ *            MX_DT_BF16); lda >= K, a multiple of 8; 16-byte aligned
+ *   B        any format; K a multiple of 64
+ *   epi      fused epilogue (NULL: none), as for mx_gemm_fused
+ *   C        device, M x N row-major, c_dtype MX_DT_F32 or MX_DT_BF16;
+ *            ldc >= N, ldc * element size a multiple of 16 bytes
+ * A dequantized element q * X must lie in a_dtype's range to be exact
+ * (bf16 holds every code of every format for scales 2^-120 .. 2^120; f16
+ * only values up to 65504).
+ */
+mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
+                       const mx_tensor* B, const mx_epilogue* epi, void* C,
+                       int32_t c_dtype, int64_t ldc, void* stream);
 
 /*
  * K-split variants.  When a problem's tiles leave clusters of SMs idle (a last,

@@ -77,10 +77,7 @@ def lib_quantize_to_oracle_form(q: mx.MXTensor):
     the oracle's plain form, using the oracle's own layout restatement."""
     data = q.data.cpu().numpy()
     sc = q.scales.cpu().numpy()
-    if q.fmt != mx.E2M1:
-        codes = data.reshape(q.outer, q.K)
-    else:
-        codes = layout.unpack_e2m1(data.reshape(q.outer, q.K // 2))
+    codes = layout.unpack_codes(data.reshape(q.outer, -1), q.fmt, q.K)
     return codes, layout.untile_scales(sc, q.outer, q.K)
 
 
@@ -88,10 +85,7 @@ def planes_from_codes(codes: np.ndarray, scales: np.ndarray, fmt: int,
                       device="cuda") -> mx.MXTensor:
     """Build library-format device planes from oracle-form codes."""
     outer, K = codes.shape
-    if fmt != oracle.E2M1:
-        data = codes.reshape(-1)
-    else:
-        data = layout.pack_e2m1(codes).reshape(-1)
+    data = layout.pack_codes(codes, fmt).reshape(-1)
     tiled = layout.tile_scales(scales, K)
     return mx.MXTensor(torch.from_numpy(np.ascontiguousarray(data)).to(device),
                        torch.from_numpy(tiled).to(device), fmt, outer, K)

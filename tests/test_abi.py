@@ -49,6 +49,11 @@ def test_status_strings_and_version(L):
 def test_plane_sizes(L, outer, K):
     assert mx.data_bytes(mx.E4M3, outer, K) == outer * K
     assert mx.data_bytes(mx.E5M2, outer, K) == outer * K
+    assert mx.data_bytes(mx.INT8, outer, K) == outer * K
+    assert mx.data_bytes(mx.INT4, outer, K) == outer * K // 2
+    assert mx.data_bytes(mx.INT2, outer, K) == outer * K // 4
+    for f in (mx.E4M3, mx.E5M2, mx.E2M1, mx.INT8, mx.INT4, mx.INT2):
+        assert mx.data_bytes(f, outer, K) == layout.data_plane_bytes(f, outer, K)
     assert mx.data_bytes(mx.E2M1, outer, K) == outer * K // 2
     assert mx.scale_bytes(outer, K) == layout.scale_plane_bytes(outer, K)
 
@@ -75,9 +80,10 @@ def _t(fmt=mx.E4M3, outer=128, K=128, data=0x1000, scales=0x2000):
 def test_host_validation_without_launch(L):
     P = 0x10000            # never dereferenced: every call fails its checks
     byref = ctypes.byref
+    ep = lambda bias=None, act=0: byref(mx.CEpilogue(bias, act))  # noqa
     # mx_quantize
     assert L.mx_quantize(P, 128, 0, None, None) == 1
-    assert L.mx_quantize(P, 128, 0, byref(_t(fmt=4)), None) == 1
+    assert L.mx_quantize(P, 128, 0, byref(_t(fmt=7)), None) == 1
     assert L.mx_quantize(P, 128, 0, byref(_t(fmt=0)), None) == 1
     assert L.mx_quantize(P, 128, 5, byref(_t()), None) == 1
     assert L.mx_quantize(None, 128, 0, byref(_t()), None) == 1
@@ -108,7 +114,44 @@ def test_host_validation_without_launch(L):
             assert L.mx_gemm(byref(ta), byref(tb), P, 1, 256, None) == 3
             assert L.mx_gemm_splitk(byref(ta), byref(tb), P, 1, 256, None, 0,
                                     None) == 3
-    assert L.mx_gemm(byref(_t(fmt=4)), byref(b), P, 1, 256, None) == 1
+    assert L.mx_gemm(byref(_t(fmt=7)), byref(b), P, 1, 256, None) == 1
+    # integer tensors are gemm_dequant's B operand only
+    for fi in (mx.INT8, mx.INT4, mx.INT2):
+        assert L.mx_gemm(byref(_t(fmt=fi)), byref(b), P, 1, 256, None) == 1
+        assert L.mx_gemm(byref(a), byref(_t(fmt=fi, outer=256)), P, 1, 256,
+                         None) == 1
+        assert L.mx_gemm_fused_quantize(byref(a), byref(b), None,
+                                        byref(_t(fmt=fi, outer=128, K=256)),
+                                        None) == 1
+    # gemm_dequant
+    bq = _t(fmt=mx.INT4, outer=256, K=128)
+    assert L.gemm_dequant(P, 0, 128, 128, byref(bq), None, P, 0, 256,
+                          None) == 1                          # a_dtype f32
+    assert L.gemm_dequant(P, 1, 128, 128, byref(bq), None, P, 2, 256,
+                          None) == 1                          # c_dtype f16
+    assert L.gemm_dequant(P, 1, 128, 128, byref(_t(fmt=7, outer=256)), None,
+                          P, 0, 256, None) == 1
+    assert L.gemm_dequant(P, 1, 128, 96, byref(_t(fmt=mx.INT4, outer=256,
+                                                   K=96)), None, P, 0, 256,
+                          None) == 2                          # K % 64
+    assert L.gemm_dequant(P, 1, 128, 100, byref(bq), None, P, 0, 256,
+                          None) == 2                          # lda % 8
+    assert L.gemm_dequant(P, 1, 128, 64, byref(bq), None, P, 0, 256,
+                          None) == 2                          # lda < K
+    assert L.gemm_dequant(P, 1, 128, 128, byref(bq), None, P, 0, 200,
+                          None) == 2                          # ldc < N
+    assert L.gemm_dequant(P + 8, 1, 128, 128, byref(bq), None, P, 0, 256,
+                          None) == 3
+    assert L.gemm_dequant(P, 1, 128, 128, byref(bq), None, P + 4, 0, 256,
+                          None) == 3
+    assert L.gemm_dequant(None, 1, 128, 128, byref(bq), None, P, 0, 256,
+                          None) == 1
+    assert L.gemm_dequant(P, 1, -1, 128, byref(bq), None, P, 0, 256,
+                          None) == 2
+    assert L.gemm_dequant(None, 1, 0, 128, byref(bq), None, None, 0, 256,
+                          None) == 0                          # M = 0
+    assert L.gemm_dequant(P, 1, 128, 128, byref(bq), ep(act=9), P, 0, 256,
+                          None) == 1
     assert L.mx_gemm(byref(a), byref(_t(outer=256, K=256)), P, 1, 256,
                      None) == 2
     assert L.mx_gemm(byref(a), byref(b), P, 2, 256, None) == 1   # f16 out
@@ -118,7 +161,6 @@ def test_host_validation_without_launch(L):
     assert L.mx_gemm(byref(a), byref(b), P + 8, 1, 256, None) == 3
     assert L.mx_gemm(byref(_t(outer=0)), byref(b), None, 1, 256, None) == 0
     # fused epilogue
-    ep = lambda bias=None, act=0: byref(mx.CEpilogue(bias, act))  # noqa
     assert L.mx_gemm_fused(byref(a), byref(b), ep(act=3), P, 1, 256,
                            None) == 1
     assert L.mx_gemm_fused(byref(a), byref(b), ep(act=-1), P, 1, 256,

@@ -14,7 +14,8 @@ from tests._parity import lib_quantize_to_oracle_form
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [oracle.E4M3, oracle.E5M2, oracle.E2M1]
+FMTS = [oracle.E4M3, oracle.E5M2, oracle.E2M1, oracle.INT8, oracle.INT4,
+        oracle.INT2]
 
 
 @pytest.fixture(scope="module", autouse=True)

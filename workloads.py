@@ -19,6 +19,10 @@ Workloads (sizes and value recipes):
              mxfp8 recipe, bf16 output
   w4a8       mixed MX formats: E4M3 activations (A, the mxfp8 recipe) times
              E2M1 weights (B, N(0, 0.02)), M=N=K in {2048, 8192}, bf16 output
+  w4a16      weight-only quantization: bf16 activations (A, N(0,1)) times
+             int4 weights (B, N(0, 0.02), quantized by the MX rule),
+             M=N=K=8192, and a decode-shaped M=64, N=K=8192; bf16 output
+  w2a16      the same with int2 weights, M=N=K=8192
   proj       transformer projections of a 1B-parameter model at 32 x 512
              tokens (M=16384), hidden 2048, FFN 8192: qkv (K=2048, N=6144),
              out (K=2048, N=2048), up (K=2048, N=8192), down (K=8192,
@@ -37,6 +41,9 @@ import torch
 # 1 = E4M3, 2 = E2M1, 3 = E5M2.
 MX_FORMATS = {"mxfp8": (1, 1), "mxfp4": (2, 2), "mxfp8_e5m2": (3, 3),
               "w4a8": (1, 2)}
+# Weight-only kinds: a bf16 A times an MX tensor B of this format (4 = int8,
+# 5 = int4, 6 = int2), dequantized in the GEMM.
+DEQUANT_FORMATS = {"w8a16": 4, "w4a16": 5, "w2a16": 6}
 
 
 @dataclass(frozen=True)
@@ -103,12 +110,30 @@ def format_cases():
     return out
 
 
+def dequant_cases():
+    out = []
+    for i, (name, kind, M) in enumerate((("w4a16_8192", "w4a16", 8192),
+                                         ("w2a16_8192", "w2a16", 8192),
+                                         ("w4a16_decode", "w4a16", 64))):
+        sa, sb = _seeds(7, i)
+        out.append(GemmCase(name, kind, M, 8192, 8192, "bf16", "normal",
+                            "weight", sa, sb))
+    return out
+
+
 def is_mx(c: GemmCase) -> bool:
     return c.kind in MX_FORMATS
 
 
+def is_dequant(c: GemmCase) -> bool:
+    return c.kind in DEQUANT_FORMATS
+
+
 def formats(c: GemmCase):
-    """(format of A, format of B) of an MX case."""
+    """(format of A, format of B): an MX case's two formats; for a
+    weight-only case (None, B's format), A being bf16."""
+    if c.kind in DEQUANT_FORMATS:
+        return None, DEQUANT_FORMATS[c.kind]
     return MX_FORMATS[c.kind]
 
 
@@ -127,7 +152,7 @@ def proj_cases():
 
 def all_cases():
     return [mx256()] + f16_cases() + mxfp8_cases() + mxfp4_cases() + \
-        format_cases() + proj_cases()
+        format_cases() + dequant_cases() + proj_cases()
 
 
 def case(name: str) -> GemmCase:
@@ -165,6 +190,8 @@ def sources(c: GemmCase, M: int | None = None, N: int | None = None,
     if c.kind in ("f16", "bf16"):
         dt = torch.float16 if c.kind == "f16" else torch.bfloat16
         A, B = A.to(dt), B.to(dt)
+    elif c.kind in DEQUANT_FORMATS:
+        A = A.to(torch.bfloat16)            # B stays fp32: it gets quantized
     return A, B
 
 
@@ -183,7 +210,9 @@ def random_codes(shape, fmt: int, seed: int, scale_lo: int = 112,
         bad = (codes & 0x7F) >= (0x7F if fmt == 1 else 0x7C)
         codes = torch.where(bad, torch.zeros_like(codes), codes)
     else:
-        codes = torch.randint(0, 16, (outer, K), generator=g,
+        # E2M1 and the integer formats: every code of their width is finite
+        ncodes = {2: 16, 4: 256, 5: 16, 6: 4}[fmt]
+        codes = torch.randint(0, ncodes, (outer, K), generator=g,
                               dtype=torch.int32)
     scales = torch.randint(scale_lo, scale_hi + 1, (outer, K // 32),
                            generator=g, dtype=torch.int32)
