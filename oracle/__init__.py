@@ -116,6 +116,9 @@ def _load():
         lib.mxo_gelu_tanh.argtypes = [dbl]
         lib.mxo_epilogue.restype = None
         lib.mxo_epilogue.argtypes = [p, i64, i64, p, i32]
+        lib.mxo_attention.restype = None
+        lib.mxo_attention.argtypes = [p, p, p, i32, i64, i64, i64, i64, dbl, p,
+                                      i64, p, p]
         lib.mxo_num_threads.restype = i32
         lib.mxo_num_threads.argtypes = []
         _lib = lib
@@ -221,6 +224,31 @@ def epilogue(C, bias=None, act: int = ACT_NONE) -> np.ndarray:
     _load().mxo_epilogue(_ptr(Y), rows, N, None if b is None else _ptr(b),
                          int(act))
     return Y
+
+
+def attention(Q_bits, K_bits, V_bits, dtype: int, scale: float | None = None,
+              rows=None):
+    """float64 O = softmax(Q K^T * scale) V per head, and Sv = sum_j w_j |v_j|.
+
+    Q is BH x Lq x d, K and V BH x Lk x d, as uint16 fp16 / bf16 bit
+    patterns; scale defaults to 1/sqrt(d); rows selects query rows (the same
+    rows of every head).  Returns O, Sv of shape BH x len(rows) x d."""
+    Q = np.ascontiguousarray(Q_bits, dtype=np.uint16)
+    K = np.ascontiguousarray(K_bits, dtype=np.uint16)
+    V = np.ascontiguousarray(V_bits, dtype=np.uint16)
+    BH, Lq, d = Q.shape
+    if K.shape != V.shape or K.shape[0] != BH or K.shape[2] != d:
+        raise ValueError("shape mismatch")
+    Lk = K.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    r, nr = _rows_arg(rows, Lq)
+    O = np.empty((BH, nr, d), dtype=np.float64)
+    Sv = np.empty((BH, nr, d), dtype=np.float64)
+    _load().mxo_attention(_ptr(Q), _ptr(K), _ptr(V), dtype, BH, Lq, Lk, d,
+                          float(scale), None if r is None else _ptr(r), nr,
+                          _ptr(O), _ptr(Sv))
+    return O, Sv
 
 
 def num_threads() -> int:

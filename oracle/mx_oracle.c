@@ -487,6 +487,67 @@ void mxo_epilogue(double* C, int64_t rows, int64_t N, const double* bias, int ac
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Attention: O = softmax(Q K^T * scale) V, one head at a time.              */
+/* ------------------------------------------------------------------------ */
+
+/* The computation the FlashAttention kernel of WWDC26 session 330
+ * ("Building advanced ops", 10:27-12:33: Q x K, a row-max reduction, exp,
+ * then the product with V) fuses into one pass, written out as its
+ * definition in float64: for head h and query i,
+ *   s_j = scale * sum_c q_ic k_jc            (j < Lk)
+ *   w_j = exp(s_j - max_j s_j) / sum_j exp(s_j - max_j s_j)
+ *   O_ic = sum_j w_j v_jc,   Sv_ic = sum_j w_j |v_jc|
+ * Q is BH x Lq x d, K and V are BH x Lk x d, fp16 or bf16 bit patterns,
+ * row-major; rows (optional, nrows of them) selects query rows of every head;
+ * O and Sv are BH x nrows x d. */
+void mxo_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int dtype,
+                   int64_t BH, int64_t Lq, int64_t Lk, int64_t d, double scale,
+                   const int64_t* rows, int64_t nrows, double* O, double* Sv)
+{
+    double* tab = (double*)malloc(sizeof(double) * 65536);
+    for (int h = 0; h < 65536; ++h)
+        tab[h] = (dtype == MXO_BF16) ? mxo_decode_bf16((uint16_t)h)
+                                     : mxo_decode_f16((uint16_t)h);
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+#pragma omp for collapse(2) schedule(dynamic, 1)
+        for (int64_t b = 0; b < BH; ++b) {
+            for (int64_t ii = 0; ii < nrows; ++ii) {
+                int64_t i = rows ? rows[ii] : ii;
+                const uint16_t* q = Q + (b * Lq + i) * d;
+                double mx = -INFINITY;
+                for (int64_t j = 0; j < Lk; ++j) {
+                    const uint16_t* k = K + (b * Lk + j) * d;
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < d; ++c) acc += tab[q[c]] * tab[k[c]];
+                    s[j] = scale * acc;
+                    if (s[j] > mx) mx = s[j];
+                }
+                double den = 0.0;
+                for (int64_t j = 0; j < Lk; ++j) {
+                    s[j] = exp(s[j] - mx);
+                    den += s[j];
+                }
+                double* o = O + (b * nrows + ii) * d;
+                double* sv = Sv + (b * nrows + ii) * d;
+                for (int64_t c = 0; c < d; ++c) { o[c] = 0.0; sv[c] = 0.0; }
+                for (int64_t j = 0; j < Lk; ++j) {
+                    const double w = s[j] / den;
+                    const uint16_t* v = V + (b * Lk + j) * d;
+                    for (int64_t c = 0; c < d; ++c) {
+                        o[c] += w * tab[v[c]];
+                        sv[c] += w * fabs(tab[v[c]]);
+                    }
+                }
+            }
+        }
+        free(s);
+    }
+    free(tab);
+}
+
 int mxo_num_threads(void)
 {
     int n = 1;

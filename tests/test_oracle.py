@@ -704,3 +704,65 @@ def test_int2_packing_roundtrip():
     assert np.array_equal(layout.unpack_codes(packed, oracle.INT2, 64), codes)
     assert layout.data_plane_bytes(oracle.INT2, 5, 64) == 80
     assert layout.data_plane_bytes(oracle.E5M2, 5, 64) == 320
+
+
+# ---------------------------------------------------------------- attention
+
+def _bits16(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dt,code", [(torch.bfloat16, oracle.BF16),
+                                     (torch.float16, oracle.F16)])
+def test_attention_matches_torch_sdpa(dt, code):
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(3, 9, 16, generator=g).to(dt)
+    k = torch.randn(3, 13, 16, generator=g).to(dt)
+    v = torch.randn(3, 13, 16, generator=g).to(dt)
+    for scale in (None, 0.3):
+        O, Sv = oracle.attention(_bits16(q), _bits16(k), _bits16(v), code,
+                                 scale=scale)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q.double(), k.double(), v.double(), scale=scale).numpy()
+        assert np.allclose(O, ref, rtol=1e-12, atol=1e-12)
+        assert (Sv >= np.abs(O) - 1e-12).all()
+
+
+def test_attention_closed_forms():
+    g = torch.Generator().manual_seed(5)
+    v = torch.randn(2, 11, 8, generator=g).to(torch.bfloat16)
+    k = torch.randn(2, 11, 8, generator=g).to(torch.bfloat16)
+    q0 = torch.zeros(2, 4, 8, dtype=torch.bfloat16)
+    # Q = 0: every score is 0, the weights uniform: O is the mean of V's rows
+    O, Sv = oracle.attention(_bits16(q0), _bits16(k), _bits16(v), oracle.BF16)
+    vd = v.double().numpy()
+    assert np.allclose(O, vd.mean(axis=1, keepdims=True).repeat(4, axis=1),
+                       rtol=1e-13, atol=1e-15)
+    assert np.allclose(Sv, np.abs(vd).mean(axis=1, keepdims=True).repeat(4, 1))
+    # one key aligned with the query and far larger than the rest: O picks
+    # that key's value row
+    q = torch.zeros(1, 1, 8, dtype=torch.bfloat16)
+    q[0, 0, 3] = 4.0
+    kk = torch.zeros(1, 6, 8, dtype=torch.bfloat16)
+    kk[0, 4, 3] = 64.0                                   # score 256 / sqrt(8)
+    vv = torch.arange(48, dtype=torch.float32).reshape(1, 6, 8).to(torch.bfloat16)
+    O, _ = oracle.attention(_bits16(q), _bits16(kk), _bits16(vv), oracle.BF16)
+    assert np.allclose(O[0, 0], vv[0, 4].double().numpy(), rtol=1e-15)
+
+
+def test_attention_permutation_and_rows():
+    g = torch.Generator().manual_seed(9)
+    q = torch.randn(2, 6, 8, generator=g).to(torch.float16)
+    k = torch.randn(2, 10, 8, generator=g).to(torch.float16)
+    v = torch.randn(2, 10, 8, generator=g).to(torch.float16)
+    O, _ = oracle.attention(_bits16(q), _bits16(k), _bits16(v), oracle.F16)
+    perm = torch.randperm(10, generator=g)
+    Op, _ = oracle.attention(_bits16(q), _bits16(k[:, perm]),
+                             _bits16(v[:, perm]), oracle.F16)
+    assert np.allclose(O, Op, rtol=1e-12, atol=1e-14)     # keys are a set
+    Ok, _ = oracle.attention(_bits16(q), _bits16(k[:, perm]), _bits16(v),
+                             oracle.F16)
+    assert not np.allclose(O, Ok, atol=1e-3)               # K and V paired
+    O2, _ = oracle.attention(_bits16(q), _bits16(k), _bits16(v), oracle.F16,
+                             rows=[5, 0])
+    assert np.array_equal(O2, O[:, [5, 0]])
