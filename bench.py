@@ -298,6 +298,25 @@ def time_fused(mx, c, dev, flusher):
     return out
 
 
+def time_attention(mx, c, dev, flusher):
+    """flash_attention on one attention workload (L2 flushed before each
+    launch): ms, TFLOP/s (4 BH Lq Lk d flop: the two matmuls), the fraction of
+    the bf16 peak, and torch's scaled_dot_product_attention on the same
+    tensors as library context."""
+    Q, K, V = (t.to(dev) for t in workloads.attn_sources(c))
+    O = torch.empty(Q.shape, dtype=torch.bfloat16, device=dev)
+    ms = event_time(lambda: mx.flash_attention(Q, K, V, out_dtype=torch.bfloat16,
+                                               out=O), flusher=flusher)
+    assert mx.mx_last_error() == 0
+    flops = 4.0 * c.BH * c.Lq * c.Lk * c.d
+    sdpa = torch.nn.functional.scaled_dot_product_attention
+    lib_ms = event_time(lambda: sdpa(Q.unsqueeze(0), K.unsqueeze(0), V.unsqueeze(0)),
+                        flusher=flusher)
+    return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "library_reference_ms": lib_ms,
+            "library_reference": "torch scaled_dot_product_attention (context only)"}
+
+
 def dequant_bytes(c):
     """Algorithmic bytes of one gemm_dequant: bf16 A read, B's codes and
     scales read, C written."""
@@ -507,6 +526,15 @@ def run_ours(args, rank, world, local_rank):
                 gbs = dequant_bytes(oc) / ms_o / 1e6
                 others[name].update({"gbs": gbs, "frac_of_hbm": gbs / hbm})
         del fl
+    attention = {}
+    if not args.no_attention and rank == 0:
+        fl = L2Flusher(dev)
+        for name in args.attention.split(","):
+            if name:
+                a = time_attention(mx, workloads.attn_case(name), dev, fl)
+                a["frac_of_peak"] = a["tflops"] / bf16
+                attention[name] = a
+        del fl
     fused = {}
     if not args.no_fused and rank == 0:
         fl = L2Flusher(dev)
@@ -544,6 +572,7 @@ def run_ours(args, rank, world, local_rank):
         "breakdown": extra,
         "gemm_only_other_workloads": others,
         "fused_epilogue": fused,
+        "attention": attention,
         "e2e": e2e,
         "clocks": clk,
     }
@@ -645,6 +674,9 @@ def parse_args(argv=None):
                     help="MX workloads on which the fused bias + GELU epilogue "
                          "is timed against the decomposed path")
     ap.add_argument("--no-fused", action="store_true")
+    ap.add_argument("--attention", default="attn_sam_d64,attn_sam_d128",
+                    help="attention workloads timed with flash_attention")
+    ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--splitk", action="store_true",
                     help="use the K-split GEMM entry points (with a workspace)")
     return ap.parse_args(argv)

@@ -36,7 +36,8 @@ STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
 
 EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
            "gemm_f16", "mx_gemm_fused", "mx_gemm_fused_quantize",
-           "gemm_f16_fused", "gemm_dequant", "mx_gemm_workspace_bytes",
+           "gemm_f16_fused", "gemm_dequant", "flash_attention",
+           "mx_gemm_workspace_bytes",
            "mx_gemm_splitk",
            "gemm_f16_workspace_bytes", "gemm_f16_splitk",
            "mx_gemm_splitk_noalloc", "mx_last_error",
@@ -107,6 +108,9 @@ def lib() -> ctypes.CDLL:
                                  i64, p]
     L.gemm_dequant.restype = i32
     L.gemm_dequant.argtypes = [p, i32, i64, i64, pt, pe, p, i32, i64, p]
+    L.flash_attention.restype = i32
+    L.flash_attention.argtypes = [p, p, p, p, i32, i32, i64, i64, i64, i64,
+                                  ctypes.c_float, p]
     L.mx_gemm_workspace_bytes.restype = sz
     L.mx_gemm_workspace_bytes.argtypes = [i32, i64, i64, i64]
     L.mx_gemm_splitk.restype = i32
@@ -356,6 +360,37 @@ def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
         out.data_ptr() if out.numel() else None, dt,
         out.stride(0) if out.dim() == 2 else B.outer, _stream(stream)),
         "gemm_dequant")
+    return out
+
+
+def flash_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+                    scale: float | None = None, out_dtype=torch.float32,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """O = softmax(Q K^T * scale) V per head.  Q is (..., Lq, d), K and V
+    (..., Lk, d), contiguous fp16 or bf16 CUDA tensors with the same leading
+    dimensions (flattened into heads); scale defaults to 1/sqrt(d)."""
+    if Q.dtype not in (torch.float16, torch.bfloat16) or K.dtype != Q.dtype \
+            or V.dtype != Q.dtype:
+        raise ValueError("Q, K, V must share an fp16 or bf16 dtype")
+    if not (Q.is_contiguous() and K.is_contiguous() and V.is_contiguous()):
+        raise ValueError("Q, K, V must be contiguous")
+    if K.shape != V.shape or Q.shape[:-2] != K.shape[:-2] or \
+            Q.shape[-1] != K.shape[-1]:
+        raise ValueError("shape mismatch")
+    Lq, d = Q.shape[-2], Q.shape[-1]
+    Lk = K.shape[-2]
+    BH = Q.numel() // max(1, Lq * d)
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    odt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16,
+           torch.float16: DT_F16}[out_dtype]
+    if out is None:
+        out = torch.empty(Q.shape, dtype=out_dtype, device=Q.device)
+    ptr = lambda t: t.data_ptr() if t.numel() else None  # noqa
+    _check(lib().flash_attention(
+        ptr(Q), ptr(K), ptr(V), ptr(out),
+        DT_F16 if Q.dtype == torch.float16 else DT_BF16, odt, BH, Lq, Lk, d,
+        float(scale), _stream(stream)), "flash_attention")
     return out
 
 

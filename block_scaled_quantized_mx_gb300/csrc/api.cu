@@ -238,6 +238,26 @@ mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
                                             static_cast<cudaStream_t>(stream)));
 }
 
+mx_status flash_attention(const void* Q, const void* K, const void* V, void* O, int32_t dtype,
+                          int32_t o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
+                          float scale, void* stream) {
+  if (dtype != MX_DT_F16 && dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
+  if (o_dtype != MX_DT_F32 && o_dtype != MX_DT_BF16 && o_dtype != MX_DT_F16)
+    return MX_ERR_INVALID_ARG;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return MX_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return MX_ERR_SHAPE;
+  if (BH < 0 || Lq < 0 || Lk < 0 || BH > 65535 || Lq > kMaxDim || Lk > kMaxDim)
+    return MX_ERR_SHAPE;
+  if (BH == 0 || Lq == 0) return MX_OK;
+  if (Lk == 0) return MX_ERR_SHAPE;
+  if (!Q || !K || !V || !O) return MX_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return MX_ERR_ALIGN;
+  mx_status s = check_device();
+  if (s != MX_OK) return s;
+  return from_cuda(mxk::launch_attention(dtype, Q, K, V, O, o_dtype, BH, Lq, Lk, d, scale,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,
                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                    void* stream) {
@@ -270,10 +290,12 @@ mx_status mx_last_error(void* stream) {
   cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
   const unsigned a = mxk::fetch_and_clear_status_quantize(&e1);
   const unsigned b = mxk::fetch_and_clear_status_gemm(&e2);
-  cudaError_t e3 = cudaSuccess;
+  cudaError_t e3 = cudaSuccess, e4 = cudaSuccess;
   const unsigned c = mxk::fetch_and_clear_status_dq(&e3);
-  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return MX_ERR_CUDA;
-  if ((a | b | c) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
+  const unsigned d = mxk::fetch_and_clear_status_attn(&e4);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess)
+    return MX_ERR_CUDA;
+  if ((a | b | c | d) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
   return MX_OK;
 }
 

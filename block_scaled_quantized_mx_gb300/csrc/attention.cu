@@ -1,0 +1,431 @@
+// attention.cu -- O = softmax(Q K^T * scale) V in one kernel, fp16 / bf16
+// operands, fp32 accumulation, the scores and probabilities never leaving
+// the SM.
+//
+// What is computed follows WWDC26 session 330, "Building advanced ops"
+// (10:27-12:33): per block of keys, S = Q x K^T; a row-max reduction; the
+// exponentials; the product with V, the probabilities fed to that second
+// matmul without a round trip through memory -- FlashAttention.  The running
+// maximum, the running sum and the final division that make the blockwise
+// form equal softmax over all keys are FlashAttention's online softmax.
+//
+// Design (one CTA per (head, block of 128 queries), 6 warps):
+//   * warp 0: TMA -- Q once, then K and V blocks of 128 keys through a
+//     two-deep ring (a 3-D tensor map per operand, so no box crosses heads);
+//   * warp 1: tensor-memory allocation; one thread issues, per key block j,
+//     S_j = Q K_j^T (tcgen05.mma kind::f16, M = 128, N = 128, K = d) into one
+//     of two TMEM score buffers, then O += P_{j-1} V_{j-1} (N = d, K = 128):
+//     the tensor core computes the next scores while the softmax warps work;
+//   * warps 2..5: softmax, one thread per query row: the row's 128 scores
+//     from TMEM, the running maximum, p = 2^(s * scale * log2 e - m) rounded
+//     to the operand type (the running sum adds exactly the rounded values,
+//     so the weights the matmul sees are the ones normalised), P written to
+//     shared memory as the K-major A operand of the second matmul; when a
+//     row's maximum grows, its O row in TMEM is rescaled first (only warps
+//     with such a row wait for the previous P V product); at the end O / sum.
+// Tensor memory: S buffers in columns [0, 128) and [128, 256), O from 256.
+//
+// Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records a
+// timeout in g_status_attn and the CTA shuts down in order.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "ptx.cuh"
+
+namespace mxk {
+
+namespace {
+
+__device__ unsigned int g_status_attn = 0;
+
+constexpr int AT_BQ = 128;          // queries per CTA
+constexpr int AT_BK = 128;          // keys per block
+constexpr int AT_THREADS = 192;     // warps 0, 1 and four softmax warps
+constexpr int AT_TMEM_COLS = 512;
+constexpr int AT_O_COL = 256;
+
+template <int D>
+struct AtSmem {
+  static constexpr int REGION = 128 * 128;          // 128 rows x 128 bytes
+  static constexpr int Q_BYTES = (D / 64) * REGION;
+  static constexpr int K_BYTES = (D / 64) * REGION;
+  static constexpr int V_BYTES = 2 * (D / 64) * 8192; // 2 halves of 64 keys
+  static constexpr int P_BYTES = 2 * REGION;          // 128 keys = 2 regions
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int V_OFF = K_OFF + 2 * K_BYTES;
+  static constexpr int P_OFF = V_OFF + 2 * V_BYTES;
+  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+  // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_empty[2],
+  // p_full[2], p_done[2]
+  static constexpr int MISC_OFF = BAR_OFF + 13 * 8;
+  static constexpr int TOTAL = MISC_OFF + 16;
+  static constexpr int ALLOC = TOTAL + 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void at_timeout(volatile int* abort, unsigned site) {
+  *abort = 1;
+  atomicOr(&g_status_attn, STATUS_TIMEOUT | site);
+}
+
+// kind::f16 instruction descriptor: D f32, A / B f16 or bf16, A K-major,
+// B K-major (b_mn = 0) or MN-major (1), N >> 3 at bit 17, M = 128.
+__device__ __forceinline__ uint32_t at_idesc(bool bf16, uint32_t n, uint32_t b_mn) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (b_mn << 16) |
+         ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// Two probabilities -> a packed pair of the operand type, and the pair's
+// rounded values back as floats (added to the running sum).
+__device__ __forceinline__ uint32_t pack_p(float a, float b, bool bf16, float& ra, float& rb) {
+  if (bf16) {
+    const uint32_t w = cvt_bf16x2(a, b);
+    ra = __uint_as_float(w << 16);
+    rb = __uint_as_float(w & 0xFFFF0000u);
+    return w;
+  }
+  const uint32_t w = cvt_f16x2(a, b);
+  f16x2_to_f32(w, ra, rb);
+  return w;
+}
+
+template <int D>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, void* __restrict__ Optr, int o_dtype,
+                 int Lq, int Lk, float scale_log2e, int bf16) {
+  using L = AtSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t bar_q = base + L::BAR_OFF;
+  const uint32_t bar_k = bar_q + 8;            // [2]
+  const uint32_t bar_v = bar_k + 16;           // [2]
+  const uint32_t bar_kv_empty = bar_v + 16;    // [2]
+  const uint32_t bar_s_full = bar_kv_empty + 16;
+  const uint32_t bar_s_empty = bar_s_full + 16;
+  const uint32_t bar_p_full = bar_s_empty + 16;
+  const uint32_t bar_p_done = bar_p_full + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC_OFF);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int head = blockIdx.y;
+  const int q0 = blockIdx.x * AT_BQ;
+  const int nkb = (Lk + AT_BK - 1) / AT_BK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_k + 8 * i, 1);
+      mbar_init(bar_v + 8 * i, 1);
+      mbar_init(bar_kv_empty + 8 * i, 1);
+      mbar_init(bar_s_full + 8 * i, 1);
+      mbar_init(bar_s_empty + 8 * i, 4);
+      mbar_init(bar_p_full + 8 * i, 4);
+      mbar_init(bar_p_done + 8 * i, 1);
+    }
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) tmem_alloc_cg<1>(smem_u32(tmem_slot), AT_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, L::Q_BYTES);
+      for (int r = 0; r < D / 64; ++r)
+        tma_load_3d(base + L::Q_OFF + r * L::REGION, &tmQ, bar_q, 64 * r, q0, head);
+      int issued = 0;
+      for (int j = 0; j < nkb; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1u;
+        if (!mbar_wait(bar_kv_empty + 8 * st, ph ^ 1u, abort)) {
+          at_timeout(abort, 0x31);
+          // let the copies already issued land before the CTA retires
+          const long long t0 = clock64();
+          while (!mbar_try_wait(bar_q, 0) && clock64() - t0 < MXK_WAIT_LIMIT_CYCLES) {
+          }
+          for (int i = issued >= 2 ? issued - 2 : 0; i < issued; ++i) {
+            const uint32_t pi = (i >> 1) & 1u;
+            const long long t1 = clock64();
+            while ((!mbar_try_wait(bar_k + 8 * (i & 1), pi) ||
+                    !mbar_try_wait(bar_v + 8 * (i & 1), pi)) &&
+                   clock64() - t1 < MXK_WAIT_LIMIT_CYCLES) {
+            }
+          }
+          break;
+        }
+        ++issued;
+        const int k0 = j * AT_BK;
+        mbar_arrive_expect_tx(bar_k + 8 * st, L::K_BYTES);
+        for (int r = 0; r < D / 64; ++r)
+          tma_load_3d(base + L::K_OFF + st * L::K_BYTES + r * L::REGION, &tmK, bar_k + 8 * st,
+                      64 * r, k0, head);
+        mbar_arrive_expect_tx(bar_v + 8 * st, L::V_BYTES);
+        for (int h = 0; h < 2; ++h)
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(base + L::V_OFF + st * L::V_BYTES + h * (D / 64) * 8192 + a * 8192, &tmV,
+                        bar_v + 8 * st, 64 * a, k0 + 64 * h, head);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = at_idesc(bf16 != 0, AT_BK, 0);
+      const uint32_t id_pv = at_idesc(bf16 != 0, D, 1);
+      bool ok = mbar_wait(bar_q, 0, abort);
+      if (!ok) at_timeout(abort, 0x32);
+      tc_fence_after();
+      for (int j = 0; j <= nkb && ok; ++j) {
+        if (j < nkb) {
+          const int st = j & 1;
+          const uint32_t ph = (j >> 1) & 1u;
+          if (!mbar_wait(bar_k + 8 * st, ph, abort) ||
+              !mbar_wait(bar_s_empty + 8 * st, ph ^ 1u, abort)) {
+            at_timeout(abort, 0x33);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t s_t = tmem_base + st * AT_BK;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
+            mma_f16_cg<1>(s_t, smem_desc(base + L::Q_OFF + off, 16, 1024, 2),
+                          smem_desc(base + L::K_OFF + st * L::K_BYTES + off, 16, 1024, 2), id_qk,
+                          kk > 0 ? 1u : 0u);
+          }
+          tc_commit_cg<1>(bar_s_full + 8 * st);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, st = jj & 1;
+          const uint32_t ph = (jj >> 1) & 1u;
+          if (!mbar_wait(bar_p_full + 8 * st, ph, abort) ||
+              !mbar_wait(bar_v + 8 * st, ph, abort)) {
+            at_timeout(abort, 0x34);
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < AT_BK / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * L::REGION + (kk & 3) * 32;
+            const uint32_t boff = (kk >> 2) * (D / 64) * 8192 + (kk & 3) * 2048;
+            mma_f16_cg<1>(tmem_base + AT_O_COL,
+                          smem_desc(base + L::P_OFF + st * L::P_BYTES + aoff, 16, 1024, 2),
+                          smem_desc(base + L::V_OFF + st * L::V_BYTES + boff, 8192, 1024, 2),
+                          id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit_cg<1>(bar_p_done + 8 * st);
+          tc_commit_cg<1>(bar_kv_empty + 8 * st);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int row = 32 * quarter + lane;                  // query row in the block
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+    const bool bf = bf16 != 0;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1u;
+      if (!mbar_wait(bar_s_full + 8 * st, ph, abort)) {
+        at_timeout(abort, 0x35);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s[AT_BK];
+#pragma unroll
+      for (int c = 0; c < AT_BK / 32; ++c)
+        tmem_ld_32x32b_x32(lane_addr + st * AT_BK + 32 * c,
+                           *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_s_empty + 8 * st);
+
+      // scores in log2 units; keys beyond Lk do not exist
+      const int valid = Lk - j * AT_BK;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < AT_BK; ++c) {
+        const float t = c < valid ? __uint_as_float(s[c]) * scale_log2e : -INFINITY;
+        s[c] = __float_as_uint(t);
+        mx = fmaxf(mx, t);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float alpha = ex2_approx(m - m_new);          // 0 on the first block
+      uint32_t pk[AT_BK / 2];
+      float sum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < AT_BK / 2; ++c) {
+        float ra, rb;
+        pk[c] = pack_p(ex2_approx(__uint_as_float(s[2 * c]) - m_new),
+                       ex2_approx(__uint_as_float(s[2 * c + 1]) - m_new), bf, ra, rb);
+        sum += ra + rb;
+      }
+      l = l * alpha + sum;
+
+      // the P buffer is free once the product that read it two blocks ago
+      // is done; O is rescaled (when a row's maximum grew) after the
+      // previous product has accumulated into it
+      if (j >= 2 && !mbar_wait(bar_p_done + 8 * st, ((j - 2) >> 1) & 1u, abort)) {
+        at_timeout(abort, 0x36);
+        ok = false;
+        break;
+      }
+      if (j >= 1 && __any_sync(0xFFFFFFFFu, m_new > m)) {
+        const int jp = j - 1;
+        if (!mbar_wait(bar_p_done + 8 * (jp & 1), (jp >> 1) & 1u, abort)) {
+          at_timeout(abort, 0x37);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(lane_addr + AT_O_COL + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_32x32b_x32(lane_addr + AT_O_COL + 32 * c, o);
+        }
+        tmem_wait_st();
+      }
+      m = m_new;
+
+      // P row: 128 keys = 16 chunks of 8 values, keys 0..63 in the first
+      // 128-byte-swizzled region, 64..127 in the second
+      uint8_t* prow = gbase + L::P_OFF + st * L::P_BYTES + row * 128;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint8_t* dst = prow + (c >> 3) * L::REGION + (((c & 7) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                                    pk[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_full + 8 * st);
+    }
+    if (ok) {
+      const int jl = nkb - 1;
+      if (!mbar_wait(bar_p_done + 8 * (jl & 1), (jl >> 1) & 1u, abort)) {
+        at_timeout(abort, 0x38);
+      } else {
+        tc_fence_after();
+        const int qrow = q0 + row;
+        const float inv = 1.0f / l;
+        const int64_t obase = (static_cast<int64_t>(head) * Lq + qrow) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(lane_addr + AT_O_COL + 32 * c, o);
+          tmem_wait_ld();
+          if (qrow < Lq) {
+            if (o_dtype == DT_F32) {
+              float* dst = reinterpret_cast<float*>(Optr) + obase + 32 * c;
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                *reinterpret_cast<float4*>(dst + 4 * v) =
+                    make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                __uint_as_float(o[4 * v + 2]) * inv,
+                                __uint_as_float(o[4 * v + 3]) * inv);
+            } else {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(Optr) + obase + 32 * c;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float a = __uint_as_float(o[8 * v + 2 * e]) * inv;
+                  const float b = __uint_as_float(o[8 * v + 2 * e + 1]) * inv;
+                  w[e] = (o_dtype == DT_BF16) ? cvt_bf16x2(a, b) : cvt_f16x2(a, b);
+                }
+                *reinterpret_cast<uint4*>(dst + 8 * v) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_cg<1>(tmem_base, AT_TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* O,
+                   int o_dtype, int64_t BH, int Lq, int Lk, float scale_log2e, int bf,
+                   cudaStream_t st) {
+  using L = AtSmem<D>;
+  auto kern = attention_kernel<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid(static_cast<unsigned>((Lq + AT_BQ - 1) / AT_BQ), static_cast<unsigned>(BH));
+  kern<<<grid, AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk, scale_log2e, bf);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(int dtype, const void* Q, const void* K, const void* V, void* O,
+                             int o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
+                             float scale, cudaStream_t st) {
+  if (BH == 0 || Lq == 0) return cudaSuccess;
+  const CUtensorMapDataType dt = (dtype == DT_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  auto enc = [&](CUtensorMap* m, const void* p, uint64_t L, uint32_t by) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(L * d) * 2};
+    cuuint32_t box[3] = {64, by, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return encode_tiled(m, dt, 3, p, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  CUtensorMap tq, tk, tv;
+  if (!enc(&tq, Q, Lq, 128) || !enc(&tk, K, Lk, 128) || !enc(&tv, V, Lk, 64))
+    return cudaErrorInvalidValue;
+  const float sl2 = scale * 1.4426950408889634f;
+  const int bf = (dtype == DT_BF16) ? 1 : 0;
+  const int lq = static_cast<int>(Lq), lk = static_cast<int>(Lk);
+  if (d == 64) return at_run<64>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, bf, st);
+  return at_run<128>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, bf, st);
+}
+
+unsigned fetch_and_clear_status_attn(cudaError_t* err) {
+  unsigned v = 0, z = 0;
+  *err = cudaMemcpyFromSymbol(&v, g_status_attn, sizeof(v));
+  if (*err == cudaSuccess) *err = cudaMemcpyToSymbol(g_status_attn, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace mxk

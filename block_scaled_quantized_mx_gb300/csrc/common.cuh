@@ -89,6 +89,13 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
                                 int64_t ldc, int64_t M, int64_t N, int64_t K, const Epilogue& epi,
                                 cudaStream_t st);
 
+// O = softmax(Q K^T * scale) V for BH heads: Q BH x Lq x d, K and V
+// BH x Lk x d, row-major, dtype DT_F16 / DT_BF16; d 64 or 128; O BH x Lq x d
+// of o_dtype (DT_F32, DT_BF16 or DT_F16).
+cudaError_t launch_attention(int dtype, const void* Q, const void* K, const void* V, void* O,
+                             int o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
+                             float scale, cudaStream_t st);
+
 // Workspace bytes the K-split needs (0: the problem is not split).
 // kind: FMT_E4M3 / FMT_E5M2 (the FP8-rate kernel, also for mixed formats),
 // FMT_E2M1 (both operands E2M1), or 0 for the 16-bit GEMM.
@@ -103,5 +110,6 @@ cudaError_t launch_selftest_timeout(long long limit_cycles, cudaStream_t st);
 unsigned fetch_and_clear_status_quantize(cudaError_t* err);
 unsigned fetch_and_clear_status_gemm(cudaError_t* err);
 unsigned fetch_and_clear_status_dq(cudaError_t* err);
+unsigned fetch_and_clear_status_attn(cudaError_t* err);
 
 }  // namespace mxk

@@ -725,6 +725,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D tensor map, row-major rows x cols (cols contiguous).
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  return enc(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes,
                uint64_t cols, uint64_t rows, uint64_t ld_elems, uint32_t box_cols,
                uint32_t box_rows, CUtensorMapSwizzle swz) {

@@ -209,4 +209,10 @@ bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem
                uint64_t cols, uint64_t rows, uint64_t ld_elems, uint32_t box_cols,
                uint32_t box_rows, CUtensorMapSwizzle swz);
 
+// Any rank: dims / box / element strides innermost first, strides in bytes
+// for dimensions 1 .. rank-1.
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  const cuuint32_t* estr, CUtensorMapSwizzle swz);
+
 }  // namespace mxk

@@ -270,6 +270,29 @@ mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
                        int32_t c_dtype, int64_t ldc, void* stream);
 
 /*
+ * flash_attention -- O = softmax(Q K^T * scale) V for BH independent heads,
+ * in one kernel: the scores and probabilities stay on the SM (WWDC26
+ * session 330, "Building advanced ops": Q x K, a row-max reduction, the
+ * exponentials and the product with V fused, the probabilities handed to the
+ * second matmul without a round trip through memory -- FlashAttention).
+ *
+ *   Q        device, BH x Lq x d, row-major, dtype (MX_DT_F16 / MX_DT_BF16)
+ *   K, V     device, BH x Lk x d, row-major, dtype
+ *   O        device, BH x Lq x d, row-major, o_dtype (MX_DT_F32, MX_DT_BF16
+ *            or MX_DT_F16); every pointer 16-byte aligned
+ *   d        64 or 128; Lk >= 1 when Lq >= 1; BH <= 65535
+ *   scale    multiplies Q K^T (commonly 1/sqrt(d)); finite
+ * The scores accumulate in fp32; the probabilities are rounded to dtype
+ * before the product with V, and the row sums add exactly those rounded
+ * values, so each output row is a weighted mean of V's rows whose weights
+ * differ from the exact softmax by at most that rounding (relative 2^-8 for
+ * bf16, 2^-11 for f16).  No mask.
+ */
+mx_status flash_attention(const void* Q, const void* K, const void* V, void* O,
+                          int32_t dtype, int32_t o_dtype, int64_t BH, int64_t Lq,
+                          int64_t Lk, int64_t d, float scale, void* stream);
+
+/*
  * K-split variants.  When a problem's tiles leave clusters of SMs idle (a last,
  * partial wave of tiles, or fewer tiles than cluster slots), these calls
  * split the affected tiles along K across the idle clusters: each part writes

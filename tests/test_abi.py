@@ -195,6 +195,21 @@ def test_host_validation_without_launch(L):
                             128, 128, None) == 3
     assert L.gemm_f16_fused(P, P, ep(act=1), P, 2, 128, 128, 0, 128, 128,
                             128, None) == 2
+    # flash_attention
+    fa = L.flash_attention
+    assert fa(P, P, P, P, 0, 0, 2, 128, 128, 64, 0.125, None) == 1      # f32 in
+    assert fa(P, P, P, P, 1, 5, 2, 128, 128, 64, 0.125, None) == 1      # o_dtype
+    assert fa(P, P, P, P, 1, 0, 2, 128, 128, 96, 0.125, None) == 2      # d
+    assert fa(P, P, P, P, 1, 0, 2, 128, 0, 64, 0.125, None) == 2        # Lk = 0
+    assert fa(P, P, P, P, 1, 0, 70000, 128, 128, 64, 0.125, None) == 2  # BH
+    assert fa(P, P, P, P, 1, 0, -1, 128, 128, 64, 0.125, None) == 2
+    assert fa(P, P, P, P, 1, 0, 2, 128, 128, 64, float("nan"), None) == 1
+    assert fa(P, P, P, P, 1, 0, 2, 128, 128, 64, float("inf"), None) == 1
+    assert fa(P + 8, P, P, P, 1, 0, 2, 128, 128, 64, 0.125, None) == 3
+    assert fa(P, P, P, P + 2, 1, 0, 2, 128, 128, 64, 0.125, None) == 3
+    assert fa(None, P, P, P, 1, 0, 2, 128, 128, 64, 0.125, None) == 1
+    assert fa(None, None, None, None, 1, 0, 0, 128, 128, 64, 0.125, None) == 0
+    assert fa(None, None, None, None, 1, 0, 2, 0, 128, 64, 0.125, None) == 0
     # gemm_f16
     assert L.gemm_f16(P, P, P, 0, 128, 128, 128, 128, 128, 128, None) == 1
     assert L.gemm_f16(P, P, P, 2, -1, 128, 128, 128, 128, 128, None) == 2

@@ -1,0 +1,138 @@
+"""flash_attention on the GPU vs the float64 oracle.
+
+Tolerance (per element, Sv = sum_j w_j |v_jc| from the oracle): the kernel
+rounds each probability to the operand type (relative 2^-9 for bf16, 2^-12
+for f16) and normalises by the sum of exactly those rounded values, so each
+weight moves by at most twice that and each output by at most
+2^-8 Sv (bf16) / 2^-11 Sv (f16); the bound used allows twice that, plus one
+ulp of a 16-bit output.  The fp32 scores and the hardware 2^x add far less.
+
+Covered: d = 64 and 128, both operand types, fp32 / bf16 / f16 outputs,
+ragged query and key counts (a partial last key block, a single key, a
+single query), a long key sequence whose maximum grows block after block
+(the rescaling path), the closed form Q = 0, determinism, and sampled rows
+of the full-size workloads."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_quantized_mx_gb300 as mx
+import oracle
+import workloads
+from tests._parity import nan_like, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 2.0 ** -7, torch.float16: 2.0 ** -10}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    mx.build()
+    mx.lib()
+
+
+def _bits(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _ulp_f16(x):
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, 2.0 ** (np.maximum(e, -14) - 10), 2.0 ** -24)
+
+
+def _check(O, Q, K, V, scale=None, rows=None, what=""):
+    code = oracle.BF16 if Q.dtype == torch.bfloat16 else oracle.F16
+    Oref, Sv = oracle.attention(_bits(Q), _bits(K), _bits(V), code,
+                                scale=scale, rows=rows)
+    Og = O.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        Og = Og[:, rows]
+    assert np.isfinite(Og).all(), f"{what}: non-finite output"
+    bound = TOL[Q.dtype] * Sv
+    if O.dtype == torch.bfloat16:
+        bound = bound + ulp_bf16(Oref)
+    elif O.dtype == torch.float16:
+        bound = bound + _ulp_f16(Oref)
+    err = np.abs(Og - Oref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} out of "
+                           f"tolerance; worst ratio {(err / bound).max():.3g}")
+    return float((err / np.maximum(Sv, 1e-30)).max())
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("BH,Lq,Lk", [(2, 256, 256), (3, 200, 300),
+                                      (1, 1, 77), (2, 130, 1),
+                                      (1, 384, 1000)])
+def test_attention_shapes(dt, d, BH, Lq, Lk):
+    g = torch.Generator().manual_seed(BH + Lq + 7 * Lk + d)
+    Q = torch.randn(BH, Lq, d, generator=g).to(dt)
+    K = torch.randn(BH, Lk, d, generator=g).to(dt)
+    V = torch.randn(BH, Lk, d, generator=g).to(dt)
+    O = nan_like((BH, Lq, d), torch.float32)
+    mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), out=O)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, what=f"{dt} d{d} {BH}x{Lq}x{Lk}")
+
+
+@pytest.mark.parametrize("odt", [torch.bfloat16, torch.float16])
+def test_attention_16bit_output(odt):
+    g = torch.Generator().manual_seed(3)
+    Q, K, V = (torch.randn(2, 256, 128, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    O = mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), out_dtype=odt)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, what=str(odt))
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_attention_growing_maximum(dt):
+    """Keys whose norm grows along the sequence, with a large scale: the row
+    maximum increases in every key block, so every block rescales O."""
+    g = torch.Generator().manual_seed(11)
+    Lk = 1536
+    Q = torch.randn(2, 256, 64, generator=g).to(dt)
+    grow = torch.linspace(0.2, 3.0, Lk).reshape(1, Lk, 1)
+    K = (torch.randn(2, Lk, 64, generator=g).abs() * grow).to(dt)
+    Q = Q.abs()
+    V = torch.randn(2, Lk, 64, generator=g).to(dt)
+    O = mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), scale=0.5)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, scale=0.5, what="growing maximum")
+
+
+def test_attention_zero_queries_average_values():
+    g = torch.Generator().manual_seed(2)
+    Q = torch.zeros(2, 130, 128, dtype=torch.bfloat16)
+    K = torch.randn(2, 700, 128, generator=g).to(torch.bfloat16)
+    V = torch.randn(2, 700, 128, generator=g).to(torch.bfloat16)
+    O = mx.flash_attention(Q.cuda(), K.cuda(), V.cuda()).cpu().numpy()
+    assert mx.mx_last_error() == 0
+    mean = V.double().numpy().mean(axis=1, keepdims=True)
+    # equal weights, each exactly representable: only fp32 sums remain
+    assert np.allclose(O, np.repeat(mean, 130, axis=1), rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("name", ["attn_sam_d64", "attn_sam_d128"])
+def test_attention_workload_sampled(name):
+    c = workloads.attn_case(name)
+    Q, K, V = workloads.attn_sources(c)
+    O = nan_like((c.BH, c.Lq, c.d), torch.float32)
+    mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), out=O)
+    assert mx.mx_last_error() == 0
+    g = np.random.default_rng(c.seed)
+    rows = sorted(set([0, 127, 128, c.Lq - 1] +
+                      g.integers(0, c.Lq, 8).tolist()))
+    _check(O, Q, K, V, rows=rows, what=name)
+
+
+def test_attention_deterministic():
+    g = torch.Generator().manual_seed(6)
+    Q, K, V = (torch.randn(4, 512, 128, generator=g).to(torch.bfloat16).cuda()
+               for _ in range(3))
+    O1 = mx.flash_attention(Q, K, V)
+    O2 = mx.flash_attention(Q, K, V)
+    assert torch.equal(O1, O2)

@@ -23,6 +23,10 @@ Workloads (sizes and value recipes):
              int4 weights (B, N(0, 0.02), quantized by the MX rule),
              M=N=K=8192, and a decode-shaped M=64, N=K=8192; bf16 output
   w2a16      the same with int2 weights, M=N=K=8192
+  attn       fused attention over image tokens: 2 images x 16 heads, 4096
+             tokens each (a 64 x 64 patch grid, the image-segmentation model
+             the FlashAttention chapter integrates into), d = 64 and 128,
+             Q / K / V N(0,1) rounded to bf16
   proj       transformer projections of a 1B-parameter model at 32 x 512
              tokens (M=16384), hidden 2048, FFN 8192: qkv (K=2048, N=6144),
              out (K=2048, N=2048), up (K=2048, N=8192), down (K=8192,
@@ -193,6 +197,43 @@ def sources(c: GemmCase, M: int | None = None, N: int | None = None,
     elif c.kind in DEQUANT_FORMATS:
         A = A.to(torch.bfloat16)            # B stays fp32: it gets quantized
     return A, B
+
+
+@dataclass(frozen=True)
+class AttnCase:
+    name: str
+    BH: int            # batch x heads
+    Lq: int
+    Lk: int
+    d: int
+    dtype: str         # "bf16" | "f16"
+    seed: int
+
+
+def attn_cases():
+    return [AttnCase(f"attn_sam_d{d}", 32, 4096, 4096, d, "bf16", 8000 + d)
+            for d in (64, 128)]
+
+
+def attn_case(name: str) -> AttnCase:
+    for c in attn_cases():
+        if c.name == name:
+            return c
+    raise KeyError(name)
+
+
+def attn_sources(c: AttnCase, BH: int | None = None, Lq: int | None = None,
+                 Lk: int | None = None):
+    """(Q, K, V): BH x Lq x d and BH x Lk x d, N(0,1) rounded to c.dtype,
+    each from its own seeded stream."""
+    BH = c.BH if BH is None else BH
+    Lq = c.Lq if Lq is None else Lq
+    Lk = c.Lk if Lk is None else Lk
+    dt = torch.bfloat16 if c.dtype == "bf16" else torch.float16
+    Q = draw((BH, Lq, c.d), "normal", c.seed + 1).to(dt)
+    K = draw((BH, Lk, c.d), "normal", c.seed + 2).to(dt)
+    V = draw((BH, Lk, c.d), "normal", c.seed + 3).to(dt)
+    return Q, K, V
 
 
 def random_codes(shape, fmt: int, seed: int, scale_lo: int = 112,
