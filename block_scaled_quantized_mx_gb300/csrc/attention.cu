@@ -9,21 +9,28 @@
 // maximum, the running sum and the final division that make the blockwise
 // form equal softmax over all keys are FlashAttention's online softmax.
 //
-// Design (one CTA per (head, block of 128 queries), 6 warps):
-//   * warp 0: TMA -- Q once, then K and V blocks of 128 keys through a
-//     two-deep ring (a 3-D tensor map per operand, so no box crosses heads);
-//   * warp 1: tensor-memory allocation; one thread issues, per key block j,
-//     S_j = Q K_j^T (tcgen05.mma kind::f16, M = 128, N = 128, K = d) into one
-//     of two TMEM score buffers, then O += P_{j-1} V_{j-1} (N = d, K = 128):
-//     the tensor core computes the next scores while the softmax warps work;
-//   * warps 2..5: softmax, one thread per query row: the row's 128 scores
-//     from TMEM, the running maximum, p = 2^(s * scale * log2 e - m) rounded
-//     to the operand type (the running sum adds exactly the rounded values,
-//     so the weights the matmul sees are the ones normalised), P written to
-//     shared memory as the K-major A operand of the second matmul; when a
-//     row's maximum grows, its O row in TMEM is rescaled first (only warps
-//     with such a row wait for the previous P V product); at the end O / sum.
-// Tensor memory: S buffers in columns [0, 128) and [128, 256), O from 256.
+// Design (one CTA per (head, 256 queries), 10 warps, two query tiles of 128
+// that take turns on the tensor core):
+//   * warp 0: TMA -- both Q tiles once, then K and V blocks of 128 keys
+//     through a two-deep ring (3-D tensor maps, so no box crosses heads);
+//   * warp 1: tensor-memory allocation; one thread issues, per key block j
+//     and tile t, O_t += P_t,{j-1} V_{j-1} and then S_t,j = Q_t K_j^T
+//     (tcgen05.mma kind::f16, M = 128): while one tile's softmax warps work,
+//     the tensor core runs the other tile's two products;
+//   * warps 2..5 (tile 0) and 6..9 (tile 1): softmax, one thread per query
+//     row: the row's 128 scores from TMEM into registers, scaled to log2
+//     units, their maximum, p = 2^(x - m) rounded to the operand type (the
+//     running sum adds exactly the rounded values), written back over the
+//     scores as the packed A operand of
+//     the P V product, which reads it from tensor memory -- the
+//     probabilities never touch shared memory.  When a row's maximum grows,
+//     its O row is rescaled in TMEM first.  At the end O / sum.
+// Ordering: the MMA thread issues P_{j-1} V before S_j, and a commit covers
+// every earlier operation of its thread, so once S_t,j is complete so is
+// the previous product that read P_t and accumulated into O_t: the softmax
+// warps may then rescale O_t and overwrite P_t without another wait.
+// Tensor memory: tile t's S (and P) in columns [256 t, 256 t + 128), its O
+// in [256 t + 128, 256 t + 128 + d).
 //
 // Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records a
 // timeout in g_status_attn and the CTA shuts down in order.
@@ -39,26 +46,22 @@ namespace {
 
 __device__ unsigned int g_status_attn = 0;
 
-constexpr int AT_BQ = 128;          // queries per CTA
+constexpr int AT_BQ = 128;          // queries per tile (two tiles per CTA)
 constexpr int AT_BK = 128;          // keys per block
-constexpr int AT_THREADS = 192;     // warps 0, 1 and four softmax warps
+constexpr int AT_THREADS = 320;     // warps 0, 1 and two softmax warpgroups
 constexpr int AT_TMEM_COLS = 512;
-constexpr int AT_O_COL = 256;
 
 template <int D>
 struct AtSmem {
   static constexpr int REGION = 128 * 128;          // 128 rows x 128 bytes
-  static constexpr int Q_BYTES = (D / 64) * REGION;
+  static constexpr int Q_BYTES = (D / 64) * REGION; // one tile
   static constexpr int K_BYTES = (D / 64) * REGION;
   static constexpr int V_BYTES = 2 * (D / 64) * 8192; // 2 halves of 64 keys
-  static constexpr int P_BYTES = 2 * REGION;          // 128 keys = 2 regions
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr int V_OFF = K_OFF + 2 * K_BYTES;
-  static constexpr int P_OFF = V_OFF + 2 * V_BYTES;
-  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
-  // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_empty[2],
-  // p_full[2], p_done[2]
+  static constexpr int BAR_OFF = V_OFF + 2 * V_BYTES;
+  // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2]
   static constexpr int MISC_OFF = BAR_OFF + 13 * 8;
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
@@ -103,20 +106,19 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint8_t* gbase = smem_raw + (base - raw);
 
   const uint32_t bar_q = base + L::BAR_OFF;
-  const uint32_t bar_k = bar_q + 8;            // [2]
-  const uint32_t bar_v = bar_k + 16;           // [2]
-  const uint32_t bar_kv_empty = bar_v + 16;    // [2]
-  const uint32_t bar_s_full = bar_kv_empty + 16;
-  const uint32_t bar_s_empty = bar_s_full + 16;
-  const uint32_t bar_p_full = bar_s_empty + 16;
-  const uint32_t bar_p_done = bar_p_full + 16;
+  const uint32_t bar_k = bar_q + 8;            // [2] ring stage
+  const uint32_t bar_v = bar_k + 16;           // [2] ring stage
+  const uint32_t bar_kv_empty = bar_v + 16;    // [2] ring stage
+  const uint32_t bar_s_full = bar_kv_empty + 16;   // [2] tile
+  const uint32_t bar_p_full = bar_s_full + 16;     // [2] tile
+  const uint32_t bar_o_done = bar_p_full + 16;     // [2] tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC_OFF);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int head = blockIdx.y;
-  const int q0 = blockIdx.x * AT_BQ;
+  const int q0 = blockIdx.x * 2 * AT_BQ;
   const int nkb = (Lk + AT_BK - 1) / AT_BK;
 
   if (threadIdx.x == 0) {
@@ -126,9 +128,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(bar_v + 8 * i, 1);
       mbar_init(bar_kv_empty + 8 * i, 1);
       mbar_init(bar_s_full + 8 * i, 1);
-      mbar_init(bar_s_empty + 8 * i, 4);
       mbar_init(bar_p_full + 8 * i, 4);
-      mbar_init(bar_p_done + 8 * i, 1);
+      mbar_init(bar_o_done + 8 * i, 1);
     }
     *abort = 0;
     fence_mbar_init();
@@ -145,9 +146,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, L::Q_BYTES);
-      for (int r = 0; r < D / 64; ++r)
-        tma_load_3d(base + L::Q_OFF + r * L::REGION, &tmQ, bar_q, 64 * r, q0, head);
+      mbar_arrive_expect_tx(bar_q, 2 * L::Q_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int r = 0; r < D / 64; ++r)
+          tma_load_3d(base + L::Q_OFF + t * L::Q_BYTES + r * L::REGION, &tmQ, bar_q, 64 * r,
+                      q0 + AT_BQ * t, head);
       int issued = 0;
       for (int j = 0; j < nkb; ++j) {
         const int st = j & 1;
@@ -190,153 +193,144 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) at_timeout(abort, 0x32);
       tc_fence_after();
       for (int j = 0; j <= nkb && ok; ++j) {
-        if (j < nkb) {
-          const int st = j & 1;
-          const uint32_t ph = (j >> 1) & 1u;
-          if (!mbar_wait(bar_k + 8 * st, ph, abort) ||
-              !mbar_wait(bar_s_empty + 8 * st, ph ^ 1u, abort)) {
-            at_timeout(abort, 0x33);
-            break;
-          }
-          tc_fence_after();
-          const uint32_t s_t = tmem_base + st * AT_BK;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const uint32_t s_t = tmem_base + 256 * t;            // S_t, then P_t
+          const uint32_t o_t = s_t + 128;
+          if (j >= 1) {
+            // O_t += P_t,{j-1} V_{j-1}, P read from tensor memory
+            const int jj = j - 1, st = jj & 1;
+            if (!mbar_wait(bar_p_full + 8 * t, jj & 1, abort) ||
+                !mbar_wait(bar_v + 8 * st, (jj >> 1) & 1u, abort)) {
+              at_timeout(abort, 0x34);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
-            mma_f16_cg<1>(s_t, smem_desc(base + L::Q_OFF + off, 16, 1024, 2),
-                          smem_desc(base + L::K_OFF + st * L::K_BYTES + off, 16, 1024, 2), id_qk,
-                          kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < AT_BK / 16; ++kk) {
+              const uint32_t boff = (kk >> 2) * (D / 64) * 8192 + (kk & 3) * 2048;
+              mma_f16_ts(o_t, s_t + 8 * kk,
+                         smem_desc(base + L::V_OFF + st * L::V_BYTES + boff, 8192, 1024, 2),
+                         id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+            }
           }
-          tc_commit_cg<1>(bar_s_full + 8 * st);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, st = jj & 1;
-          const uint32_t ph = (jj >> 1) & 1u;
-          if (!mbar_wait(bar_p_full + 8 * st, ph, abort) ||
-              !mbar_wait(bar_v + 8 * st, ph, abort)) {
-            at_timeout(abort, 0x34);
-            break;
-          }
-          tc_fence_after();
+          if (j < nkb) {
+            // S_t,j = Q_t K_j^T, after the product that read P_t
+            const int st = j & 1;
+            if (!mbar_wait(bar_k + 8 * st, (j >> 1) & 1u, abort)) {
+              at_timeout(abort, 0x33);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < AT_BK / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * L::REGION + (kk & 3) * 32;
-            const uint32_t boff = (kk >> 2) * (D / 64) * 8192 + (kk & 3) * 2048;
-            mma_f16_cg<1>(tmem_base + AT_O_COL,
-                          smem_desc(base + L::P_OFF + st * L::P_BYTES + aoff, 16, 1024, 2),
-                          smem_desc(base + L::V_OFF + st * L::V_BYTES + boff, 8192, 1024, 2),
-                          id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
+              mma_f16_cg<1>(s_t,
+                            smem_desc(base + L::Q_OFF + t * L::Q_BYTES + off, 16, 1024, 2),
+                            smem_desc(base + L::K_OFF + st * L::K_BYTES + off, 16, 1024, 2),
+                            id_qk, kk > 0 ? 1u : 0u);
+            }
+            tc_commit_cg<1>(bar_s_full + 8 * t);
+          } else {
+            tc_commit_cg<1>(bar_o_done + 8 * t);
           }
-          tc_commit_cg<1>(bar_p_done + 8 * st);
-          tc_commit_cg<1>(bar_kv_empty + 8 * st);
         }
+        // both tiles are done with K_{j-1} (read by S_{j-1}) and V_{j-1}
+        if (ok && j >= 1) tc_commit_cg<1>(bar_kv_empty + 8 * ((j - 1) & 1));
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;                          // query tile
     const int quarter = warp & 3;
-    const int row = 32 * quarter + lane;                  // query row in the block
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+    const int row = 32 * quarter + lane;                    // row in the tile
+    const uint32_t lane_addr =
+        tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + 256 * t;
     const bool bf = bf16 != 0;
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1u;
-      if (!mbar_wait(bar_s_full + 8 * st, ph, abort)) {
+      if (!mbar_wait(bar_s_full + 8 * t, j & 1, abort)) {
         at_timeout(abort, 0x35);
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t s[AT_BK];
+      const int valid = Lk - j * AT_BK;                      // keys in this block
+      // the row's 128 scores, four loads in flight, scaled to log2 units
+      uint32_t sv[AT_BK];
 #pragma unroll
       for (int c = 0; c < AT_BK / 32; ++c)
-        tmem_ld_32x32b_x32(lane_addr + st * AT_BK + 32 * c,
-                           *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
+        tmem_ld_32x32b_x32(lane_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s_empty + 8 * st);
-
-      // scores in log2 units; keys beyond Lk do not exist
-      const int valid = Lk - j * AT_BK;
       float mx = -INFINITY;
+      if (valid >= AT_BK) {
 #pragma unroll
-      for (int c = 0; c < AT_BK; ++c) {
-        const float t = c < valid ? __uint_as_float(s[c]) * scale_log2e : -INFINITY;
-        s[c] = __float_as_uint(t);
-        mx = fmaxf(mx, t);
+        for (int e = 0; e < AT_BK; ++e) {
+          const float x = __uint_as_float(sv[e]) * scale_log2e;
+          sv[e] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < AT_BK; ++e) {
+          const float x = e < valid ? __uint_as_float(sv[e]) * scale_log2e : -INFINITY;
+          sv[e] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
       }
       const float m_new = fmaxf(m, mx);
-      const float alpha = ex2_approx(m - m_new);          // 0 on the first block
-      uint32_t pk[AT_BK / 2];
-      float sum = 0.0f;
-#pragma unroll
-      for (int c = 0; c < AT_BK / 2; ++c) {
-        float ra, rb;
-        pk[c] = pack_p(ex2_approx(__uint_as_float(s[2 * c]) - m_new),
-                       ex2_approx(__uint_as_float(s[2 * c + 1]) - m_new), bf, ra, rb);
-        sum += ra + rb;
-      }
-      l = l * alpha + sum;
-
-      // the P buffer is free once the product that read it two blocks ago
-      // is done; O is rescaled (when a row's maximum grew) after the
-      // previous product has accumulated into it
-      if (j >= 2 && !mbar_wait(bar_p_done + 8 * st, ((j - 2) >> 1) & 1u, abort)) {
-        at_timeout(abort, 0x36);
-        ok = false;
-        break;
-      }
+      const float alpha = ex2_approx(m - m_new);             // 0 on the first block
+      // O_t rescale when a row's maximum grew; the product that last wrote
+      // O_t completed before this block's scores did
       if (j >= 1 && __any_sync(0xFFFFFFFFu, m_new > m)) {
-        const int jp = j - 1;
-        if (!mbar_wait(bar_p_done + 8 * (jp & 1), (jp >> 1) & 1u, abort)) {
-          at_timeout(abort, 0x37);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(lane_addr + AT_O_COL + 32 * c, o);
+          tmem_ld_32x32b_x32(lane_addr + 128 + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_32x32b_x32(lane_addr + AT_O_COL + 32 * c, o);
+          tmem_st_32x32b_x32(lane_addr + 128 + 32 * c, o);
         }
-        tmem_wait_st();
       }
-      m = m_new;
-
-      // P row: 128 keys = 16 chunks of 8 values, keys 0..63 in the first
-      // 128-byte-swizzled region, 64..127 in the second
-      uint8_t* prow = gbase + L::P_OFF + st * L::P_BYTES + row * 128;
+      // p = 2^(x - m), rounded to the operand type, written back as packed P
+      // over the scores (already in registers): chunk c of P is columns
+      // 16 c .. 16 c + 15; keys beyond Lk have x = -inf, p = 0
+      float sum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint8_t* dst = prow + (c >> 3) * L::REGION + (((c & 7) ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                                                    pk[4 * c + 3]);
+      for (int c = 0; c < AT_BK / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(__uint_as_float(sv[32 * c + 2 * e]) - m_new);
+          const float p1 = ex2_approx(__uint_as_float(sv[32 * c + 2 * e + 1]) - m_new);
+          float r0, r1;
+          pk[e] = pack_p(p0, p1, bf, r0, r1);
+          sum += r0 + r1;
+        }
+        tmem_st_32x32b_x16(lane_addr + 16 * c, pk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      l = l * alpha + sum;
+      m = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full + 8 * st);
+      if (lane == 0) mbar_arrive(bar_p_full + 8 * t);
     }
     if (ok) {
-      const int jl = nkb - 1;
-      if (!mbar_wait(bar_p_done + 8 * (jl & 1), (jl >> 1) & 1u, abort)) {
+      if (!mbar_wait(bar_o_done + 8 * t, 0, abort)) {
         at_timeout(abort, 0x38);
       } else {
         tc_fence_after();
-        const int qrow = q0 + row;
+        const int qrow = q0 + AT_BQ * t + row;
         const float inv = 1.0f / l;
         const int64_t obase = (static_cast<int64_t>(head) * Lq + qrow) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(lane_addr + AT_O_COL + 32 * c, o);
+          tmem_ld_32x32b_x32(lane_addr + 128 + 32 * c, o);
           tmem_wait_ld();
           if (qrow < Lq) {
             if (o_dtype == DT_F32) {
@@ -390,7 +384,7 @@ cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>((Lq + AT_BQ - 1) / AT_BQ), static_cast<unsigned>(BH));
+  dim3 grid(static_cast<unsigned>((Lq + 2 * AT_BQ - 1) / (2 * AT_BQ)), static_cast<unsigned>(BH));
   kern<<<grid, AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk, scale_log2e, bf);
   return cudaGetLastError();
 }

@@ -136,3 +136,14 @@ def test_attention_deterministic():
     O1 = mx.flash_attention(Q, K, V)
     O2 = mx.flash_attention(Q, K, V)
     assert torch.equal(O1, O2)
+
+
+def test_attention_negative_scale():
+    """A negative scale turns the largest dot product into the smallest
+    score: the maximum must be taken over the scaled scores."""
+    g = torch.Generator().manual_seed(13)
+    Q, K, V = (torch.randn(2, 200, 64, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    O = mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), scale=-0.3)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, scale=-0.3, what="negative scale")
