@@ -227,7 +227,11 @@ def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
     C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
     if workloads.is_dequant(c):
         qb = mx.mx_quantize(B.to(dev), workloads.formats(c)[1], k_strided=True)
-        f = lambda: mx.gemm_dequant(dA, qb, out_dtype=out_dt, out=C)  # noqa
+        # the K-split whenever the tiles leave SMs idle (decode shapes)
+        nb = mx.gemm_dequant_workspace_bytes(c.M, c.N, c.K)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        f = lambda: mx.gemm_dequant(dA, qb, out_dtype=out_dt, out=C,  # noqa
+                                    workspace=ws)
     elif workloads.is_mx(c):
         fa, fb = workloads.formats(c)
         qa = mx.mx_quantize(dA, fa)

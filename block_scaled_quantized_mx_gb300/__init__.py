@@ -36,7 +36,8 @@ STATUS = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE",
 
 EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
            "gemm_f16", "mx_gemm_fused", "mx_gemm_fused_quantize",
-           "gemm_f16_fused", "gemm_dequant", "flash_attention",
+           "gemm_f16_fused", "gemm_dequant", "gemm_dequant_splitk",
+           "gemm_dequant_workspace_bytes", "flash_attention",
            "mx_gemm_workspace_bytes",
            "mx_gemm_splitk",
            "gemm_f16_workspace_bytes", "gemm_f16_splitk",
@@ -108,6 +109,11 @@ def lib() -> ctypes.CDLL:
                                  i64, p]
     L.gemm_dequant.restype = i32
     L.gemm_dequant.argtypes = [p, i32, i64, i64, pt, pe, p, i32, i64, p]
+    L.gemm_dequant_splitk.restype = i32
+    L.gemm_dequant_splitk.argtypes = [p, i32, i64, i64, pt, pe, p, i32, i64, p,
+                                      sz, p]
+    L.gemm_dequant_workspace_bytes.restype = sz
+    L.gemm_dequant_workspace_bytes.argtypes = [i64, i64, i64]
     L.flash_attention.restype = i32
     L.flash_attention.argtypes = [p, p, p, p, i32, i32, i64, i64, i64, i64,
                                   ctypes.c_float, p]
@@ -335,12 +341,18 @@ def gemm_f16_fused(A: torch.Tensor, B: torch.Tensor,
     return out
 
 
+def gemm_dequant_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().gemm_dequant_workspace_bytes(M, N, K))
+
+
 def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
                  act: int = ACT_NONE, out_dtype=torch.float32,
-                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                 out: torch.Tensor | None = None, stream=None,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
     """C = act(A * dequant(B)^T + bias) for a row-major fp16 / bf16 A
     (M x K) and an MX tensor B of any format (N x K, quantized from a K x N
-    matrix): B is dequantized to A's type in shared memory."""
+    matrix): B is dequantized to A's type in shared memory.  With a
+    workspace (gemm_dequant_workspace_bytes) the K-split entry point runs."""
     if A.dtype not in (torch.float16, torch.bfloat16) or A.dim() != 2:
         raise ValueError("A must be a 2-D fp16 or bf16 tensor")
     if A.stride(1) != 1:
@@ -353,13 +365,18 @@ def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
     if out is None:
         out = torch.empty((M, B.outer), dtype=out_dtype, device=A.device)
     cb, ep = B.c(), _epilogue(bias, act)
-    _check(lib().gemm_dequant(
-        A.data_ptr() if A.numel() else None,
-        DT_F16 if A.dtype == torch.float16 else DT_BF16, M, A.stride(0),
-        ctypes.byref(cb), ctypes.byref(ep),
-        out.data_ptr() if out.numel() else None, dt,
-        out.stride(0) if out.dim() == 2 else B.outer, _stream(stream)),
-        "gemm_dequant")
+    args = (A.data_ptr() if A.numel() else None,
+            DT_F16 if A.dtype == torch.float16 else DT_BF16, M, A.stride(0),
+            ctypes.byref(cb), ctypes.byref(ep),
+            out.data_ptr() if out.numel() else None, dt,
+            out.stride(0) if out.dim() == 2 else B.outer)
+    if workspace is None:
+        _check(lib().gemm_dequant(*args, _stream(stream)), "gemm_dequant")
+    else:
+        _check(lib().gemm_dequant_splitk(
+            *args, workspace.data_ptr() if workspace.numel() else None,
+            workspace.numel() * workspace.element_size(), _stream(stream)),
+            "gemm_dequant_splitk")
     return out
 
 

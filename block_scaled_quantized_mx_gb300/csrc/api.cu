@@ -214,9 +214,10 @@ mx_status mx_gemm_fused_quantize(const mx_tensor* A, const mx_tensor* B,
                                        static_cast<cudaStream_t>(stream)));
 }
 
-mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
-                       const mx_tensor* B, const mx_epilogue* epi, void* C, int32_t c_dtype,
-                       int64_t ldc, void* stream) {
+mx_status gemm_dequant_splitk(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
+                              const mx_tensor* B, const mx_epilogue* epi, void* C,
+                              int32_t c_dtype, int64_t ldc, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   mx_status s;
   if (a_dtype != MX_DT_F16 && a_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
   if (c_dtype != MX_DT_F32 && c_dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
@@ -231,11 +232,26 @@ mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
   if (lda < K || lda % 8) return MX_ERR_SHAPE;
   const int64_t eb = (c_dtype == MX_DT_BF16) ? 2 : 4;
   if (ldc < N || (ldc * eb) % 16) return MX_ERR_SHAPE;
-  if (!aligned16(A) || !aligned16(C)) return MX_ERR_ALIGN;
+  if (!aligned16(A) || !aligned16(C) || (workspace && !aligned16(workspace)))
+    return MX_ERR_ALIGN;
   if ((s = check_device()) != MX_OK) return s;
   return from_cuda(mxk::launch_gemm_dequant(a_dtype, A, lda, B->fmt, B->data, B->scales, C,
-                                            c_dtype, ldc, M, N, K, e,
+                                            c_dtype, ldc, M, N, K, e, workspace,
+                                            workspace_bytes,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
+                       const mx_tensor* B, const mx_epilogue* epi, void* C, int32_t c_dtype,
+                       int64_t ldc, void* stream) {
+  return gemm_dequant_splitk(A, a_dtype, M, lda, B, epi, C, c_dtype, ldc, nullptr, 0, stream);
+}
+
+size_t gemm_dequant_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 64 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return 0;
+  if (check_device() != MX_OK) return 0;
+  return mxk::dequant_workspace_bytes(M, N, K);
 }
 
 mx_status flash_attention(const void* Q, const void* K, const void* V, void* O, int32_t dtype,

@@ -83,11 +83,13 @@ cudaError_t launch_gemm_f16(int ab_dtype, const void* A, const void* B, float* C
 
 // C = A * dequant(B)^T for a row-major 16-bit A (a_dtype DT_F16 / DT_BF16,
 // M x K, leading dimension lda) and an MX tensor B of any format (N x K);
-// K a multiple of 64.
+// K a multiple of 64.  With a workspace of at least dequant_workspace_bytes
+// the tiles' K ranges are split over otherwise idle SMs (plain outputs).
 cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt_b,
                                 const void* b_data, const uint8_t* b_sf, void* C, int c_dtype,
                                 int64_t ldc, int64_t M, int64_t N, int64_t K, const Epilogue& epi,
-                                cudaStream_t st);
+                                void* ws, size_t ws_bytes, cudaStream_t st);
+size_t dequant_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 // O = softmax(Q K^T * scale) V for BH heads: Q BH x Lq x d, K and V
 // BH x Lk x d, row-major, dtype DT_F16 / DT_BF16; d 64 or 128; O BH x Lq x d

@@ -216,11 +216,27 @@ __device__ __forceinline__ void dq_block(const uint8_t* codes, uint32_t sc, bool
   }
 }
 
+// Work items: tile t of the raster, K range `part` of `split` (split = 1:
+// whole tiles).  Item w = t * split + part, so the parts of a tile are
+// neighbours; a split item writes its fp32 partial tile to the workspace and
+// dq_reduce_kernel adds the parts.
+struct DqWork {
+  TileSched sched;
+  int num_kb, split, total;
+  __device__ __forceinline__ void item(int w, int& mb, int& nb, int& kb0, int& kb1) const {
+    const int t = w / split, part = w - t * split;
+    sched.tile(t, mb, nb);
+    kb0 = part * num_kb / split;
+    kb1 = (part + 1) * num_kb / split;
+  }
+};
+
 template <int CG, int OUT>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
 dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmSF, void* __restrict__ Cptr, int64_t ldc,
-              int M, int N, int K, int fmt_b, int a_bf16, EpiArgs epi) {
+              int M, int N, int K, int fmt_b, int a_bf16, EpiArgs epi, float* __restrict__ ws,
+              int split) {
   using L = DqSmem<CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -245,10 +261,13 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   const int num_kb = K / DQ_KPS;                       // K % 64 == 0 (host check)
   const int k_atoms = (K + 127) / 128;
   const int row_bytes = (fmt_b == FMT_INT2) ? 16 : (fmt_b == FMT_INT4 || fmt_b == FMT_E2M1) ? 32 : 64;
-  TileSched sched;
-  sched.num_m = (M + BM * CG - 1) / (BM * CG);
-  sched.num_n = (N + BN - 1) / BN;
-  sched.total = sched.num_m * sched.num_n;
+  DqWork work;
+  work.sched.num_m = (M + BM * CG - 1) / (BM * CG);
+  work.sched.num_n = (N + BN - 1) / BN;
+  work.sched.total = work.sched.num_m * work.sched.num_n;
+  work.num_kb = num_kb;
+  work.split = split;
+  work.total = work.sched.total * split;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::STAGES; ++s) {
@@ -285,12 +304,12 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       uint32_t ph = 0;
       bool ok = true;
       const uint32_t code_tx = static_cast<uint32_t>((L::B_ROWS / 128) * 128 * row_bytes + L::SF_BYTES);
-      for (int t = cluster_id; t < sched.total && ok; t += num_clusters) {
-        int mb, nb;
-        sched.tile(t, mb, nb);
+      for (int w = cluster_id; w < work.total && ok; w += num_clusters) {
+        int mb, nb, kb0, kb1;
+        work.item(w, mb, nb, kb0, kb1);
         const int m0 = mb * BM * CG + static_cast<int>(rank) * BM;
         const int n0 = nb * BN + static_cast<int>(rank) * L::B_ROWS;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort)) {
             dq_timeout(abort, 0x21);
             ok = false;
@@ -340,7 +359,9 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       uint32_t ph = 0;
       uint32_t tc = 0;
       bool ok = true;
-      for (int t = cluster_id; t < sched.total && ok; t += num_clusters, ++tc) {
+      for (int w = cluster_id; w < work.total && ok; w += num_clusters, ++tc) {
+        int mb, nb, kb0, kb1;
+        work.item(w, mb, nb, kb0, kb1);
         const uint32_t b = tc & 1u;
         const uint32_t acc = tmem_base + b * BN;
         if (!mbar_wait_spin(bar_acc_empty + 8 * b, ((tc >> 1) & 1u) ^ 1u, abort)) {
@@ -348,7 +369,7 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(bar_a_full + 8 * s, ph, abort) ||
               !mbar_wait(bar_dq_full + 8 * s, ph, abort)) {
             dq_timeout(abort, 0x23);
@@ -360,7 +381,7 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           const uint64_t b_d = b_desc0 + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
 #pragma unroll
           for (int m = 0; m < 4; ++m)      // 4 x 16 K = 64 K; 32 bytes per step
-            mma_f16_cg<CG>(acc, a_d + 2 * m, b_d + 2 * m, id, (kb > 0 || m > 0) ? 1u : 0u);
+            mma_f16_cg<CG>(acc, a_d + 2 * m, b_d + 2 * m, id, (kb > kb0 || m > 0) ? 1u : 0u);
           tc_commit_cg<CG>(bar_empty + 8 * s);
           if (++s == L::STAGES) {
             s = 0;
@@ -376,9 +397,9 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int q = warp & 3;                          // TMEM lane quarter
     const int cg_ = (warp - DQ_EPI_WARP0) >> 2;      // which 128 columns
     uint32_t tc = 0;
-    for (int t = cluster_id; t < sched.total; t += num_clusters, ++tc) {
-      int mb, nb;
-      sched.tile(t, mb, nb);
+    for (int w = cluster_id; w < work.total; w += num_clusters, ++tc) {
+      int mb, nb, kb0, kb1;
+      work.item(w, mb, nb, kb0, kb1);
       const uint32_t b = tc & 1u;
       if (!mbar_wait(bar_acc_full + 8 * b, (tc >> 1) & 1u, abort)) {
         dq_timeout(abort, 0x24);
@@ -396,6 +417,17 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                            r);
         tmem_wait_ld();
         const int c = col0 + 32 * i;
+        if (split > 1) {
+          // a part of a split tile: the raw fp32 accumulator to the workspace
+          // (rows and columns beyond M, N included; the reduction skips them)
+          float* wrow = ws + static_cast<int64_t>(w) * (BM * CG * BN) +
+                        static_cast<int64_t>(rank * BM + 32 * q + lane) * BN + cg_ * 128 + 32 * i;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<uint4*>(wrow + 4 * v) =
+                make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          continue;
+        }
         if (epi.bias != nullptr || epi.act != ACT_NONE) apply_bias_act(r, epi, c, N);
         if (OUT == OUT_MX8 || OUT == OUT_MX4) {
           if (row < M && c < N)
@@ -405,7 +437,8 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           store_plain_chunk<OUT>(r, Cptr, ldc, row, c, N);
         }
       }
-      if (OUT == OUT_MX8 || OUT == OUT_MX4) store_mx_scales(sf_word, epi, row, col0, N);
+      if ((OUT == OUT_MX8 || OUT == OUT_MX4) && split == 1)
+        store_mx_scales(sf_word, epi, row, col0, N);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -425,9 +458,11 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     int s = 0;
     uint32_t ph = 0;
     const bool bf = a_bf16 != 0;
-    for (int tile = cluster_id; tile < sched.total; tile += num_clusters) {
+    for (int w = cluster_id; w < work.total; w += num_clusters) {
+      int mb, nb, kb0, kb1;
+      work.item(w, mb, nb, kb0, kb1);
       bool ok = true;
-      for (int kb = 0; kb < num_kb; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort) ||
             !mbar_wait(bar_codes + 8 * s, ph, abort)) {
           dq_timeout(abort, 0x25);
@@ -484,6 +519,47 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   }
 }
 
+// Sum the `split` fp32 partials of each tile in a fixed order (results do not
+// depend on timing), apply the epilogue's bias and activation, write C (fp32
+// or bf16).  CTA = (tile, group of 4 tile rows); a thread owns 4 columns.
+template <int OUT>
+__global__ void __launch_bounds__(256)
+dq_reduce_kernel(const float* __restrict__ ws, void* __restrict__ Cptr, int64_t ldc, int M,
+                 int N, TileSched sched, int split, int tile_rows, EpiArgs epi) {
+  const int t = blockIdx.x;
+  int mb, nb;
+  sched.tile(t, mb, nb);
+  const int i = blockIdx.y * 4 + (threadIdx.x >> 6);
+  const int c = (threadIdx.x & 63) * 4;
+  const int64_t row = static_cast<int64_t>(mb) * tile_rows + i;
+  const int col = nb * BN + c;
+  if (row >= M || col >= N) return;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int p = 0; p < split; ++p) {
+    const float4 v = *reinterpret_cast<const float4*>(
+        ws + (static_cast<int64_t>(t * split + p) * tile_rows + i) * BN + c);
+    a[0] += v.x;
+    a[1] += v.y;
+    a[2] += v.z;
+    a[3] += v.w;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (epi.bias != nullptr && col + e < N) a[e] += __ldg(epi.bias + col + e);
+    if (epi.act == ACT_GELU) a[e] = gelu_exact(a[e]);
+    else if (epi.act == ACT_GELU_TANH) a[e] = gelu_tanh(a[e]);
+  }
+  if (OUT == OUT_BF16) {
+    uint16_t* crow = reinterpret_cast<uint16_t*>(Cptr) + row * ldc;
+    const uint32_t w[2] = {cvt_bf16x2(a[0], a[1]), cvt_bf16x2(a[2], a[3])};
+    for (int e = 0; e < 4 && col + e < N; ++e)
+      crow[col + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+  } else {
+    float* crow = reinterpret_cast<float*>(Cptr) + row * ldc;
+    for (int e = 0; e < 4 && col + e < N; ++e) crow[col + e] = a[e];
+  }
+}
+
 int dq_sm_count() {
   static int cache[64] = {};
   int dev = 0;
@@ -496,10 +572,34 @@ int dq_sm_count() {
   return n;
 }
 
+// K-split plan: when the tiles leave clusters idle, each tile's K range is
+// cut into `split` parts (at least 4 stages each, at most 16) over the idle
+// clusters.
+struct DqPlan {
+  int split;
+  size_t ws_bytes;
+};
+
+DqPlan dq_plan(int64_t M, int64_t N, int64_t K, bool use_split) {
+  DqPlan p{1, 0};
+  const int cg = (M > BM) ? 2 : 1;
+  const int64_t tiles = ((M + BM * cg - 1) / (BM * cg)) * ((N + BN - 1) / BN);
+  const int64_t clusters = dq_sm_count() / cg;
+  const int64_t nkb = K / DQ_KPS;
+  if (!use_split || tiles >= clusters || nkb < 8) return p;
+  int64_t sp = clusters / tiles;
+  if (sp > nkb / 4) sp = nkb / 4;
+  if (sp > 16) sp = 16;
+  if (sp < 2) return p;
+  p.split = static_cast<int>(sp);
+  p.ws_bytes = static_cast<size_t>(tiles * sp) * (BM * cg) * BN * sizeof(float);
+  return p;
+}
+
 template <int CG, int OUT>
 cudaError_t dq_run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsf, void* C,
                    int64_t ldc, int M, int N, int K, int fmt_b, int a_bf16, const EpiArgs& ea,
-                   cudaStream_t st) {
+                   float* ws, int split, cudaStream_t st) {
   using L = DqSmem<CG>;
   auto kern = dqgemm_kernel<CG, OUT>;
   static bool attr_set[64] = {};
@@ -511,9 +611,13 @@ cudaError_t dq_run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
-  const int tiles = ((M + BM * CG - 1) / (BM * CG)) * ((N + BN - 1) / BN);
+  TileSched sched;
+  sched.num_m = (M + BM * CG - 1) / (BM * CG);
+  sched.num_n = (N + BN - 1) / BN;
+  sched.total = sched.num_m * sched.num_n;
+  const int items = sched.total * split;
   int clusters = dq_sm_count() / CG;
-  if (clusters > tiles) clusters = tiles;
+  if (clusters > items) clusters = items;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
   cfg.blockDim = dim3(DQ_THREADS, 1, 1);
@@ -526,15 +630,22 @@ cudaError_t dq_run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsf, C, ldc, M, N, K, fmt_b, a_bf16, ea);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsf, C, ldc, M, N, K, fmt_b, a_bf16, ea, ws, split);
+  if (e != cudaSuccess || split < 2) return e;
+  if constexpr (OUT == OUT_F32 || OUT == OUT_BF16) {
+    dim3 grid(static_cast<unsigned>(sched.total), BM * CG / 4);
+    dq_reduce_kernel<OUT><<<grid, 256, 0, st>>>(ws, C, ldc, M, N, sched, split, BM * CG, ea);
+    return cudaGetLastError();
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int OUT>
 cudaError_t dq_dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsf,
                         void* C, int64_t ldc, int M, int N, int K, int fmt_b, int a_bf16,
-                        const EpiArgs& ea, cudaStream_t st) {
-  if (M > BM) return dq_run<2, OUT>(ta, tb, tsf, C, ldc, M, N, K, fmt_b, a_bf16, ea, st);
-  return dq_run<1, OUT>(ta, tb, tsf, C, ldc, M, N, K, fmt_b, a_bf16, ea, st);
+                        const EpiArgs& ea, float* ws, int split, cudaStream_t st) {
+  if (M > BM) return dq_run<2, OUT>(ta, tb, tsf, C, ldc, M, N, K, fmt_b, a_bf16, ea, ws, split, st);
+  return dq_run<1, OUT>(ta, tb, tsf, C, ldc, M, N, K, fmt_b, a_bf16, ea, ws, split, st);
 }
 
 }  // namespace
@@ -542,9 +653,13 @@ cudaError_t dq_dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt_b,
                                 const void* b_data, const uint8_t* b_sf, void* C, int c_dtype,
                                 int64_t ldc, int64_t M, int64_t N, int64_t K, const Epilogue& epi,
-                                cudaStream_t st) {
+                                void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0 || K % DQ_KPS) return cudaErrorInvalidValue;
+  DqPlan plan = dq_plan(M, N, K, ws != nullptr && epi.q_fmt == 0);
+  if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = DqPlan{1, 0};
+  float* w = static_cast<float*>(ws);
+  const int sp = plan.split;
   const int bits = (fmt_b == FMT_INT2) ? 2 : (fmt_b == FMT_INT4 || fmt_b == FMT_E2M1) ? 4 : 8;
   const uint64_t row_bytes = static_cast<uint64_t>(K) * bits / 8;
   const bool pair = M > BM;
@@ -574,11 +689,20 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
                   : c_dtype == DT_BF16  ? OUT_BF16
                                         : OUT_F32;
   switch (out) {
-    case OUT_BF16: return dq_dispatch<OUT_BF16>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, st);
-    case OUT_MX8: return dq_dispatch<OUT_MX8>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, st);
-    case OUT_MX4: return dq_dispatch<OUT_MX4>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, st);
-    default: return dq_dispatch<OUT_F32>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, st);
+    case OUT_BF16:
+      return dq_dispatch<OUT_BF16>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, w, sp, st);
+    case OUT_MX8:
+      return dq_dispatch<OUT_MX8>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, w, 1, st);
+    case OUT_MX4:
+      return dq_dispatch<OUT_MX4>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, w, 1, st);
+    default:
+      return dq_dispatch<OUT_F32>(ta, tb, tsf, C, ldc, m, n, k, fmt_b, bf, ea, w, sp, st);
   }
+}
+
+size_t dequant_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % DQ_KPS) return 0;
+  return dq_plan(M, N, K, true).ws_bytes;
 }
 
 unsigned fetch_and_clear_status_dq(cudaError_t* err) {

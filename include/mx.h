@@ -269,6 +269,20 @@ mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
                        const mx_tensor* B, const mx_epilogue* epi, void* C,
                        int32_t c_dtype, int64_t ldc, void* stream);
 
+/* gemm_dequant with a K-split: when the output tiles leave SMs idle (a few
+ * rows of A, as in decoding one token at a time), each tile's K range is
+ * split into parts that run on those SMs, each writing an fp32 partial tile
+ * to the workspace; a second kernel adds the parts in a fixed order, applies
+ * the epilogue and writes C.  workspace: device, 16-byte aligned, at least
+ * gemm_dequant_workspace_bytes(M, N, K) bytes (0: the problem is not split;
+ * NULL or smaller: the call runs unsplit). */
+size_t gemm_dequant_workspace_bytes(int64_t M, int64_t N, int64_t K);
+mx_status gemm_dequant_splitk(const void* A, int32_t a_dtype, int64_t M,
+                              int64_t lda, const mx_tensor* B,
+                              const mx_epilogue* epi, void* C, int32_t c_dtype,
+                              int64_t ldc, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /*
  * flash_attention -- O = softmax(Q K^T * scale) V for BH independent heads,
  * in one kernel: the scores and probabilities stay on the SM (WWDC26

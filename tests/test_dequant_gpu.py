@@ -147,3 +147,51 @@ def test_dequant_deterministic():
     C1 = mx.gemm_dequant(A, b)
     C2 = mx.gemm_dequant(A, b)
     assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("fmt", [oracle.INT4, oracle.INT2, oracle.E4M3])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 4096), (16, 1024, 8192),
+                                   (64, 2048, 2048), (128, 512, 4096),
+                                   (200, 768, 4096)])
+def test_dequant_splitk(fmt, out, M, N, K):
+    """Decode-like shapes: few output tiles, K split over the idle SMs; the
+    parts are summed in a fixed order by the reduction kernel."""
+    g = torch.Generator().manual_seed(M + N + K + fmt)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    cb, sb = workloads.random_codes((N, K), fmt, seed=N + fmt, scale_lo=116,
+                                    scale_hi=127)
+    b = planes_from_codes(cb, sb, fmt)
+    nbytes = mx.gemm_dequant_workspace_bytes(M, N, K)
+    assert nbytes > 0, "expected a split for this shape"
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    C = nan_like((M, N), _odt(out))
+    mx.gemm_dequant(A.cuda(), b, out_dtype=_odt(out), out=C, workspace=ws)
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_a16_bmx(f16_bits(A), oracle.BF16, cb, sb, fmt)
+    check_close(C.float().cpu().numpy(), Cr, S, out, f"split {M}x{N}x{K}")
+    C2 = mx.gemm_dequant(A.cuda(), b, out_dtype=_odt(out), workspace=ws)
+    assert torch.equal(C.view(torch.uint8), C2.view(torch.uint8))
+
+
+def test_dequant_splitk_fused_epilogue():
+    M, N, K = 32, 1024, 4096
+    g = torch.Generator().manual_seed(44)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = torch.randn(K, N, generator=g) * 0.02
+    bias = torch.randn(N, generator=g) * 0.5
+    b = mx.mx_quantize(W.cuda(), mx.INT4, k_strided=True)
+    ws = torch.empty(mx.gemm_dequant_workspace_bytes(M, N, K),
+                     dtype=torch.uint8, device="cuda")
+    C = mx.gemm_dequant(A.cuda(), b, bias.cuda(), mx.ACT_GELU, workspace=ws)
+    assert mx.mx_last_error() == 0
+    cb, sb = oracle.quantize(W.numpy(), oracle.INT4, k_axis=0)
+    Cr, S = oracle.gemm_a16_bmx(f16_bits(A), oracle.BF16, cb, sb, oracle.INT4)
+    check_epilogue_close(C.cpu().numpy(), Cr, S, bias.numpy(), oracle.ACT_GELU,
+                         "f32", "split + GELU")
+
+
+def test_dequant_workspace_only_for_idle_sms():
+    assert mx.gemm_dequant_workspace_bytes(8192, 8192, 8192) == 0
+    assert mx.gemm_dequant_workspace_bytes(64, 8192, 8192) > 0
+    assert mx.gemm_dequant_workspace_bytes(64, 8192, 100) == 0      # K % 64
