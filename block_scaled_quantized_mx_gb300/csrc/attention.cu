@@ -23,8 +23,9 @@
 //     running sum adds exactly the rounded values), written back over the
 //     scores as the packed A operand of
 //     the P V product, which reads it from tensor memory -- the
-//     probabilities never touch shared memory.  When a row's maximum grows,
-//     its O row is rescaled in TMEM first.  At the end O / sum.
+//     probabilities never touch shared memory.  The exponentials' reference
+//     point moves only when a row's maximum outgrows it by more than 2^8;
+//     then the row's O is rescaled in TMEM first.  At the end O / sum.
 // Ordering: the MMA thread issues P_{j-1} V before S_j, and a commit covers
 // every earlier operation of its thread, so once S_t,j is complete so is
 // the previous product that read P_t and accumulated into O_t: the softmax
@@ -50,6 +51,7 @@ constexpr int AT_BQ = 128;          // queries per tile (two tiles per CTA)
 constexpr int AT_BK = 128;          // keys per block
 constexpr int AT_THREADS = 320;     // warps 0, 1 and two softmax warpgroups
 constexpr int AT_TMEM_COLS = 512;
+constexpr float AT_LAZY = 8.0f;     // slack of the exponentials' reference point
 
 template <int D>
 struct AtSmem {
@@ -61,8 +63,8 @@ struct AtSmem {
   static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr int V_OFF = K_OFF + 2 * K_BYTES;
   static constexpr int BAR_OFF = V_OFF + 2 * V_BYTES;
-  // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2]
-  static constexpr int MISC_OFF = BAR_OFF + 13 * 8;
+  // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full[2], o_done[2]
+  static constexpr int MISC_OFF = BAR_OFF + 15 * 8;
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -94,11 +96,11 @@ __device__ __forceinline__ uint32_t pack_p(float a, float b, bool bf16, float& r
   return w;
 }
 
-template <int D>
+template <int D, bool BF>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, void* __restrict__ Optr, int o_dtype,
-                 int Lq, int Lk, float scale_log2e, int bf16) {
+                 int Lq, int Lk, float scale_log2e) {
   using L = AtSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -108,8 +110,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t bar_q = base + L::BAR_OFF;
   const uint32_t bar_k = bar_q + 8;            // [2] ring stage
   const uint32_t bar_v = bar_k + 16;           // [2] ring stage
-  const uint32_t bar_kv_empty = bar_v + 16;    // [2] ring stage
-  const uint32_t bar_s_full = bar_kv_empty + 16;   // [2] tile
+  const uint32_t bar_k_empty = bar_v + 16;     // [2] ring stage
+  const uint32_t bar_v_empty = bar_k_empty + 16;   // [2] ring stage
+  const uint32_t bar_s_full = bar_v_empty + 16;    // [2] tile
   const uint32_t bar_p_full = bar_s_full + 16;     // [2] tile
   const uint32_t bar_o_done = bar_p_full + 16;     // [2] tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC_OFF);
@@ -126,7 +129,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_k + 8 * i, 1);
       mbar_init(bar_v + 8 * i, 1);
-      mbar_init(bar_kv_empty + 8 * i, 1);
+      mbar_init(bar_k_empty + 8 * i, 1);
+      mbar_init(bar_v_empty + 8 * i, 1);
       mbar_init(bar_s_full + 8 * i, 1);
       mbar_init(bar_p_full + 8 * i, 4);
       mbar_init(bar_o_done + 8 * i, 1);
@@ -151,32 +155,43 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int r = 0; r < D / 64; ++r)
           tma_load_3d(base + L::Q_OFF + t * L::Q_BYTES + r * L::REGION, &tmQ, bar_q, 64 * r,
                       q0 + AT_BQ * t, head);
-      int issued = 0;
+      // K_j and V_j have separate slots: K_j's is free once both tiles'
+      // S_j are done, V_j's only after both P_j V_j products
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkb; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1u;
-        if (!mbar_wait(bar_kv_empty + 8 * st, ph ^ 1u, abort)) {
+        const int k0 = j * AT_BK;
+        bool okp = mbar_wait(bar_k_empty + 8 * st, ph ^ 1u, abort);
+        if (okp) {
+          ++k_issued;
+          mbar_arrive_expect_tx(bar_k + 8 * st, L::K_BYTES);
+          for (int r = 0; r < D / 64; ++r)
+            tma_load_3d(base + L::K_OFF + st * L::K_BYTES + r * L::REGION, &tmK, bar_k + 8 * st,
+                        64 * r, k0, head);
+          okp = mbar_wait(bar_v_empty + 8 * st, ph ^ 1u, abort);
+        }
+        if (!okp) {
           at_timeout(abort, 0x31);
           // let the copies already issued land before the CTA retires
           const long long t0 = clock64();
           while (!mbar_try_wait(bar_q, 0) && clock64() - t0 < MXK_WAIT_LIMIT_CYCLES) {
           }
-          for (int i = issued >= 2 ? issued - 2 : 0; i < issued; ++i) {
-            const uint32_t pi = (i >> 1) & 1u;
+          for (int i = k_issued >= 2 ? k_issued - 2 : 0; i < k_issued; ++i) {
             const long long t1 = clock64();
-            while ((!mbar_try_wait(bar_k + 8 * (i & 1), pi) ||
-                    !mbar_try_wait(bar_v + 8 * (i & 1), pi)) &&
+            while (!mbar_try_wait(bar_k + 8 * (i & 1), (i >> 1) & 1u) &&
+                   clock64() - t1 < MXK_WAIT_LIMIT_CYCLES) {
+            }
+          }
+          for (int i = v_issued >= 2 ? v_issued - 2 : 0; i < v_issued; ++i) {
+            const long long t1 = clock64();
+            while (!mbar_try_wait(bar_v + 8 * (i & 1), (i >> 1) & 1u) &&
                    clock64() - t1 < MXK_WAIT_LIMIT_CYCLES) {
             }
           }
           break;
         }
-        ++issued;
-        const int k0 = j * AT_BK;
-        mbar_arrive_expect_tx(bar_k + 8 * st, L::K_BYTES);
-        for (int r = 0; r < D / 64; ++r)
-          tma_load_3d(base + L::K_OFF + st * L::K_BYTES + r * L::REGION, &tmK, bar_k + 8 * st,
-                      64 * r, k0, head);
+        ++v_issued;
         mbar_arrive_expect_tx(bar_v + 8 * st, L::V_BYTES);
         for (int h = 0; h < 2; ++h)
           for (int a = 0; a < D / 64; ++a)
@@ -187,8 +202,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_qk = at_idesc(bf16 != 0, AT_BK, 0);
-      const uint32_t id_pv = at_idesc(bf16 != 0, D, 1);
+      const uint32_t id_qk = at_idesc(BF, AT_BK, 0);
+      const uint32_t id_pv = at_idesc(BF, D, 1);
       bool ok = mbar_wait(bar_q, 0, abort);
       if (!ok) at_timeout(abort, 0x32);
       tc_fence_after();
@@ -213,6 +228,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                          smem_desc(base + L::V_OFF + st * L::V_BYTES + boff, 8192, 1024, 2),
                          id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
             }
+            // both tiles' products with V_{j-1} issued: its slot frees when they end
+            if (t == 1) tc_commit_cg<1>(bar_v_empty + 8 * st);
           }
           if (j < nkb) {
             // S_t,j = Q_t K_j^T, after the product that read P_t
@@ -232,12 +249,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                             id_qk, kk > 0 ? 1u : 0u);
             }
             tc_commit_cg<1>(bar_s_full + 8 * t);
+            // both tiles' S_j issued: K_j's slot frees when they end
+            if (t == 1) tc_commit_cg<1>(bar_k_empty + 8 * st);
           } else {
             tc_commit_cg<1>(bar_o_done + 8 * t);
           }
         }
-        // both tiles are done with K_{j-1} (read by S_{j-1}) and V_{j-1}
-        if (ok && j >= 1) tc_commit_cg<1>(bar_kv_empty + 8 * ((j - 1) & 1));
       }
     }
   } else {
@@ -247,7 +264,6 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int row = 32 * quarter + lane;                    // row in the tile
     const uint32_t lane_addr =
         tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + 256 * t;
-    const bool bf = bf16 != 0;
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
@@ -264,27 +280,37 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int c = 0; c < AT_BK / 32; ++c)
         tmem_ld_32x32b_x32(lane_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
       tmem_wait_ld();
-      float mx = -INFINITY;
+      // row maximum over eight independent partial maxima (short chains)
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
       if (valid >= AT_BK) {
 #pragma unroll
         for (int e = 0; e < AT_BK; ++e) {
           const float x = __uint_as_float(sv[e]) * scale_log2e;
           sv[e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          mx8[e & 7] = fmaxf(mx8[e & 7], x);
         }
       } else {
 #pragma unroll
         for (int e = 0; e < AT_BK; ++e) {
           const float x = e < valid ? __uint_as_float(sv[e]) * scale_log2e : -INFINITY;
           sv[e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          mx8[e & 7] = fmaxf(mx8[e & 7], x);
         }
       }
-      const float m_new = fmaxf(m, mx);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // The reference point m of the exponentials moves only when the block's
+      // maximum exceeds it by more than AT_LAZY (log2 units): every p stays
+      // <= 2^AT_LAZY, exact in fp32 and in the 16-bit operand types, and O / l
+      // does not depend on which m was used, so the O rescale (a round trip
+      // of the row's O through registers) is skipped for almost every block.
+      const float m_new = (mx > m + AT_LAZY) ? mx : m;
       const float alpha = ex2_approx(m - m_new);             // 0 on the first block
-      // O_t rescale when a row's maximum grew; the product that last wrote
-      // O_t completed before this block's scores did
-      if (j >= 1 && __any_sync(0xFFFFFFFFu, m_new > m)) {
+      // O_t rescale when a row's reference moved; the product that last
+      // wrote O_t completed before this block's scores did
+      if (j >= 1 && __any_sync(0xFFFFFFFFu, m_new != m)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -298,22 +324,24 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // p = 2^(x - m), rounded to the operand type, written back as packed P
       // over the scores (already in registers): chunk c of P is columns
       // 16 c .. 16 c + 15; keys beyond Lk have x = -inf, p = 0
-      float sum = 0.0f;
+      float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int c = 0; c < AT_BK / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(sv[32 * c + 2 * e]) - m_new);
-          const float p1 = ex2_approx(__uint_as_float(sv[32 * c + 2 * e + 1]) - m_new);
+          const float x0 = __uint_as_float(sv[32 * c + 2 * e]) - m_new;
+          const float x1 = __uint_as_float(sv[32 * c + 2 * e + 1]) - m_new;
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
           float r0, r1;
-          pk[e] = pack_p(p0, p1, bf, r0, r1);
-          sum += r0 + r1;
+          pk[e] = pack_p(p0, p1, BF, r0, r1);
+          sum4[e & 3] += r0 + r1;
         }
         tmem_st_32x32b_x16(lane_addr + 16 * c, pk);
       }
       tmem_wait_st();
-      l = l * alpha + sum;
+      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m = m_new;
       tc_fence_before();
       __syncwarp();
@@ -369,12 +397,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
 }
 
-template <int D>
+template <int D, bool BF>
 cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* O,
-                   int o_dtype, int64_t BH, int Lq, int Lk, float scale_log2e, int bf,
-                   cudaStream_t st) {
+                   int o_dtype, int64_t BH, int Lq, int Lk, float scale_log2e, cudaStream_t st) {
   using L = AtSmem<D>;
-  auto kern = attention_kernel<D>;
+  auto kern = attention_kernel<D, BF>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -385,7 +412,7 @@ cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     if (dev < 64) attr_set[dev] = true;
   }
   dim3 grid(static_cast<unsigned>((Lq + 2 * AT_BQ - 1) / (2 * AT_BQ)), static_cast<unsigned>(BH));
-  kern<<<grid, AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk, scale_log2e, bf);
+  kern<<<grid, AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk, scale_log2e);
   return cudaGetLastError();
 }
 
@@ -409,10 +436,13 @@ cudaError_t launch_attention(int dtype, const void* Q, const void* K, const void
   if (!enc(&tq, Q, Lq, 128) || !enc(&tk, K, Lk, 128) || !enc(&tv, V, Lk, 64))
     return cudaErrorInvalidValue;
   const float sl2 = scale * 1.4426950408889634f;
-  const int bf = (dtype == DT_BF16) ? 1 : 0;
+  const bool bf = dtype == DT_BF16;
   const int lq = static_cast<int>(Lq), lk = static_cast<int>(Lk);
-  if (d == 64) return at_run<64>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, bf, st);
-  return at_run<128>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, bf, st);
+  if (d == 64)
+    return bf ? at_run<64, true>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st)
+              : at_run<64, false>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st);
+  return bf ? at_run<128, true>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st)
+            : at_run<128, false>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st);
 }
 
 unsigned fetch_and_clear_status_attn(cudaError_t* err) {
