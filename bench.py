@@ -309,14 +309,21 @@ def time_attention(mx, c, dev, flusher):
     tensors as library context."""
     Q, K, V = (t.to(dev) for t in workloads.attn_sources(c))
     O = torch.empty(Q.shape, dtype=torch.bfloat16, device=dev)
+    ms_whole = event_time(lambda: mx.flash_attention(Q, K, V, out_dtype=torch.bfloat16,
+                                                     out=O), flusher=flusher)
+    # the key-split entry point, when the (head, 256-query) units leave a
+    # partial last wave of SMs
+    nbytes = mx.flash_attention_workspace_bytes(c.BH, c.Lq, c.Lk, c.d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
     ms = event_time(lambda: mx.flash_attention(Q, K, V, out_dtype=torch.bfloat16,
-                                               out=O), flusher=flusher)
+                                               out=O, workspace=ws), flusher=flusher)
     assert mx.mx_last_error() == 0
     flops = 4.0 * c.BH * c.Lq * c.Lk * c.d
     sdpa = torch.nn.functional.scaled_dot_product_attention
     lib_ms = event_time(lambda: sdpa(Q.unsqueeze(0), K.unsqueeze(0), V.unsqueeze(0)),
                         flusher=flusher)
     return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "split_kv": nbytes > 0, "unsplit_ms": ms_whole,
             "library_reference_ms": lib_ms,
             "library_reference": "torch scaled_dot_product_attention (context only)"}
 
@@ -678,7 +685,7 @@ def parse_args(argv=None):
                     help="MX workloads on which the fused bias + GELU epilogue "
                          "is timed against the decomposed path")
     ap.add_argument("--no-fused", action="store_true")
-    ap.add_argument("--attention", default="attn_sam_d64,attn_sam_d128",
+    ap.add_argument("--attention", default="attn_sam_d64,attn_sam_d128,attn_long_d128",
                     help="attention workloads timed with flash_attention")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--splitk", action="store_true",

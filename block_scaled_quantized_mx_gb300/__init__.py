@@ -38,6 +38,7 @@ EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
            "gemm_f16", "mx_gemm_fused", "mx_gemm_fused_quantize",
            "gemm_f16_fused", "gemm_dequant", "gemm_dequant_splitk",
            "gemm_dequant_workspace_bytes", "flash_attention",
+           "flash_attention_workspace_bytes", "flash_attention_splitkv",
            "mx_gemm_workspace_bytes",
            "mx_gemm_splitk",
            "gemm_f16_workspace_bytes", "gemm_f16_splitk",
@@ -117,6 +118,11 @@ def lib() -> ctypes.CDLL:
     L.flash_attention.restype = i32
     L.flash_attention.argtypes = [p, p, p, p, i32, i32, i64, i64, i64, i64,
                                   ctypes.c_float, p]
+    L.flash_attention_workspace_bytes.restype = sz
+    L.flash_attention_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    L.flash_attention_splitkv.restype = i32
+    L.flash_attention_splitkv.argtypes = [p, p, p, p, i32, i32, i64, i64, i64,
+                                          i64, ctypes.c_float, p, sz, p]
     L.mx_gemm_workspace_bytes.restype = sz
     L.mx_gemm_workspace_bytes.argtypes = [i32, i64, i64, i64]
     L.mx_gemm_splitk.restype = i32
@@ -382,10 +388,13 @@ def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
 
 def flash_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
                     scale: float | None = None, out_dtype=torch.float32,
-                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                    out: torch.Tensor | None = None, stream=None,
+                    workspace: torch.Tensor | None = None) -> torch.Tensor:
     """O = softmax(Q K^T * scale) V per head.  Q is (..., Lq, d), K and V
     (..., Lk, d), contiguous fp16 or bf16 CUDA tensors with the same leading
-    dimensions (flattened into heads); scale defaults to 1/sqrt(d)."""
+    dimensions (flattened into heads); scale defaults to 1/sqrt(d).  With a
+    device `workspace` (uint8, flash_attention_workspace_bytes() long) the
+    key axis is split over SMs that would otherwise idle."""
     if Q.dtype not in (torch.float16, torch.bfloat16) or K.dtype != Q.dtype \
             or V.dtype != Q.dtype:
         raise ValueError("Q, K, V must share an fp16 or bf16 dtype")
@@ -404,11 +413,22 @@ def flash_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
     if out is None:
         out = torch.empty(Q.shape, dtype=out_dtype, device=Q.device)
     ptr = lambda t: t.data_ptr() if t.numel() else None  # noqa
-    _check(lib().flash_attention(
-        ptr(Q), ptr(K), ptr(V), ptr(out),
-        DT_F16 if Q.dtype == torch.float16 else DT_BF16, odt, BH, Lq, Lk, d,
-        float(scale), _stream(stream)), "flash_attention")
+    dt = DT_F16 if Q.dtype == torch.float16 else DT_BF16
+    if workspace is None:
+        _check(lib().flash_attention(
+            ptr(Q), ptr(K), ptr(V), ptr(out), dt, odt, BH, Lq, Lk, d,
+            float(scale), _stream(stream)), "flash_attention")
+    else:
+        _check(lib().flash_attention_splitkv(
+            ptr(Q), ptr(K), ptr(V), ptr(out), dt, odt, BH, Lq, Lk, d,
+            float(scale), ptr(workspace), workspace.numel(), _stream(stream)),
+            "flash_attention_splitkv")
     return out
+
+
+def flash_attention_workspace_bytes(BH: int, Lq: int, Lk: int, d: int) -> int:
+    """Bytes of workspace flash_attention splits into (0: no split)."""
+    return int(lib().flash_attention_workspace_bytes(BH, Lq, Lk, d))
 
 
 def mx_last_error(stream=None) -> int:

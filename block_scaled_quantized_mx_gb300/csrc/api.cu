@@ -254,9 +254,11 @@ size_t gemm_dequant_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return mxk::dequant_workspace_bytes(M, N, K);
 }
 
-mx_status flash_attention(const void* Q, const void* K, const void* V, void* O, int32_t dtype,
-                          int32_t o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
-                          float scale, void* stream) {
+namespace {
+
+mx_status attention(const void* Q, const void* K, const void* V, void* O, int32_t dtype,
+                    int32_t o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream) {
   if (dtype != MX_DT_F16 && dtype != MX_DT_BF16) return MX_ERR_INVALID_ARG;
   if (o_dtype != MX_DT_F32 && o_dtype != MX_DT_BF16 && o_dtype != MX_DT_F16)
     return MX_ERR_INVALID_ARG;
@@ -270,8 +272,33 @@ mx_status flash_attention(const void* Q, const void* K, const void* V, void* O, 
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return MX_ERR_ALIGN;
   mx_status s = check_device();
   if (s != MX_OK) return s;
+  if (workspace && !aligned16(workspace)) return MX_ERR_ALIGN;
   return from_cuda(mxk::launch_attention(dtype, Q, K, V, O, o_dtype, BH, Lq, Lk, d, scale,
+                                         workspace, workspace_bytes,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+mx_status flash_attention(const void* Q, const void* K, const void* V, void* O, int32_t dtype,
+                          int32_t o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
+                          float scale, void* stream) {
+  return attention(Q, K, V, O, dtype, o_dtype, BH, Lq, Lk, d, scale, nullptr, 0, stream);
+}
+
+size_t flash_attention_workspace_bytes(int64_t BH, int64_t Lq, int64_t Lk, int64_t d) {
+  if (BH <= 0 || Lq <= 0 || Lk <= 0 || BH > 65535 || Lq > kMaxDim || Lk > kMaxDim) return 0;
+  if (d != 64 && d != 128) return 0;
+  if (check_device() != MX_OK) return 0;
+  return mxk::attention_workspace_bytes(BH, Lq, Lk, d);
+}
+
+mx_status flash_attention_splitkv(const void* Q, const void* K, const void* V, void* O,
+                                  int32_t dtype, int32_t o_dtype, int64_t BH, int64_t Lq,
+                                  int64_t Lk, int64_t d, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return attention(Q, K, V, O, dtype, o_dtype, BH, Lq, Lk, d, scale, workspace, workspace_bytes,
+                   stream);
 }
 
 mx_status gemm_f16(const void* A, const void* B, float* C, int32_t ab_dtype, int64_t M,

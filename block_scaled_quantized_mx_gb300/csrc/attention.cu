@@ -37,6 +37,8 @@
 // timeout in g_status_attn and the CTA shuts down in order.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
@@ -96,11 +98,23 @@ __device__ __forceinline__ uint32_t pack_p(float a, float b, bool bf16, float& r
   return w;
 }
 
+// The work of one launch: units are (head, 256 queries), head-major.  Units
+// [0, whole) run whole; each later unit is cut into `split` parts along the
+// key blocks, and a part writes its un-normalised O together with each row's
+// reference point m and sum l to the workspace (part r of the split units at
+// ws + r * 256 * (D + 2) floats: O 256 x D row-major, then m[256], l[256]).
+struct AtWork {
+  int units_per_head;   // ceil(Lq / 256)
+  int whole;
+  int split;
+  float* ws;
+};
+
 template <int D, bool BF>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, void* __restrict__ Optr, int o_dtype,
-                 int Lq, int Lk, float scale_log2e) {
+                 int Lq, int Lk, float scale_log2e, AtWork work) {
   using L = AtSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -120,9 +134,19 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int head = blockIdx.y;
-  const int q0 = blockIdx.x * 2 * AT_BQ;
-  const int nkb = (Lk + AT_BK - 1) / AT_BK;
+  const int nkb_all = (Lk + AT_BK - 1) / AT_BK;
+  const int item = blockIdx.x;
+  int unit = item, kb0 = 0, nkb = nkb_all, part_slot = -1;
+  if (item >= work.whole) {
+    const int r = item - work.whole;
+    const int part = r % work.split;
+    unit = work.whole + r / work.split;
+    kb0 = static_cast<int>(static_cast<int64_t>(part) * nkb_all / work.split);
+    nkb = static_cast<int>(static_cast<int64_t>(part + 1) * nkb_all / work.split) - kb0;
+    part_slot = r;
+  }
+  const int head = unit / work.units_per_head;
+  const int q0 = (unit % work.units_per_head) * 2 * AT_BQ;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -161,7 +185,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int j = 0; j < nkb; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1u;
-        const int k0 = j * AT_BK;
+        const int k0 = (kb0 + j) * AT_BK;
         bool okp = mbar_wait(bar_k_empty + 8 * st, ph ^ 1u, abort);
         if (okp) {
           ++k_issued;
@@ -273,7 +297,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         break;
       }
       tc_fence_after();
-      const int valid = Lk - j * AT_BK;                      // keys in this block
+      const int valid = Lk - (kb0 + j) * AT_BK;              // keys in this block
       // the row's 128 scores, four loads in flight, scaled to log2 units
       uint32_t sv[AT_BK];
 #pragma unroll
@@ -355,6 +379,25 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int qrow = q0 + AT_BQ * t + row;
         const float inv = 1.0f / l;
         const int64_t obase = (static_cast<int64_t>(head) * Lq + qrow) * D;
+        if (part_slot >= 0) {
+          // a part: un-normalised O, m and l of every row of the unit
+          float* ws = work.ws + static_cast<int64_t>(part_slot) * (2 * AT_BQ) * (D + 2);
+          const int urow = AT_BQ * t + row;
+          float* dst0 = ws + static_cast<int64_t>(urow) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(lane_addr + 128 + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<float4*>(dst0 + 32 * c + 4 * v) =
+                  make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                              __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+          }
+          ws[(2 * AT_BQ) * D + urow] = m;
+          ws[(2 * AT_BQ) * (D + 1) + urow] = l;
+        } else {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -385,6 +428,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
           }
         }
+        }
       }
     }
   }
@@ -397,9 +441,56 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
 }
 
+// Merge the parts of the split units: per row, M = max over parts of m_p,
+// O = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p, parts in a fixed order.
+// One thread per (split unit, row, four columns).
+template <int D>
+__global__ void __launch_bounds__(256)
+attention_merge_kernel(const float* __restrict__ ws, void* __restrict__ Optr, int o_dtype, int Lq,
+                       AtWork work, int64_t n_threads) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_threads) return;
+  constexpr int G = D / 4;
+  const int g = static_cast<int>(gid % G);
+  const int urow = static_cast<int>((gid / G) % (2 * AT_BQ));
+  const int su = static_cast<int>(gid / (G * 2 * AT_BQ));
+  const int unit = work.whole + su;
+  const int head = unit / work.units_per_head;
+  const int qrow = (unit % work.units_per_head) * 2 * AT_BQ + urow;
+  if (qrow >= Lq) return;
+  constexpr int64_t PART = (2 * AT_BQ) * (D + 2);
+  const float* base = ws + static_cast<int64_t>(su) * work.split * PART;
+  float M = -INFINITY;
+  for (int p = 0; p < work.split; ++p) M = fmaxf(M, base[p * PART + (2 * AT_BQ) * D + urow]);
+  float l = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int p = 0; p < work.split; ++p) {
+    const float* part = base + p * PART;
+    const float w = ex2_approx(part[(2 * AT_BQ) * D + urow] - M);
+    l = fmaf(w, part[(2 * AT_BQ) * (D + 1) + urow], l);
+    const float4 o = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(urow) * D + 4 * g);
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+  }
+  const float inv = 1.0f / l;
+  const int64_t obase = (static_cast<int64_t>(head) * Lq + qrow) * D + 4 * g;
+  if (o_dtype == DT_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(Optr) + obase) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  } else {
+    const bool bf = o_dtype == DT_BF16;
+    const uint32_t w0 = bf ? cvt_bf16x2(acc.x * inv, acc.y * inv) : cvt_f16x2(acc.x * inv, acc.y * inv);
+    const uint32_t w1 = bf ? cvt_bf16x2(acc.z * inv, acc.w * inv) : cvt_f16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(Optr) + obase) = make_uint2(w0, w1);
+  }
+}
+
 template <int D, bool BF>
 cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* O,
-                   int o_dtype, int64_t BH, int Lq, int Lk, float scale_log2e, cudaStream_t st) {
+                   int o_dtype, const AtWork& work, int64_t items, int Lq, int Lk,
+                   float scale_log2e, cudaStream_t st) {
   using L = AtSmem<D>;
   auto kern = attention_kernel<D, BF>;
   static bool attr_set[64] = {};
@@ -411,17 +502,71 @@ cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>((Lq + 2 * AT_BQ - 1) / (2 * AT_BQ)), static_cast<unsigned>(BH));
-  kern<<<grid, AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk, scale_log2e);
+  kern<<<static_cast<unsigned>(items), AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk,
+                                                                   scale_log2e, work);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || work.split <= 1) return e;
+  const int64_t split_units = (items - work.whole) / work.split;
+  const int64_t n = split_units * (2 * AT_BQ) * (D / 4);
+  attention_merge_kernel<D><<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+      work.ws, O, o_dtype, Lq, work, n);
   return cudaGetLastError();
+}
+
+int at_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+struct AtPlan {
+  int64_t units, whole, split, items;
+  size_t ws_bytes;
+};
+
+// Whole units fill whole waves of one CTA per SM; the units of a last partial
+// wave (all units, when there are fewer than SMs) are split along the key
+// blocks over the idle SMs: parts of at least two blocks, at most 16 parts.
+AtPlan at_plan(int64_t BH, int64_t Lq, int64_t Lk, int64_t d, bool use_split) {
+  AtPlan p{};
+  const int64_t uph = (Lq + 2 * AT_BQ - 1) / (2 * AT_BQ);
+  p.units = BH * uph;
+  p.whole = p.units;
+  p.split = 1;
+  p.items = p.units;
+  const int64_t sms = at_sm_count();
+  const int64_t nkb = (Lk + AT_BK - 1) / AT_BK;
+  if (!use_split || sms <= 0 || p.units == 0) return p;
+  const int64_t tail = p.units % sms;
+  if (tail == 0) return p;
+  const int64_t split = std::min<int64_t>(std::min<int64_t>(sms / tail, nkb / 2), 16);
+  if (split < 2) return p;
+  p.whole = p.units - tail;
+  p.split = split;
+  p.items = p.whole + tail * split;
+  p.ws_bytes = static_cast<size_t>(tail * split) * (2 * AT_BQ) * (d + 2) * sizeof(float);
+  return p;
 }
 
 }  // namespace
 
+size_t attention_workspace_bytes(int64_t BH, int64_t Lq, int64_t Lk, int64_t d) {
+  return at_plan(BH, Lq, Lk, d, true).ws_bytes;
+}
+
 cudaError_t launch_attention(int dtype, const void* Q, const void* K, const void* V, void* O,
                              int o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
-                             float scale, cudaStream_t st) {
+                             float scale, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (BH == 0 || Lq == 0) return cudaSuccess;
+  AtPlan plan = at_plan(BH, Lq, Lk, d, ws != nullptr);
+  if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = at_plan(BH, Lq, Lk, d, false);
+  if (plan.items > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  AtWork work;
+  work.units_per_head = static_cast<int>((Lq + 2 * AT_BQ - 1) / (2 * AT_BQ));
+  work.whole = static_cast<int>(plan.whole);
+  work.split = static_cast<int>(plan.split);
+  work.ws = static_cast<float*>(ws);
   const CUtensorMapDataType dt = (dtype == DT_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   auto enc = [&](CUtensorMap* m, const void* p, uint64_t L, uint32_t by) {
@@ -438,11 +583,12 @@ cudaError_t launch_attention(int dtype, const void* Q, const void* K, const void
   const float sl2 = scale * 1.4426950408889634f;
   const bool bf = dtype == DT_BF16;
   const int lq = static_cast<int>(Lq), lk = static_cast<int>(Lk);
+  const int64_t it = plan.items;
   if (d == 64)
-    return bf ? at_run<64, true>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st)
-              : at_run<64, false>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st);
-  return bf ? at_run<128, true>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st)
-            : at_run<128, false>(tq, tk, tv, O, o_dtype, BH, lq, lk, sl2, st);
+    return bf ? at_run<64, true>(tq, tk, tv, O, o_dtype, work, it, lq, lk, sl2, st)
+              : at_run<64, false>(tq, tk, tv, O, o_dtype, work, it, lq, lk, sl2, st);
+  return bf ? at_run<128, true>(tq, tk, tv, O, o_dtype, work, it, lq, lk, sl2, st)
+            : at_run<128, false>(tq, tk, tv, O, o_dtype, work, it, lq, lk, sl2, st);
 }
 
 unsigned fetch_and_clear_status_attn(cudaError_t* err) {

@@ -94,9 +94,11 @@ size_t dequant_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // O = softmax(Q K^T * scale) V for BH heads: Q BH x Lq x d, K and V
 // BH x Lk x d, row-major, dtype DT_F16 / DT_BF16; d 64 or 128; O BH x Lq x d
 // of o_dtype (DT_F32, DT_BF16 or DT_F16).
+// ws / ws_bytes: scratch for the parts of split units (nullptr: no split).
 cudaError_t launch_attention(int dtype, const void* Q, const void* K, const void* V, void* O,
                              int o_dtype, int64_t BH, int64_t Lq, int64_t Lk, int64_t d,
-                             float scale, cudaStream_t st);
+                             float scale, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t attention_workspace_bytes(int64_t BH, int64_t Lq, int64_t Lk, int64_t d);
 
 // Workspace bytes the K-split needs (0: the problem is not split).
 // kind: FMT_E4M3 / FMT_E5M2 (the FP8-rate kernel, also for mixed formats),

@@ -307,6 +307,34 @@ mx_status flash_attention(const void* Q, const void* K, const void* V, void* O,
                           int64_t Lk, int64_t d, float scale, void* stream);
 
 /*
+ * flash_attention_splitkv -- flash_attention with the key axis split where
+ * SMs would otherwise idle.  A CTA computes one (head, 256 queries) unit.
+ * The units of a last, partial wave (all units, when there are fewer units
+ * than SMs, as in decoding with few queries and a long context) are each cut
+ * into up to 16 ranges of key blocks (at least two blocks each).  Each range
+ * writes its un-normalised output rows with their reference point m and row
+ * sum l into the workspace.  A second kernel merges the ranges in a fixed
+ * order as sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p, where M = max_p m_p.
+ * This is the exact identity behind the online softmax, so results stay
+ * within the flash_attention bound; they can differ from the unsplit call
+ * in the last bits.
+ *
+ *   workspace        device, 16-byte aligned, caller-owned scratch of at least
+ *                    flash_attention_workspace_bytes() bytes; contents on
+ *                    entry do not matter and are garbage after.  NULL or a
+ *                    smaller size: the call runs unsplit.
+ *   other arguments  as for flash_attention.
+ * flash_attention_workspace_bytes returns 0 when nothing would be split (the
+ * units fill whole waves, or Lk < 256), on bad arguments, or without a
+ * compute capability 10.3 device.  The size depends on the device's SM count.
+ */
+size_t flash_attention_workspace_bytes(int64_t BH, int64_t Lq, int64_t Lk, int64_t d);
+mx_status flash_attention_splitkv(const void* Q, const void* K, const void* V, void* O,
+                                  int32_t dtype, int32_t o_dtype, int64_t BH, int64_t Lq,
+                                  int64_t Lk, int64_t d, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
  * K-split variants.  When a problem's tiles leave clusters of SMs idle (a last,
  * partial wave of tiles, or fewer tiles than cluster slots), these calls
  * split the affected tiles along K across the idle clusters: each part writes

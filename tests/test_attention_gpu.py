@@ -9,9 +9,13 @@ ulp of a 16-bit output.  The fp32 scores and the hardware 2^x add far less.
 
 Covered: d = 64 and 128, both operand types, fp32 / bf16 / f16 outputs,
 ragged query and key counts (a partial last key block, a single key, a
-single query), a long key sequence whose maximum grows block after block
-(the rescaling path), the closed form Q = 0, determinism, and sampled rows
-of the full-size workloads."""
+single query), a long key sequence whose maximum grows by more than 2^8
+many times (the path that moves the exponentials' reference point and
+rescales O), the closed form Q = 0, determinism, and sampled rows of the
+full-size workloads.  The key-split entry point (flash_attention_splitkv):
+decode-like shapes with fewer units than SMs, a last partial wave beside
+whole waves, ranges whose maxima differ widely (the merge's reweighting),
+16-bit outputs, determinism, and the workspace rule."""
 import numpy as np
 import pytest
 import torch
@@ -116,12 +120,19 @@ def test_attention_zero_queries_average_values():
     assert np.allclose(O, np.repeat(mean, 130, axis=1), rtol=0, atol=1e-4)
 
 
-@pytest.mark.parametrize("name", ["attn_sam_d64", "attn_sam_d128"])
-def test_attention_workload_sampled(name):
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("name", ["attn_sam_d64", "attn_sam_d128",
+                                  "attn_long_d128"])
+def test_attention_workload_sampled(name, split):
+    """The benchmark's attention workloads at full size, through both entry
+    points (the split one as the benchmark launches it)."""
     c = workloads.attn_case(name)
     Q, K, V = workloads.attn_sources(c)
     O = nan_like((c.BH, c.Lq, c.d), torch.float32)
-    mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), out=O)
+    nbytes = mx.flash_attention_workspace_bytes(c.BH, c.Lq, c.Lk, c.d)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") \
+        if split else None
+    mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), out=O, workspace=ws)
     assert mx.mx_last_error() == 0
     g = np.random.default_rng(c.seed)
     rows = sorted(set([0, 127, 128, c.Lq - 1] +
@@ -147,3 +158,114 @@ def test_attention_negative_scale():
     O = mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), scale=-0.3)
     assert mx.mx_last_error() == 0
     _check(O, Q, K, V, scale=-0.3, what="negative scale")
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _split_call(Q, K, V, **kw):
+    BH = Q.numel() // (Q.shape[-2] * Q.shape[-1])
+    nbytes = mx.flash_attention_workspace_bytes(BH, Q.shape[-2], K.shape[-2],
+                                                Q.shape[-1])
+    assert nbytes > 0, "expected a split for this shape"
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    return mx.flash_attention(Q, K, V, workspace=ws, **kw), ws
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("BH,Lq,Lk", [(2, 128, 4096), (3, 300, 1000),
+                                      (1, 1, 777), (8, 256, 2048),
+                                      (1, 513, 600)])
+def test_attention_splitkv_shapes(dt, d, BH, Lq, Lk):
+    """Fewer (head, 256-query) units than SMs: every unit is split along the
+    keys (ragged ranges, a partial last key block in the last range)."""
+    g = torch.Generator().manual_seed(BH * 3 + Lq + Lk + d)
+    Q = torch.randn(BH, Lq, d, generator=g).to(dt)
+    K = torch.randn(BH, Lk, d, generator=g).to(dt)
+    V = torch.randn(BH, Lk, d, generator=g).to(dt)
+    O = nan_like((BH, Lq, d), torch.float32)
+    _split_call(Q.cuda(), K.cuda(), V.cuda(), out=O)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, what=f"split {dt} d{d} {BH}x{Lq}x{Lk}")
+
+
+@pytest.mark.parametrize("odt", [torch.bfloat16, torch.float16])
+def test_attention_splitkv_16bit_output(odt):
+    g = torch.Generator().manual_seed(21)
+    Q, K, V = (torch.randn(2, 256, 128, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    K = torch.randn(2, 2048, 128, generator=g).to(torch.bfloat16)
+    V = torch.randn(2, 2048, 128, generator=g).to(torch.bfloat16)
+    O, _ = _split_call(Q.cuda(), K.cuda(), V.cuda(), out_dtype=odt)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, what=f"split {odt}")
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_attention_splitkv_growing_maximum(dt):
+    """Ranges of keys whose maxima differ by tens of powers of two: the
+    merge must weight each range by 2^(m_p - M)."""
+    g = torch.Generator().manual_seed(12)
+    Lk = 1536
+    Q = torch.randn(2, 256, 64, generator=g).abs().to(dt)
+    grow = torch.linspace(0.2, 3.0, Lk).reshape(1, Lk, 1)
+    K = (torch.randn(2, Lk, 64, generator=g).abs() * grow).to(dt)
+    V = torch.randn(2, Lk, 64, generator=g).to(dt)
+    O, _ = _split_call(Q.cuda(), K.cuda(), V.cuda(), scale=0.5)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, scale=0.5, what="split growing maximum")
+
+
+def test_attention_splitkv_tail_beside_whole_waves():
+    """Five units more than one per SM: a whole wave of units runs unsplit,
+    the five left over are split; sampled rows of every head against the
+    oracle."""
+    sms = _sms()
+    BH, Lq, Lk, d = sms + 5, 256, 1024, 64
+    g = torch.Generator().manual_seed(31)
+    Q = torch.randn(BH, Lq, d, generator=g).to(torch.bfloat16)
+    K = torch.randn(BH, Lk, d, generator=g).to(torch.bfloat16)
+    V = torch.randn(BH, Lk, d, generator=g).to(torch.bfloat16)
+    O = nan_like((BH, Lq, d), torch.float32)
+    _split_call(Q.cuda(), K.cuda(), V.cuda(), out=O)
+    assert mx.mx_last_error() == 0
+    _check(O, Q, K, V, rows=[0, 77, 128, 255], what="tail beside whole waves")
+
+
+def test_attention_splitkv_deterministic_and_close_to_unsplit():
+    g = torch.Generator().manual_seed(8)
+    Q = torch.randn(4, 256, 128, generator=g).to(torch.bfloat16).cuda()
+    K = torch.randn(4, 4096, 128, generator=g).to(torch.bfloat16).cuda()
+    V = torch.randn(4, 4096, 128, generator=g).to(torch.bfloat16).cuda()
+    O1, ws = _split_call(Q, K, V)
+    O2 = mx.flash_attention(Q, K, V, workspace=ws)
+    assert torch.equal(O1, O2)
+    O0 = mx.flash_attention(Q, K, V)
+    assert mx.mx_last_error() == 0
+    # both are within the same bound of the exact result; they differ only
+    # in how the sums are grouped
+    assert (O1 - O0).abs().max().item() < 1e-3
+
+
+def test_attention_splitkv_small_workspace_runs_unsplit():
+    g = torch.Generator().manual_seed(9)
+    Q = torch.randn(2, 256, 64, generator=g).to(torch.bfloat16).cuda()
+    K = torch.randn(2, 1024, 64, generator=g).to(torch.bfloat16).cuda()
+    V = torch.randn(2, 1024, 64, generator=g).to(torch.bfloat16).cuda()
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    O1 = mx.flash_attention(Q, K, V, workspace=ws)
+    O0 = mx.flash_attention(Q, K, V)
+    assert mx.mx_last_error() == 0
+    assert torch.equal(O1, O0)
+
+
+def test_attention_workspace_rule():
+    sms = _sms()
+    assert mx.flash_attention_workspace_bytes(sms, 256, 4096, 128) == 0  # whole wave
+    assert mx.flash_attention_workspace_bytes(2, 256, 128, 128) == 0     # one key block
+    assert mx.flash_attention_workspace_bytes(2, 256, 4096, 128) > 0
+    n = mx.flash_attention_workspace_bytes(sms + 1, 256, 4096, 64)
+    # one tail unit, 16 parts of 256 rows x (64 + 2) floats
+    assert n == 16 * 256 * 66 * 4

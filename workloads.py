@@ -211,8 +211,12 @@ class AttnCase:
 
 
 def attn_cases():
+    # 32 heads x 4096 tokens (self-attention, d 64 / 128); 8 heads of 256
+    # queries against a 32768-token context (long-context prefill chunk:
+    # fewer (head, 256-query) units than SMs)
     return [AttnCase(f"attn_sam_d{d}", 32, 4096, 4096, d, "bf16", 8000 + d)
-            for d in (64, 128)]
+            for d in (64, 128)] + [
+        AttnCase("attn_long_d128", 8, 256, 32768, 128, "bf16", 8300)]
 
 
 def attn_case(name: str) -> AttnCase:
