@@ -13,10 +13,11 @@
 // that take turns on the tensor core):
 //   * warp 0: TMA -- both Q tiles once, then K and V blocks of 128 keys
 //     through a two-deep ring (3-D tensor maps, so no box crosses heads);
-//   * warp 1: tensor-memory allocation; one thread issues, per key block j
-//     and tile t, O_t += P_t,{j-1} V_{j-1} and then S_t,j = Q_t K_j^T
-//     (tcgen05.mma kind::f16, M = 128): while one tile's softmax warps work,
-//     the tensor core runs the other tile's two products;
+//   * warp 1: tensor-memory allocation; the whole warp runs the issue loop
+//     (so its descriptors stay warp-uniform) and one elected lane issues, per
+//     key block j and tile t, O_t += P_t,{j-1} V_{j-1} and then
+//     S_t,j = Q_t K_j^T (tcgen05.mma kind::f16, M = 128): while one tile's
+//     softmax warps work, the tensor core runs the other tile's two products;
 //   * warps 2..5 (tile 0) and 6..9 (tile 1): softmax, one thread per query
 //     row: the row's 128 scores from TMEM into registers, scaled to log2
 //     units, their maximum, p = 2^(x - m) rounded to the operand type (the
@@ -26,7 +27,7 @@
 //     probabilities never touch shared memory.  The exponentials' reference
 //     point moves only when a row's maximum outgrows it by more than 2^8;
 //     then the row's O is rescaled in TMEM first.  At the end O / sum.
-// Ordering: the MMA thread issues P_{j-1} V before S_j, and a commit covers
+// Ordering: the MMA lane issues P_{j-1} V before S_j, and a commit covers
 // every earlier operation of its thread, so once S_t,j is complete so is
 // the previous product that read P_t and accumulated into O_t: the softmax
 // warps may then rescale O_t and overwrite P_t without another wait.
@@ -82,6 +83,33 @@ __device__ __forceinline__ void at_timeout(volatile int* abort, unsigned site) {
 __device__ __forceinline__ uint32_t at_idesc(bool bf16, uint32_t n, uint32_t b_mn) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (b_mn << 16) |
          ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// The MMA warp runs its loop with all 32 lanes, so that the descriptors and
+// addresses it computes are warp-uniform; one elected lane (always the same
+// one: the lowest) issues each tcgen05 operation.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // Two probabilities -> a packed pair of the operand type, and the pair's
@@ -225,9 +253,13 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       const uint32_t id_qk = at_idesc(BF, AT_BK, 0);
       const uint32_t id_pv = at_idesc(BF, D, 1);
+      // descriptors of the operand regions; an MMA adds its offset (16-byte units)
+      const uint64_t dq0 = smem_desc(base + L::Q_OFF, 16, 1024, 2);
+      const uint64_t dk0 = smem_desc(base + L::K_OFF, 16, 1024, 2);
+      const uint64_t dv0 = smem_desc(base + L::V_OFF, 8192, 1024, 2);
       bool ok = mbar_wait(bar_q, 0, abort);
       if (!ok) at_timeout(abort, 0x32);
       tc_fence_after();
@@ -248,12 +280,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int kk = 0; kk < AT_BK / 16; ++kk) {
               const uint32_t boff = (kk >> 2) * (D / 64) * 8192 + (kk & 3) * 2048;
-              mma_f16_ts(o_t, s_t + 8 * kk,
-                         smem_desc(base + L::V_OFF + st * L::V_BYTES + boff, 8192, 1024, 2),
-                         id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+              mma_ts_elect(o_t, s_t + 8 * kk,
+                           dv0 + static_cast<uint64_t>((st * L::V_BYTES + boff) >> 4),
+                           id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
             }
             // both tiles' products with V_{j-1} issued: its slot frees when they end
-            if (t == 1) tc_commit_cg<1>(bar_v_empty + 8 * st);
+            if (t == 1) commit_elect(bar_v_empty + 8 * st);
           }
           if (j < nkb) {
             // S_t,j = Q_t K_j^T, after the product that read P_t
@@ -267,16 +299,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
-              mma_f16_cg<1>(s_t,
-                            smem_desc(base + L::Q_OFF + t * L::Q_BYTES + off, 16, 1024, 2),
-                            smem_desc(base + L::K_OFF + st * L::K_BYTES + off, 16, 1024, 2),
-                            id_qk, kk > 0 ? 1u : 0u);
+              mma_ss_elect(s_t, dq0 + static_cast<uint64_t>((t * L::Q_BYTES + off) >> 4),
+                           dk0 + static_cast<uint64_t>((st * L::K_BYTES + off) >> 4), id_qk,
+                           kk > 0 ? 1u : 0u);
             }
-            tc_commit_cg<1>(bar_s_full + 8 * t);
+            commit_elect(bar_s_full + 8 * t);
             // both tiles' S_j issued: K_j's slot frees when they end
-            if (t == 1) tc_commit_cg<1>(bar_k_empty + 8 * st);
+            if (t == 1) commit_elect(bar_k_empty + 8 * st);
           } else {
-            tc_commit_cg<1>(bar_o_done + 8 * t);
+            commit_elect(bar_o_done + 8 * t);
           }
         }
       }
