@@ -351,7 +351,10 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (leader && lane == 0) {
+    // the whole warp runs the loop (warp-uniform descriptors); one elected
+    // lane issues
+    if (leader) {
+      const bool issuer = elect_one();
       const uint64_t a_desc0 = smem_desc(base + L::A_OFF, 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(base + L::B_OFF, 16, 1024, 2);
       const uint32_t id = idesc_dq<CG>(a_bf16 != 0);
@@ -379,17 +382,19 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           tc_fence_after();
           const uint64_t a_d = a_desc0 + static_cast<uint64_t>((s * L::A_BYTES) >> 4);
           const uint64_t b_d = b_desc0 + static_cast<uint64_t>((s * L::B_BYTES) >> 4);
+          if (issuer) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m)      // 4 x 16 K = 64 K; 32 bytes per step
-            mma_f16_cg<CG>(acc, a_d + 2 * m, b_d + 2 * m, id, (kb > kb0 || m > 0) ? 1u : 0u);
-          tc_commit_cg<CG>(bar_empty + 8 * s);
+            for (int m = 0; m < 4; ++m)    // 4 x 16 K = 64 K; 32 bytes per step
+              mma_f16_cg<CG>(acc, a_d + 2 * m, b_d + 2 * m, id, (kb > kb0 || m > 0) ? 1u : 0u);
+            tc_commit_cg<CG>(bar_empty + 8 * s);
+          }
           if (++s == L::STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_cg<CG>(bar_acc_full + 8 * b);
+        if (issuer) tc_commit_cg<CG>(bar_acc_full + 8 * b);
       }
     }
   } else if (warp < DQ_WARP0) {

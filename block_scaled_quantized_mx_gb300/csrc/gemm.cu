@@ -308,12 +308,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread of the leader issues every MMA of the group.  The issuing
+    // One lane of the leader issues every MMA of the group.  The issuing
     // thread is the critical path (each tcgen05.mma occupies it for about as
     // long as the tensor core takes to run it), so it does nothing else per
-    // stage: one wait, the stage's MMAs, one commit.  Scale factors are
-    // copied into tensor memory by the scale-copy warp.
-    if (leader && lane == 0) {
+    // stage: one wait, the stage's MMAs, one commit.  The whole warp runs the
+    // loop, so that its descriptors and addresses are warp-uniform, and the
+    // elected lane issues (measured: MXFP4 8192^3 0.191 -> 0.164 ms, MXFP8
+    // 0.331 -> 0.322 ms against the same loop in lane 0 alone).  Scale
+    // factors are copied into tensor memory by the scale-copy warp.
+    if (leader) {
+      const bool issuer = elect_one();
       const uint64_t a_desc0 = smem_desc(base + L::A_OFF, 16, 1024, 2);
       const uint64_t b_desc0 = T::MX ? smem_desc(base + L::B_OFF, 16, 1024, 2)
                                      : smem_desc(base + L::B_OFF, 64 * 128, 1024, 2);
@@ -356,7 +360,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               const int u = m / MMAS_PER_SUB, mm = m % MMAS_PER_SUB;
               const uint64_t ad = a_d + ((u * L::A_SUB) >> 4) + mm * A_STEP;
               const uint64_t bd = b_d + ((u * L::B_SUB) >> 4) + mm * B_STEP;
-              if (KIND == KIND_F16 || KIND == KIND_BF16) {
+              if (!issuer) {
+              } else if (KIND == KIND_F16 || KIND == KIND_BF16) {
                 mma_f16_cg<CG>(tmem_base, ad, bd, idesc_f16<KIND, CG>(), acc);
               } else if (KIND == KIND_MXF8) {
                 // one scale atom (4 blocks) per sub-tile; byte mm of it
@@ -376,14 +381,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               }
             }
           }
-          tc_commit_cg<CG>(bar_empty + 8 * s);
+          if (issuer) tc_commit_cg<CG>(bar_empty + 8 * s);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_cg<CG>(bar_acc_full);
+        if (issuer) tc_commit_cg<CG>(bar_acc_full);
       }
     }
   } else if (warp < SF_WARP) {
@@ -479,7 +484,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // to the stage's sf_ready barrier, which the MMA issuer waits on.  The
     // slot is free: the stage was refilled only after the MMAs that last read
     // it had completed.
-    if (leader && lane == 0) {
+    if (leader) {
+      const bool issuer = elect_one();
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -499,14 +505,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const uint32_t sfb_t = sfa_t + T::CK * 4;
         const uint32_t sfa_s = base + L::SFA_OFF + s * L::SFA_BYTES;
         const uint32_t sfb_s = base + L::SFB_OFF + s * L::SFB_BYTES;
-        for (int c = 0; c < ck_used; ++c) {
+        for (int c = 0; c < ck_used && issuer; ++c) {
           tc_cp_32x128b_x4_cg<CG>(sfa_t + 4 * c, smem_desc(sfa_s + c * 512, 0, 128, 0));
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
             tc_cp_32x128b_x4_cg<CG>(sfb_t + c * 4 * (BN / 128) + 4 * h,
                                     smem_desc(sfb_s + (h * T::CK + c) * 512, 0, 128, 0));
         }
-        tc_commit_leader<CG>(bar_sf_ready + 8 * s);
+        if (issuer) tc_commit_leader<CG>(bar_sf_ready + 8 * s);
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
