@@ -16,21 +16,27 @@
 //   * 64 K per stage (one 128-byte swizzled row of 16-bit values).
 //   * warp 0: TMA producer -- A's tile into the operand ring; B's codes (raw
 //     bytes) and the stage's scale atom into a staging ring;
-//   * warp 1: tensor-memory allocation; one thread of the leader issues the
-//     MMAs, four per stage;
-//   * warps 2..9: epilogue, draining a double-buffered accumulator 32 columns
-//     at a time while the next tile accumulates into the other buffer;
-//   * warps 10..17: dequantizers -- one thread per 32-element block of a row
-//     of B (one scale): codes and scale to 16-bit values, written in the
-//     128-byte-swizzled K-major layout the MMA reads, then a proxy fence and
-//     an arrive on the leader's barrier.  Two dequantizing warps per
-//     scheduler hide the latency of each other's shared-memory traffic.
+//   * warp 1: tensor-memory allocation; the leader's warp runs the issue
+//     loop and one elected lane issues the MMAs, four per stage;
+//   * warps 2..5: epilogue, one per TMEM lane quarter, draining both
+//     128-column halves of a double-buffered accumulator 32 columns at a
+//     time while the next tile accumulates into the other buffer;
+//   * warps 6..29: dequantizers, three groups of eight that take the stages
+//     in turn.  A group has three stages' time for each of its own, which
+//     hides the latency of one stage's conversion chain (W4A16 8192^3: 0.94
+//     ms with one group, 0.70 with two, 0.67 with three).  In a group, one
+//     thread per 32-element block of a row of B (one scale): codes and scale
+//     to 16-bit values, written in the 128-byte-swizzled K-major layout the
+//     MMA reads, then a proxy fence and an arrive on the leader's barrier.
+//     int4 / int2 codes against a bf16 A are spread to bytes with masks and
+//     byte permutes and scaled two at a time with a packed bf16 FMA.
 // Tensor memory: accumulators in columns [0, 256) and [256, 512).
 //
 // Exactness: a code times its scale is exact in fp32 (integers by an exact
-// fused multiply-add on a magic-number float; 8- and 4-bit floats by the
-// hardware conversion to f16x2), and exact in the 16-bit type whenever the
-// value lies in its range.
+// fused multiply-add on a magic-number float, or for scales beyond the
+// constant's range by an exact subtraction and product; 8- and 4-bit floats
+// by the hardware conversion to f16x2), and exact in the 16-bit type
+// whenever the value lies in its range.
 //
 // Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records a
 // timeout in g_status_dq and the CTA shuts down in order.
@@ -48,11 +54,12 @@ __device__ unsigned int g_status_dq = 0;
 
 constexpr int DQ_KPS = 64;                 // K per stage
 constexpr int TMEM_COLS_DQ = 512;          // two 256-column accumulators
-constexpr int DQ_EPI_WARP0 = 2;            // warps 2..9
-constexpr int DQ_NUM_EPI = 8;
-constexpr int DQ_WARP0 = DQ_EPI_WARP0 + DQ_NUM_EPI;   // warps 10..17
-constexpr int DQ_NUM_DQ = 8;
-constexpr int DQ_THREADS = 32 * (DQ_WARP0 + DQ_NUM_DQ);   // 576
+constexpr int DQ_EPI_WARP0 = 2;            // warps 2..5
+constexpr int DQ_NUM_EPI = 4;
+constexpr int DQ_WARP0 = DQ_EPI_WARP0 + DQ_NUM_EPI;   // warps 6..29
+constexpr int DQ_NUM_DQ = 8;                // dequantizer warps per stage
+constexpr int DQ_GROUPS = 3;                // groups taking turns on the stages
+constexpr int DQ_THREADS = 32 * (DQ_WARP0 + DQ_GROUPS * DQ_NUM_DQ);   // 960
 constexpr int DQ_CODE_MAX = 128 * 64;      // code bytes per stage and 128 rows (8-bit)
 
 template <int CG>
@@ -100,30 +107,37 @@ __device__ __forceinline__ float scale_value(uint32_t c) {
 // Eight values of one B row (codes already in registers) -> four 16-bit
 // pairs.  Integers: a code's biased value u = q + 2^(bits-1) becomes the float
 // 2^23 + u (OR into the bit pattern of 2^23), and fma(2^23 + u, X,
-// -(2^23 + 2^(bits-1)) X) = q X exactly, rounded once.
-template <int FMT>
+// -(2^23 + 2^(bits-1)) X) = q X exactly, rounded once.  That constant
+// overflows fp32 for X >= 2^105; with SAFE the code is first turned into the
+// exact float q = (2^23 + u) - (2^23 + 2^(bits-1)) and then multiplied by X
+// (exact, or +-inf when q X itself is out of range).
+template <int FMT, bool SAFE = false>
 __device__ __forceinline__ void dq8(const uint32_t* w, int i, float X, bool bf16, uint32_t (&o)[4]) {
   float y[8];
+  // m: the bit pattern of 2^23 + u
+  auto from_magic = [&](uint32_t m, float bias_magic, float c) {
+    return SAFE ? (__uint_as_float(m) - bias_magic) * X : fmaf(__uint_as_float(m), X, c);
+  };
   if (FMT == FMT_INT8) {
     const float c = -8388736.0f * X;                     // -(2^23 + 128) X
     const uint32_t v0 = w[2 * i] ^ 0x80808080u, v1 = w[2 * i + 1] ^ 0x80808080u;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      y[e] = fmaf(__uint_as_float(__byte_perm(v0, 0x4B000000u, 0x7650 | (e << 0)) ), X, c);
-      y[4 + e] = fmaf(__uint_as_float(__byte_perm(v1, 0x4B000000u, 0x7650 | (e << 0))), X, c);
+      y[e] = from_magic(__byte_perm(v0, 0x4B000000u, 0x7650 | e), 8388736.0f, c);
+      y[4 + e] = from_magic(__byte_perm(v1, 0x4B000000u, 0x7650 | e), 8388736.0f, c);
     }
   } else if (FMT == FMT_INT4) {
     const float c = -8388616.0f * X;                     // -(2^23 + 8) X
     const uint32_t v = w[i] ^ 0x88888888u;
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      y[e] = fmaf(__uint_as_float(((v >> (4 * e)) & 0xFu) | 0x4B000000u), X, c);
+      y[e] = from_magic(((v >> (4 * e)) & 0xFu) | 0x4B000000u, 8388616.0f, c);
   } else if (FMT == FMT_INT2) {
     const float c = -8388610.0f * X;                     // -(2^23 + 2) X
     const uint32_t v = (w[i >> 1] >> (16 * (i & 1))) ^ 0xAAAAu;
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      y[e] = fmaf(__uint_as_float(((v >> (2 * e)) & 0x3u) | 0x4B000000u), X, c);
+      y[e] = from_magic(((v >> (2 * e)) & 0x3u) | 0x4B000000u, 8388610.0f, c);
   } else if (FMT == FMT_E2M1) {
     const uint32_t v = w[i];
 #pragma unroll
@@ -150,19 +164,45 @@ __device__ __forceinline__ void dq8(const uint32_t* w, int i, float X, bool bf16
 }
 
 // bf16 pairs of integer codes, the packed path for a bf16 A: the biased code
-// u = q + 2^(bits-1) (< 128) ORed into the mantissa of bf16 128.0 is the
+// u = q + 2^(bits-1) (< 128) as the low byte under the high byte 0x43 is the
 // bf16 value 128 + u, exactly; fma(128 + u, X, -(128 + 2^(bits-1)) X) = q X,
 // one rounding of an exact bf16 value (X a power of two, so every product
-// here is exact): two elements per instruction, no conversions.
-template <int BITS>
-__device__ __forceinline__ void dq8_bf16_int(uint32_t v, uint32_t x2, uint32_t c2,
-                                             uint32_t (&o)[4]) {
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t lo = (v >> (2 * BITS * p)) & ((1u << BITS) - 1u);
-    const uint32_t hi = (v >> (2 * BITS * p + BITS)) & ((1u << BITS) - 1u);
-    o[p] = fma_bf16x2(lo | (hi << 16) | 0x43004300u, x2, c2);
-  }
+// here is exact): two elements per instruction, no conversions.  The biased
+// codes are spread one per byte with masks, paired with byte permutes, and
+// the 0x43 bytes are spliced in with a last permute.
+constexpr uint32_t kBf16Hi = 0x43434343u;
+
+// 8 int4 codes (element e at bits 4e) -> four bf16 pairs (128 + u).
+__device__ __forceinline__ void int4_pairs(uint32_t v, uint32_t (&o)[4]) {
+  const uint32_t L = (v & 0x0F0F0F0Fu) ^ 0x08080808u;          // u0 u2 u4 u6
+  const uint32_t H = ((v >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // u1 u3 u5 u7
+  const uint32_t t0 = __byte_perm(L, H, 0x5140);               // u0 u1 u2 u3
+  const uint32_t t1 = __byte_perm(L, H, 0x7362);               // u4 u5 u6 u7
+  o[0] = __byte_perm(t0, kBf16Hi, 0x4140);
+  o[1] = __byte_perm(t0, kBf16Hi, 0x4342);
+  o[2] = __byte_perm(t1, kBf16Hi, 0x4140);
+  o[3] = __byte_perm(t1, kBf16Hi, 0x4342);
+}
+
+// 16 int2 codes (element e at bits 2e) -> eight bf16 pairs (128 + u),
+// elements 0..7 in o[0..3], 8..15 in o[4..7].
+__device__ __forceinline__ void int2_pairs(uint32_t v, uint32_t (&o)[8]) {
+  const uint32_t E0 = (v & 0x03030303u) ^ 0x02020202u;         // e0 e4 e8 e12
+  const uint32_t E1 = ((v >> 2) & 0x03030303u) ^ 0x02020202u;  // e1 e5 e9 e13
+  const uint32_t E2 = ((v >> 4) & 0x03030303u) ^ 0x02020202u;  // e2 e6 e10 e14
+  const uint32_t E3 = ((v >> 6) & 0x03030303u) ^ 0x02020202u;  // e3 e7 e11 e15
+  const uint32_t a = __byte_perm(E0, E1, 0x5140);              // e0 e1 e4 e5
+  const uint32_t b = __byte_perm(E2, E3, 0x5140);              // e2 e3 e6 e7
+  const uint32_t c = __byte_perm(E0, E1, 0x7362);              // e8 e9 e12 e13
+  const uint32_t d = __byte_perm(E2, E3, 0x7362);              // e10 e11 e14 e15
+  o[0] = __byte_perm(a, kBf16Hi, 0x4140);
+  o[1] = __byte_perm(b, kBf16Hi, 0x4140);
+  o[2] = __byte_perm(a, kBf16Hi, 0x4342);
+  o[3] = __byte_perm(b, kBf16Hi, 0x4342);
+  o[4] = __byte_perm(c, kBf16Hi, 0x4140);
+  o[5] = __byte_perm(d, kBf16Hi, 0x4140);
+  o[6] = __byte_perm(c, kBf16Hi, 0x4342);
+  o[7] = __byte_perm(d, kBf16Hi, 0x4342);
 }
 
 // Dequantize one 32-element block of one row of B (its codes at `codes`, its
@@ -191,19 +231,47 @@ __device__ __forceinline__ void dq_block(const uint8_t* codes, uint32_t sc, bool
     }
   }
   const float X = scale_value(sc);
-  if ((FMT == FMT_INT4 || FMT == FMT_INT2) && bf16) {
+  constexpr bool INT = (FMT == FMT_INT8 || FMT == FMT_INT4 || FMT == FMT_INT2);
+  auto put = [&](int j, const uint32_t* o) {
+    const int c = 4 * h + j;
+    *reinterpret_cast<uint4*>(dst_row + ((c ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  // -(128 + 2^(bits-1)) X is a finite bf16 up to X = 2^120 (scale code 247)
+  if ((FMT == FMT_INT4 || FMT == FMT_INT2) && bf16 && sc <= 247u) {
     constexpr int BITS = (FMT == FMT_INT4) ? 4 : 2;
     const uint32_t xb = __float_as_uint(X) >> 16;                      // exact
     const uint32_t cb = __float_as_uint(-(128.0f + (1 << (BITS - 1))) * X) >> 16;
     const uint32_t x2 = xb | (xb << 16), c2 = cb | (cb << 16);
+    if (BITS == 4) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t o[4];
+        int4_pairs(w[j], o);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = fma_bf16x2(o[e], x2, c2);
+        put(j, o);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t o[8];
+        int2_pairs(w[k], o);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = fma_bf16x2(o[e], x2, c2);
+        put(2 * k, o);
+        put(2 * k + 1, o + 4);
+      }
+    }
+    return;
+  }
+  // the fp32 magic constant -(2^23 + 2^(bits-1)) X is finite up to X = 2^104
+  // (scale code 231); larger scales of integer codes take the exact two-step
+  if (INT && sc > 231u) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t o[4];
-      const uint32_t v = (BITS == 4) ? (w[j] ^ 0x88888888u)
-                                     : ((w[j >> 1] >> (16 * (j & 1))) ^ 0xAAAAu);
-      dq8_bf16_int<BITS>(v, x2, c2, o);
-      const int c = 4 * h + j;
-      *reinterpret_cast<uint4*>(dst_row + ((c ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      dq8<FMT, true>(w, j, X, bf16, o);
+      put(j, o);
     }
     return;
   }
@@ -211,8 +279,7 @@ __device__ __forceinline__ void dq_block(const uint8_t* codes, uint32_t sc, bool
   for (int j = 0; j < 4; ++j) {
     uint32_t o[4];
     dq8<FMT>(w, j, X, bf16, o);
-    const int c = 4 * h + j;
-    *reinterpret_cast<uint4*>(dst_row + ((c ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    put(j, o);
   }
 }
 
@@ -400,7 +467,6 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp < DQ_WARP0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                          // TMEM lane quarter
-    const int cg_ = (warp - DQ_EPI_WARP0) >> 2;      // which 128 columns
     uint32_t tc = 0;
     for (int w = cluster_id; w < work.total; w += num_clusters, ++tc) {
       int mb, nb, kb0, kb1;
@@ -412,6 +478,8 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       }
       tc_fence_after();
       const int64_t row = static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q + lane;
+#pragma unroll 1
+      for (int cg_ = 0; cg_ < BN / 128; ++cg_) {
       const int col0 = nb * BN + cg_ * 128;
       uint32_t sf_word = 0;
 #pragma unroll 1
@@ -444,6 +512,7 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       }
       if ((OUT == OUT_MX8 || OUT == OUT_MX4) && split == 1)
         store_mx_scales(sf_word, epi, row, col0, N);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -455,9 +524,13 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
   } else {
     // ------------------------------------------------------------ dequantizers
-    // Unit u = thread + 256 i (i < 2 / CG) is block u % 2 of row u / 2 of this
+    // Group grp takes the stages with it % DQ_GROUPS == grp.  In a group,
+    // unit u = thread + 256 i (i < 2 / CG) is block u % 2 of row u / 2 of this
     // CTA's rows of B: 32 codes and one scale.
-    const int t = threadIdx.x - 32 * DQ_WARP0;
+    const int tg = threadIdx.x - 32 * DQ_WARP0;
+    const int t = tg % (32 * DQ_NUM_DQ);
+    const uint32_t grp = static_cast<uint32_t>(tg / (32 * DQ_NUM_DQ));
+    uint32_t it = 0;
     const uint32_t dq_full0 = (CG == 2) ? map_to_cta(bar_dq_full, 0) : bar_dq_full;
     const int block_bytes = row_bytes / 2;
     int s = 0;
@@ -468,6 +541,14 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       work.item(w, mb, nb, kb0, kb1);
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
+        // the groups take the stages in turn
+        if ((it++ % DQ_GROUPS) != grp) {
+          if (++s == L::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+          continue;
+        }
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort) ||
             !mbar_wait(bar_codes + 8 * s, ph, abort)) {
           dq_timeout(abort, 0x25);

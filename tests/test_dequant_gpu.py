@@ -102,6 +102,28 @@ def test_dequant_wide_scales_bf16(fmt):
     check_close(np.where(ok, C.cpu().numpy(), Cr), Cr, S, "f32", "wide scales")
 
 
+@pytest.mark.parametrize("fmt", [oracle.INT8, oracle.INT4, oracle.INT2])
+def test_dequant_extreme_scales_bf16(fmt):
+    """Scale codes from 226 up to the largest whose every q X fits bf16
+    (int8: -128 X, so X <= 2^120, code 247; int4 / int2: code 248), against
+    a bf16 A of magnitude 2^-100 so that every product stays in range: the
+    integer paths must stay exact where their multiply-add constants would
+    overflow (fp32 beyond X = 2^104, bf16 beyond X = 2^120)."""
+    M, N, K = 128, 256, 256
+    g = torch.Generator().manual_seed(70 + fmt)
+    A = (torch.randn(M, K, generator=g) * 2.0 ** -100).to(torch.bfloat16)
+    hi = 247 if fmt == oracle.INT8 else 248
+    cb, sb = workloads.random_codes((N, K), fmt, seed=71 + fmt, scale_lo=226,
+                                    scale_hi=hi)
+    b = planes_from_codes(cb, sb, fmt)
+    C = nan_like((M, N), torch.float32)
+    mx.gemm_dequant(A.cuda(), b, out_dtype=torch.float32, out=C)
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_a16_bmx(f16_bits(A), oracle.BF16, cb, sb, fmt)
+    assert (S < 1e37).all() and sb.max() == hi and sb.min() <= 231
+    check_close(C.cpu().numpy(), Cr, S, "f32", f"extreme scales fmt{fmt}")
+
+
 @pytest.mark.parametrize("fmt", [oracle.INT4, oracle.E2M1])
 @pytest.mark.parametrize("act", [oracle.ACT_GELU, oracle.ACT_GELU_TANH])
 def test_dequant_fused_epilogue(fmt, act):
