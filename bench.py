@@ -45,6 +45,10 @@ NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0,
                  "mxfp8_e5m2": 2.0, "w4a8": 2.0,
                  # weight-only: B dequantized to bf16, the bf16 tensor rate
                  "w8a16": 1.0, "w4a16": 1.0, "w2a16": 1.0}
+# the per-clock rate of each kind's tcgen05.mma relative to bf16, measured on
+# GB300 with back-to-back MMAs (M = 128, N = 256): fp8 2x, every FP4 form 4x
+# (not the nominal 6x)
+INSTRUCTION_RATIO = dict(NOMINAL_RATIO, mxfp4=4.0)
 DTYPE_NAME = {"mxfp8": "e4m3", "mxfp4": "e2m1", "mxfp8_e5m2": "e5m2",
               "w4a8": "e4m3 x e2m1"}
 
@@ -533,6 +537,9 @@ def run_ours(args, rank, world, local_rank):
                                         splitk=args.splitk)
             others[name] = {"gemm_ms": ms_o, "tflops": tf_o,
                             "frac_of_peak": tf_o / (bf16 * NOMINAL_RATIO[oc.kind])}
+            if INSTRUCTION_RATIO[oc.kind] != NOMINAL_RATIO[oc.kind]:
+                others[name]["frac_of_instruction_rate"] = \
+                    tf_o / (bf16 * INSTRUCTION_RATIO[oc.kind])
             if workloads.is_dequant(oc):
                 gbs = dequant_bytes(oc) / ms_o / 1e6
                 others[name].update({"gbs": gbs, "frac_of_hbm": gbs / hbm})
