@@ -9,8 +9,8 @@
 // maximum, the running sum and the final division that make the blockwise
 // form equal softmax over all keys are FlashAttention's online softmax.
 //
-// Design (one CTA per (head, 256 queries), 10 warps, two query tiles of 128
-// that take turns on the tensor core):
+// Design (one CTA per (head, 256 queries), 12 warps in three warpgroups, two
+// query tiles of 128 that take turns on the tensor core):
 //   * warp 0: TMA -- both Q tiles once, then K and V blocks of 128 keys
 //     through a two-deep ring (3-D tensor maps, so no box crosses heads);
 //   * warp 1: tensor-memory allocation; the whole warp runs the issue loop
@@ -18,7 +18,9 @@
 //     key block j and tile t, O_t += P_t,{j-1} V_{j-1} and then
 //     S_t,j = Q_t K_j^T (tcgen05.mma kind::f16, M = 128): while one tile's
 //     softmax warps work, the tensor core runs the other tile's two products;
-//   * warps 2..5 (tile 0) and 6..9 (tile 1): softmax, one thread per query
+//   * warps 2, 3: idle (they complete warpgroup 0, whose registers go to the
+//     softmax warpgroups);
+//   * warps 4..7 (tile 0) and 8..11 (tile 1): softmax, one thread per query
 //     row: the row's 128 scores from TMEM into registers, scaled to log2
 //     units, their maximum, p = 2^(x - m) rounded to the operand type (the
 //     running sum adds exactly the rounded values), written back over the
@@ -52,7 +54,14 @@ __device__ unsigned int g_status_attn = 0;
 
 constexpr int AT_BQ = 128;          // queries per tile (two tiles per CTA)
 constexpr int AT_BK = 128;          // keys per block
-constexpr int AT_THREADS = 320;     // warps 0, 1 and two softmax warpgroups
+constexpr int AT_THREADS = 384;     // warpgroup 0 (TMA, MMA, 2 idle), two softmax warpgroups
+// Registers: launched at 168 per thread (384 threads); warpgroup 0 gives its
+// share down to 80 and the softmax warpgroups take theirs up to 208:
+// 80 * 128 + 208 * 256 = 63488 <= 384 * 168 = 64512, the launch's
+// allocation, so the increase never waits on registers that do not exist.
+// (56 / 224 made the MMA warp spill; 80 / 208 spills nowhere.)
+constexpr int AT_REGS_LOW = 80;
+constexpr int AT_REGS_HIGH = 208;
 constexpr int AT_TMEM_COLS = 512;
 constexpr float AT_LAZY = 8.0f;     // slack of the exponentials' reference point
 
@@ -199,6 +208,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Each role's code sits inside the branch that sets its register count,
+  // so the compiler allots each its own budget; every warp of a warpgroup
+  // executes the same setmaxnreg.
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_REGS_LOW));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -312,9 +326,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_HIGH));
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;                          // query tile
+    const int t = (warp - 4) >> 2;                          // query tile
     const int quarter = warp & 3;
     const int row = 32 * quarter + lane;                    // row in the tile
     const uint32_t lane_addr =
