@@ -21,8 +21,10 @@
 //   * warps 2, 3: idle (they complete warpgroup 0, whose registers go to the
 //     softmax warpgroups);
 //   * warps 4..7 (tile 0) and 8..11 (tile 1): softmax, one thread per query
-//     row: the row's 128 scores from TMEM into registers, scaled to log2
-//     units, their maximum, p = 2^(x - m) rounded to the operand type (the
+//     row: the row's 128 scores from TMEM into registers; their maximum in
+//     log2 units (for a full key block taken on the raw scores and scaled
+//     once, the scale then folded into the exponent's FMA); p = 2^(x - m)
+//     rounded to the operand type (the
 //     running sum adds exactly the rounded values), written back over the
 //     scores as the packed A operand of
 //     the P V product, which reads it from tensor memory -- the
@@ -355,13 +357,25 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+      float s_eff = 1.0f;
       if (valid >= AT_BK) {
+        // a full block: the scale goes into the exponent's FMA instead of a
+        // multiply per score; the largest scaled score is the scale times
+        // the largest raw score (the smallest, for a negative scale) --
+        // rounding is monotonic, so this is exactly the maximum of the
+        // rounded products.  A partial block scales and masks as below.
+        s_eff = scale_log2e;
+        if (scale_log2e >= 0.0f) {
 #pragma unroll
-        for (int e = 0; e < AT_BK; ++e) {
-          const float x = __uint_as_float(sv[e]) * scale_log2e;
-          sv[e] = __float_as_uint(x);
-          mx8[e & 7] = fmaxf(mx8[e & 7], x);
+          for (int e = 0; e < AT_BK; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = INFINITY;
+#pragma unroll
+          for (int e = 0; e < AT_BK; ++e) mx8[e & 7] = fminf(mx8[e & 7], __uint_as_float(sv[e]));
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] *= scale_log2e;
       } else {
 #pragma unroll
         for (int e = 0; e < AT_BK; ++e) {
@@ -401,8 +415,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float x0 = __uint_as_float(sv[32 * c + 2 * e]) - m_new;
-          const float x1 = __uint_as_float(sv[32 * c + 2 * e + 1]) - m_new;
+          const float x0 = fmaf(__uint_as_float(sv[32 * c + 2 * e]), s_eff, -m_new);
+          const float x1 = fmaf(__uint_as_float(sv[32 * c + 2 * e + 1]), s_eff, -m_new);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
           float r0, r1;

@@ -140,6 +140,23 @@ def test_attention_workload_sampled(name, split):
     _check(O, Q, K, V, rows=rows, what=name)
 
 
+@pytest.mark.parametrize("Lk", [256, 300])
+def test_attention_zero_scale_averages_values(Lk):
+    """scale = 0: every key gets the same weight, so each output row is the
+    mean of V's rows (full key blocks fold the scale into the exponent,
+    the partial last block of Lk = 300 scales and masks)."""
+    g = torch.Generator().manual_seed(17)
+    Q, K = (torch.randn(2, 200, 64, generator=g).to(torch.bfloat16)
+            for _ in range(2))
+    K = torch.randn(2, Lk, 64, generator=g).to(torch.bfloat16)
+    V = torch.randn(2, Lk, 64, generator=g).to(torch.bfloat16)
+    O = mx.flash_attention(Q.cuda(), K.cuda(), V.cuda(), scale=0.0)
+    assert mx.mx_last_error() == 0
+    mean = V.double().numpy().mean(axis=1, keepdims=True)
+    assert np.allclose(O.cpu().numpy(), np.repeat(mean, 200, axis=1), rtol=0,
+                       atol=1e-4)
+
+
 def test_attention_deterministic():
     g = torch.Generator().manual_seed(6)
     Q, K, V = (torch.randn(4, 512, 128, generator=g).to(torch.bfloat16).cuda()
