@@ -24,8 +24,9 @@
 //     row: the row's 128 scores from TMEM into registers; their maximum in
 //     log2 units (for a full key block taken on the raw scores and scaled
 //     once, the scale then folded into the exponent's FMA); p = 2^(x - m)
-//     rounded to the operand type (the
-//     running sum adds exactly the rounded values), written back over the
+//     rounded to the operand type (the running sum adds the fp32 values:
+//     each output is then within the rounding unit of the operand type,
+//     relative to sum_j w_j |v_j|, of the exact one), written back over the
 //     scores as the packed A operand of
 //     the P V product, which reads it from tensor memory -- the
 //     probabilities never touch shared memory.  The exponentials' reference
@@ -123,18 +124,9 @@ __device__ __forceinline__ void commit_elect(uint32_t bar) {
       : "memory");
 }
 
-// Two probabilities -> a packed pair of the operand type, and the pair's
-// rounded values back as floats (added to the running sum).
-__device__ __forceinline__ uint32_t pack_p(float a, float b, bool bf16, float& ra, float& rb) {
-  if (bf16) {
-    const uint32_t w = cvt_bf16x2(a, b);
-    ra = __uint_as_float(w << 16);
-    rb = __uint_as_float(w & 0xFFFF0000u);
-    return w;
-  }
-  const uint32_t w = cvt_f16x2(a, b);
-  f16x2_to_f32(w, ra, rb);
-  return w;
+// Two probabilities -> a packed pair of the operand type.
+__device__ __forceinline__ uint32_t pack_p(float a, float b, bool bf16) {
+  return bf16 ? cvt_bf16x2(a, b) : cvt_f16x2(a, b);
 }
 
 // The work of one launch: units are (head, 256 queries), head-major.  Units
@@ -419,9 +411,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           const float x1 = fmaf(__uint_as_float(sv[32 * c + 2 * e + 1]), s_eff, -m_new);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
-          float r0, r1;
-          pk[e] = pack_p(p0, p1, BF, r0, r1);
-          sum4[e & 3] += r0 + r1;
+          pk[e] = pack_p(p0, p1, BF);
+          sum4[e & 3] += p0 + p1;
         }
         tmem_st_32x32b_x16(lane_addr + 16 * c, pk);
       }

@@ -297,10 +297,10 @@ mx_status gemm_dequant_splitk(const void* A, int32_t a_dtype, int64_t M,
  *   d        64 or 128; Lk >= 1 when Lq >= 1; BH <= 65535
  *   scale    multiplies Q K^T (commonly 1/sqrt(d)); finite
  * The scores accumulate in fp32; the probabilities are rounded to dtype
- * before the product with V, and the row sums add exactly those rounded
- * values, so each output row is a weighted mean of V's rows whose weights
- * differ from the exact softmax by at most that rounding (relative 2^-8 for
- * bf16, 2^-11 for f16).  No mask.
+ * before the product with V and the row sums add them in fp32, so each
+ * output row is a combination of V's rows whose weights differ from the
+ * exact softmax by at most that rounding (relative 2^-8 for bf16, 2^-11 for
+ * f16).  No mask.
  */
 mx_status flash_attention(const void* Q, const void* K, const void* V, void* O,
                           int32_t dtype, int32_t o_dtype, int64_t BH, int64_t Lq,

@@ -1,11 +1,12 @@
 """flash_attention on the GPU vs the float64 oracle.
 
 Tolerance (per element, Sv = sum_j w_j |v_jc| from the oracle): the kernel
-rounds each probability to the operand type (relative 2^-9 for bf16, 2^-12
-for f16) and normalises by the sum of exactly those rounded values, so each
-weight moves by at most twice that and each output by at most
-2^-8 Sv (bf16) / 2^-11 Sv (f16); the bound used allows twice that, plus one
-ulp of a 16-bit output.  The fp32 scores and the hardware 2^x add far less.
+rounds each probability p_j to the operand type (relative error at most the
+unit roundoff u = 2^-8 for bf16, 2^-11 for f16) before the product with V
+and divides by the fp32 sum of the unrounded p, so each weight differs from
+softmax by at most u relative and each output by at most u Sv; the bound
+used allows twice that (2^-7 Sv / 2^-10 Sv), plus one ulp of a 16-bit
+output.  The fp32 scores, the sum and the hardware 2^x add far less.
 
 Covered: d = 64 and 128, both operand types, fp32 / bf16 / f16 outputs,
 ragged query and key counts (a partial last key block, a single key, a
