@@ -597,6 +597,81 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------------------ provenance
+
+def source_hash() -> str:
+    """sha256 (first 16 hex digits) of every CUDA source and header the
+    library is built from: identifies the code where no git metadata is."""
+    import glob
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "block_scaled_quantized_mx_gb300", "csrc", "*"))
+                   + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def provenance_rows(line):
+    """One record per measured operation of a bench line: the code
+    (source hash, and the git commit where there is one), the workload's
+    shapes and seeds, times, throughput, fractions of peak, SM clock and the
+    environment."""
+    try:
+        commit = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"],
+                                capture_output=True, text=True,
+                                timeout=5).stdout.strip() or None
+    except Exception:
+        commit = None
+    env = {"sources": source_hash(), "commit": commit,
+           "utc": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
+           "torch": torch.__version__, "cuda": torch.version.cuda,
+           "device": torch.cuda.get_device_name(0) if torch.cuda.is_available() else None,
+           "nproc": os.cpu_count(),
+           "sm_mhz": (line.get("clocks") or {}).get("sm_mhz"),
+           "clock_reasons": (line.get("clocks") or {}).get("reasons")}
+
+    def case_fields(name):
+        try:
+            c = workloads.case(name)
+            return {"M": c.M, "N": c.N, "K": c.K, "seed_a": c.seed_a,
+                    "seed_b": c.seed_b, "kind": c.kind, "out": c.out}
+        except KeyError:
+            c = workloads.attn_case(name)
+            return {"BH": c.BH, "Lq": c.Lq, "Lk": c.Lk, "d": c.d,
+                    "seed": c.seed, "kind": "attention", "out": "bf16"}
+
+    cfg = line["config"]
+    rows = [dict(env, op="step", workload=cfg["workload"],
+                 **case_fields(cfg["workload"]), ms=line["ms_per_step"],
+                 tflops=line["value"],
+                 frac_of_peak=(line.get("roofline") or {}).get("frac"),
+                 breakdown=line.get("breakdown"))]
+    for name, r in (line.get("gemm_only_other_workloads") or {}).items():
+        rows.append(dict(env, op="gemm", workload=name, **case_fields(name),
+                         ms=r["gemm_ms"], tflops=r["tflops"],
+                         frac_of_peak=r["frac_of_peak"],
+                         frac_of_instruction_rate=r.get("frac_of_instruction_rate"),
+                         gbs=r.get("gbs")))
+    for name, r in (line.get("fused_epilogue") or {}).items():
+        rows.append(dict(env, op="fused_epilogue", workload=name,
+                         **case_fields(name), ms=r["fused_ms"],
+                         tflops=r.get("fused_tflops"), plain_ms=r["gemm_ms"],
+                         decomposed_ms=r["decomposed_ms"],
+                         fused_quantize_ms=r["fused_quantize_ms"]))
+    for name, r in (line.get("attention") or {}).items():
+        rows.append(dict(env, op="attention", workload=name,
+                         **case_fields(name), ms=r["ms"], tflops=r["tflops"],
+                         frac_of_peak=r.get("frac_of_peak"),
+                         unsplit_ms=r.get("unsplit_ms")))
+    if line.get("e2e"):
+        rows.append(dict(env, op="e2e", workload=cfg["workload"],
+                         **case_fields(cfg["workload"]),
+                         ms=line["e2e"]["ms_per_step"],
+                         tflops=line["e2e"]["value"]))
+    return rows
+
+
 # ------------------------------------------------------------------ oracle
 
 def oracle_sample(c, budget_s: float):
@@ -695,6 +770,9 @@ def parse_args(argv=None):
     ap.add_argument("--attention", default="attn_sam_d64,attn_sam_d128,attn_long_d128",
                     help="attention workloads timed with flash_attention")
     ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--jsonl", default=None,
+                    help="append one provenance record per measured operation "
+                         "(code hash, shapes, seeds, times, clocks, environment)")
     ap.add_argument("--splitk", action="store_true",
                     help="use the K-split GEMM entry points (with a workspace)")
     return ap.parse_args(argv)
@@ -733,6 +811,10 @@ def main(argv=None):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+        if args.jsonl:
+            with open(args.jsonl, "a") as f:
+                for row in provenance_rows(line):
+                    f.write(json.dumps(row) + "\n")
 
 
 if __name__ == "__main__":
