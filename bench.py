@@ -332,6 +332,29 @@ def time_attention(mx, c, dev, flusher):
             "library_reference": "torch scaled_dot_product_attention (context only)"}
 
 
+def cublaslt_mx_reference(c, qa, qb, out_dt, C, mx):
+    """Context only: cuBLASLt's MXFP8 GEMM (torch._scaled_mm with UE8M0
+    block scales) on the step's own quantized planes -- the scale plane is
+    the tensor-core layout both read -- timed the same way as the step's
+    GEMM (mean CUDA-event time, L2 flushed before every launch), and
+    whether its C equals ours bit for bit."""
+    try:
+        af = qa.data.view(torch.float8_e4m3fn).view(c.M, c.K)
+        bf = qb.data.view(torch.float8_e4m3fn).view(c.N, c.K)
+        sa = qa.scales.view(torch.float8_e8m0fnu)
+        sb = qb.scales.view(torch.float8_e8m0fnu)
+        f = lambda: torch._scaled_mm(af, bf.t(), scale_a=sa, scale_b=sb,  # noqa
+                                     out_dtype=out_dt)
+        Ct = f()
+        same = bool(torch.equal(Ct, C))
+        ms = event_time(f, flusher=L2Flusher(C.device))
+    except Exception as e:                     # no block-scaled path in torch
+        return {"unavailable": "%s: %s" % (type(e).__name__, str(e)[:120])}
+    return {"library": "cuBLASLt MXFP8 via torch._scaled_mm (context only)",
+            "ms": ms, "tflops": flops_of(c) / (ms * 1e-3) / 1e12,
+            "bit_identical_c": same}
+
+
 def dequant_bytes(c):
     """Algorithmic bytes of one gemm_dequant: bf16 A read, B's codes and
     scales read, C written."""
@@ -457,6 +480,8 @@ def run_ours(args, rank, world, local_rank):
         extra["quantize_b_gbs"] = quant_bytes(fb, c.N, c.K) / qb_ms / 1e6
         extra["quantize_a_frac_hbm"] = extra["quantize_a_gbs"] / hbm
         extra["quantize_b_frac_hbm"] = extra["quantize_b_gbs"] / hbm
+        if rank == 0 and fa == fb == 1:
+            extra["library_reference"] = cublaslt_mx_reference(c, qa, qb, out_dt, C, mx)
 
     # ---- end to end through the C ABI with host buffers
     # Every step copies its fp32 inputs from pinned host memory and its

@@ -302,3 +302,32 @@ def test_deterministic(name):
         C1 = mx.mx_gemm(a, b)
         C2 = mx.mx_gemm(a, b)
     assert torch.equal(C1.view(torch.uint8), C2.view(torch.uint8))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (1024, 1024, 1024)])
+def test_matches_cublaslt_block_scaled(M, N, K):
+    """An independent check of the data and scale planes: cuBLASLt's MXFP8
+    GEMM (through torch._scaled_mm with UE8M0 block scales) reads the
+    library's quantized bytes and scale planes as they are -- the scale
+    plane is the tensor-core scale-factor layout both use -- and its bf16 C
+    equals mx_gemm's bit for bit (both accumulate the same products in fp32
+    in the same K order).  Skipped where torch has no block-scaled path."""
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch without UE8M0 scales")
+    g = torch.Generator().manual_seed(M + N + K)
+    A = torch.randn(M, K, generator=g).cuda()
+    B = torch.randn(K, N, generator=g).cuda()
+    a = mx.mx_quantize(A, mx.E4M3)
+    b = mx.mx_quantize(B, mx.E4M3, k_strided=True)
+    C = mx.mx_gemm(a, b, out_dtype=torch.bfloat16)
+    assert mx.mx_last_error() == 0
+    af = a.data.view(torch.float8_e4m3fn).view(M, K)
+    bf = b.data.view(torch.float8_e4m3fn).view(N, K)
+    try:
+        Ct = torch._scaled_mm(af, bf.t(), scale_a=a.scales.view(torch.float8_e8m0fnu),
+                              scale_b=b.scales.view(torch.float8_e8m0fnu),
+                              out_dtype=torch.bfloat16)
+    except (RuntimeError, TypeError, ValueError) as e:
+        pytest.skip(f"no block-scaled cuBLASLt path: {e}")
+    assert torch.equal(C.view(torch.int16), Ct.view(torch.int16))
+
