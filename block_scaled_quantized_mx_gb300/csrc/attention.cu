@@ -552,6 +552,14 @@ cudaError_t at_run(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if (dev >= 64 || !attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the registers it asks for are free: it can
+    // only complete if the launch allocated at least what the two splits
+    // add up to.  Refuse to launch otherwise instead of waiting forever.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * AT_THREADS < AT_REGS_LOW * 128 + AT_REGS_HIGH * 256)
+      return cudaErrorInvalidConfiguration;
     if (dev < 64) attr_set[dev] = true;
   }
   kern<<<static_cast<unsigned>(items), AT_THREADS, L::ALLOC, st>>>(tq, tk, tv, O, o_dtype, Lq, Lk,
