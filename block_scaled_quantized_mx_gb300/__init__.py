@@ -13,6 +13,7 @@ load, every call raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from dataclasses import dataclass
 
@@ -177,10 +178,12 @@ class MXTensor:
                          self.fmt, self.outer, self.K)
 
 
+@functools.lru_cache(maxsize=1024)
 def data_bytes(fmt: int, outer: int, K: int) -> int:
     return int(lib().mx_data_bytes(fmt, outer, K))
 
 
+@functools.lru_cache(maxsize=1024)
 def scale_bytes(outer: int, K: int) -> int:
     return int(lib().mx_scale_bytes(outer, K))
 
@@ -191,6 +194,38 @@ def empty_mx(fmt: int, outer: int, K: int, device="cuda") -> MXTensor:
     return MXTensor(torch.empty(nd, dtype=torch.uint8, device=device),
                     torch.empty(ns, dtype=torch.uint8, device=device),
                     fmt, outer, K)
+
+
+def _check_mx(t: MXTensor, name: str, fmt=None, outer=None, K=None):
+    """An MX tensor's planes are contiguous buffers holding at least the
+    bytes the library reads or writes for its format and shape (the C ABI
+    receives bare pointers and cannot check their extent)."""
+    if ((fmt is not None and t.fmt != fmt) or
+            (outer is not None and t.outer != outer) or
+            (K is not None and t.K != K)):
+        raise ValueError(f"{name} must be format {fmt}, {outer} x {K}")
+    for plane, need in ((t.data, data_bytes(t.fmt, t.outer, t.K)),
+                        (t.scales, scale_bytes(t.outer, t.K))):
+        if not plane.is_contiguous():
+            raise ValueError(f"{name}: planes must be contiguous")
+        if plane.numel() * plane.element_size() < need:
+            raise ValueError(f"{name}: a plane holds fewer than the {need} "
+                             "bytes its format and shape need")
+
+
+def _check_out(out: torch.Tensor, rows: int, cols: int, dtype):
+    """A caller-supplied output matrix: of the requested dtype, on the GPU,
+    rows x cols with a unit inner stride (its row stride becomes ldc)."""
+    if out.dtype != dtype or not out.is_cuda:
+        raise ValueError(f"out must be a {dtype} CUDA tensor")
+    if out.dim() != 2 or tuple(out.shape) != (rows, cols):
+        raise ValueError(f"out must be {rows} x {cols}")
+    if cols > 1 and out.stride(1) != 1:
+        raise ValueError("out must have a unit inner stride")
+
+
+def _nbytes(t: torch.Tensor | None) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
 
 
 def mx_quantize(src: torch.Tensor, fmt: int, k_strided: bool = False,
@@ -208,6 +243,7 @@ def mx_quantize(src: torch.Tensor, fmt: int, k_strided: bool = False,
         outer, K = src.shape
     if out is None:
         out = empty_mx(fmt, outer, K, src.device)
+    _check_mx(out, "out", fmt, outer, K)
     ct = out.c()
     _check(lib().mx_quantize(src.data_ptr(), src.stride(0),
                              SRC_K_STRIDED if k_strided else SRC_K_CONTIGUOUS,
@@ -230,12 +266,15 @@ def mx_gemm(A: MXTensor, B: MXTensor, out_dtype=torch.bfloat16,
     two may hold different element formats.  With a workspace (a CUDA tensor of at least mx_gemm_workspace_bytes()
     bytes) the K-split entry point is used."""
     dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    _check_mx(A, "A")
+    _check_mx(B, "B")
     if out is None:
         out = torch.empty((A.outer, B.outer), dtype=out_dtype,
                           device=A.data.device)
+    _check_out(out, A.outer, B.outer, out_dtype)
     ca, cb = A.c(), B.c()
     cptr = out.data_ptr() if out.numel() else None
-    ldc = out.stride(0) if out.dim() == 2 else B.outer
+    ldc = out.stride(0)
     if workspace is None:
         _check(lib().mx_gemm(ctypes.byref(ca), ctypes.byref(cb), cptr, dt, ldc,
                              _stream(stream)), "mx_gemm")
@@ -243,7 +282,7 @@ def mx_gemm(A: MXTensor, B: MXTensor, out_dtype=torch.bfloat16,
         _check(lib().mx_gemm_splitk(
             ctypes.byref(ca), ctypes.byref(cb), cptr, dt, ldc,
             workspace.data_ptr() if workspace.numel() else None,
-            workspace.numel() * workspace.element_size(), _stream(stream)),
+            _nbytes(workspace), _stream(stream)),
             "mx_gemm_splitk")
     return out
 
@@ -259,6 +298,7 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
         raise ValueError("inner dimensions differ")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check_out(out, M, N, torch.float32)
     dt = DT_F16 if A.dtype == torch.float16 else DT_BF16
     args = (A.data_ptr() if A.numel() else None,
             B.data_ptr() if B.numel() else None,
@@ -269,7 +309,7 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None,
     else:
         _check(lib().gemm_f16_splitk(
             *args, workspace.data_ptr() if workspace.numel() else None,
-            workspace.numel() * workspace.element_size(), _stream(stream)),
+            _nbytes(workspace), _stream(stream)),
             "gemm_f16_splitk")
     return out
 
@@ -295,11 +335,14 @@ def mx_gemm_fused(A: MXTensor, B: MXTensor, bias: torch.Tensor | None = None,
     fp32 accumulator inside the GEMM epilogue."""
     _check_bias(bias, B.outer)
     dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    _check_mx(A, "A")
+    _check_mx(B, "B")
     if out is None:
         out = torch.empty((A.outer, B.outer), dtype=out_dtype,
                           device=A.data.device)
+    _check_out(out, A.outer, B.outer, out_dtype)
     ca, cb, ep = A.c(), B.c(), _epilogue(bias, act)
-    ldc = out.stride(0) if out.dim() == 2 else B.outer
+    ldc = out.stride(0)
     _check(lib().mx_gemm_fused(ctypes.byref(ca), ctypes.byref(cb),
                                ctypes.byref(ep),
                                out.data_ptr() if out.numel() else None, dt,
@@ -314,8 +357,11 @@ def mx_gemm_fused_quantize(A: MXTensor, B: MXTensor, fmt: int,
     """act(A * B + bias) quantized in the GEMM epilogue to an M x N MX
     tensor (blocks of 32 along N) of element format fmt."""
     _check_bias(bias, B.outer)
+    _check_mx(A, "A")
+    _check_mx(B, "B")
     if out is None:
         out = empty_mx(fmt, A.outer, B.outer, A.data.device)
+    _check_mx(out, "out", fmt, A.outer, B.outer)
     ca, cb, cc, ep = A.c(), B.c(), out.c(), _epilogue(bias, act)
     _check(lib().mx_gemm_fused_quantize(ctypes.byref(ca), ctypes.byref(cb),
                                         ctypes.byref(ep), ctypes.byref(cc),
@@ -337,6 +383,7 @@ def gemm_f16_fused(A: torch.Tensor, B: torch.Tensor,
     _check_bias(bias, N)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check_out(out, M, N, torch.float32)
     dt = DT_F16 if A.dtype == torch.float16 else DT_BF16
     ep = _epilogue(bias, act)
     _check(lib().gemm_f16_fused(
@@ -368,20 +415,22 @@ def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
         raise ValueError("inner dimensions differ")
     _check_bias(bias, B.outer)
     dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    _check_mx(B, "B")
     if out is None:
         out = torch.empty((M, B.outer), dtype=out_dtype, device=A.device)
+    _check_out(out, M, B.outer, out_dtype)
     cb, ep = B.c(), _epilogue(bias, act)
     args = (A.data_ptr() if A.numel() else None,
             DT_F16 if A.dtype == torch.float16 else DT_BF16, M, A.stride(0),
             ctypes.byref(cb), ctypes.byref(ep),
             out.data_ptr() if out.numel() else None, dt,
-            out.stride(0) if out.dim() == 2 else B.outer)
+            out.stride(0))
     if workspace is None:
         _check(lib().gemm_dequant(*args, _stream(stream)), "gemm_dequant")
     else:
         _check(lib().gemm_dequant_splitk(
             *args, workspace.data_ptr() if workspace.numel() else None,
-            workspace.numel() * workspace.element_size(), _stream(stream)),
+            _nbytes(workspace), _stream(stream)),
             "gemm_dequant_splitk")
     return out
 
@@ -412,6 +461,10 @@ def flash_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
            torch.float16: DT_F16}[out_dtype]
     if out is None:
         out = torch.empty(Q.shape, dtype=out_dtype, device=Q.device)
+    if (out.dtype != out_dtype or not out.is_cuda or out.shape != Q.shape
+            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous CUDA tensor of Q's shape "
+                         "and type out_dtype")
     ptr = lambda t: t.data_ptr() if t.numel() else None  # noqa
     dt = DT_F16 if Q.dtype == torch.float16 else DT_BF16
     if workspace is None:
@@ -421,7 +474,7 @@ def flash_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
     else:
         _check(lib().flash_attention_splitkv(
             ptr(Q), ptr(K), ptr(V), ptr(out), dt, odt, BH, Lq, Lk, d,
-            float(scale), ptr(workspace), workspace.numel(), _stream(stream)),
+            float(scale), ptr(workspace), _nbytes(workspace), _stream(stream)),
             "flash_attention_splitkv")
     return out
 

@@ -492,13 +492,17 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const int c = col0 + 32 * i;
         if (split > 1) {
           // a part of a split tile: the raw fp32 accumulator to the workspace
-          // (rows and columns beyond M, N included; the reduction skips them)
-          float* wrow = ws + static_cast<int64_t>(w) * (BM * CG * BN) +
-                        static_cast<int64_t>(rank * BM + 32 * q + lane) * BN + cg_ * 128 + 32 * i;
+          // (rows beyond M are left out, columns beyond N included: the
+          // reduction reads neither)
+          if (row < M) {
+            float* wrow = ws + static_cast<int64_t>(w) * (BM * CG * BN) +
+                          static_cast<int64_t>(rank * BM + 32 * q + lane) * BN + cg_ * 128 +
+                          32 * i;
+            const bool wide = (reinterpret_cast<uintptr_t>(wrow) & 31u) == 0;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<uint4*>(wrow + 4 * v) =
-                make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+              store_32B(wrow + 8 * v, *reinterpret_cast<const uint32_t(*)[8]>(r + 8 * v), wide);
+          }
           continue;
         }
         if (epi.bias != nullptr || epi.act != ACT_NONE) apply_bias_act(r, epi, c, N);
@@ -507,7 +511,7 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             sf_word |= quantize_block_row<OUT>(r, epi, static_cast<uint8_t*>(Cptr), row, c, N)
                        << (8 * i);
         } else if (row < M) {
-          store_plain_chunk<OUT>(r, Cptr, ldc, row, c, N);
+          store_row_segment<OUT, 32>(r, Cptr, ldc, row, c, N);
         }
       }
       if ((OUT == OUT_MX8 || OUT == OUT_MX4) && split == 1)

@@ -423,14 +423,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
       if (unit >= 0) {
         // partial of a split tile: the whole fp32 accumulator row segment to
-        // the workspace (rows and columns beyond M, N included; the reduction
-        // ignores them)
-        float* wrow = ws + static_cast<int64_t>(unit) * (BM * CG * BN) +
-                      static_cast<int64_t>(rank * BM + 32 * q + lane) * BN + cg_ * EPI_COLS;
+        // the workspace (rows beyond M are left out, columns beyond N
+        // included: the reduction reads neither)
+        if (static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q + lane < M) {
+          float* wrow = ws + static_cast<int64_t>(unit) * (BM * CG * BN) +
+                        static_cast<int64_t>(rank * BM + 32 * q + lane) * BN + cg_ * EPI_COLS;
+          const bool wide = (reinterpret_cast<uintptr_t>(wrow) & 31u) == 0;
 #pragma unroll
-        for (int v = 0; v < EPI_COLS / 4; ++v)
-          *reinterpret_cast<uint4*>(wrow + 4 * v) =
-              make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          for (int v = 0; v < EPI_COLS / 8; ++v)
+            store_32B(wrow + 8 * v, *reinterpret_cast<const uint32_t(*)[8]>(r + 8 * v), wide);
+        }
         continue;
       }
       const int64_t row = static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q + lane;
@@ -440,41 +442,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         store_mx_row<OUT>(r, epi, static_cast<uint8_t*>(Cptr), row, col0, M, N);
         continue;
       }
-      if (row < M) {
-        if (OUT == OUT_BF16) {
-          uint16_t* crow = reinterpret_cast<uint16_t*>(Cptr) + row * ldc;
-#pragma unroll
-          for (int v = 0; v < EPI_COLS / 8; ++v) {    // 8 columns per vector
-            const int c = col0 + 8 * v;
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = cvt_bf16x2(__uint_as_float(r[8 * v + 2 * e]),
-                                __uint_as_float(r[8 * v + 2 * e + 1]));
-            if (c + 7 < N) {
-              *reinterpret_cast<uint4*>(crow + c) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (c + e < N) crow[c + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
-            }
-          }
-        } else {
-          float* crow = reinterpret_cast<float*>(Cptr) + row * ldc;
-#pragma unroll
-          for (int v = 0; v < EPI_COLS / 4; ++v) {    // 4 columns per vector
-            const int c = col0 + 4 * v;
-            if (c + 3 < N) {
-              *reinterpret_cast<uint4*>(crow + c) =
-                  make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (c + e < N) crow[c + e] = __uint_as_float(r[4 * v + e]);
-            }
-          }
-        }
-      }
+      if (row < M) store_row_segment<OUT, EPI_COLS>(r, Cptr, ldc, row, col0, N);
     }
   } else if (T::MX) {
     // ------------------------------------------------------------ scale copies

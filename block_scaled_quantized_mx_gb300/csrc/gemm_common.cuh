@@ -98,6 +98,18 @@ __device__ __forceinline__ void apply_bias_act(uint32_t (&r)[NC], const EpiArgs&
   }
 }
 
+// 32 bytes to p (16-byte aligned): one 256-bit store where p is 32-byte
+// aligned, else two 16-byte stores.
+__device__ __forceinline__ void store_32B(void* p, const uint32_t (&w)[8], bool wide) {
+  if (wide) {
+    st_global_v8(p, w);
+  } else {
+    uint4* q = reinterpret_cast<uint4*>(p);
+    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // Quantize one row's 32 values of C (one block: columns c .. c + 31, c < N,
 // N a multiple of 32) by the OCP rule: codes to the MX data plane (row stride
 // N codes), the block's scale code returned.
@@ -120,9 +132,8 @@ __device__ __forceinline__ uint32_t quantize_block_row(const uint32_t (&x)[32], 
       q[i] = e5 ? (cvt_e5m2x2(x0, x1) | (cvt_e5m2x2(x2, x3) << 16))
                 : (cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16));
     }
-    uint4* dst = reinterpret_cast<uint4*>(data + row * N + c);
-    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    uint8_t* dst = data + row * N + c;
+    store_32B(dst, q, (reinterpret_cast<uintptr_t>(dst) & 31u) == 0);
   } else {
     uint32_t q[4];
 #pragma unroll
@@ -169,40 +180,49 @@ __device__ __forceinline__ void store_mx_row(const uint32_t (&r)[NC], const EpiA
   store_mx_scales(sf, e, row, col0, N);
 }
 
-// One row's 32 values of a plain C (columns c .. c + 31; fp32, or bf16 RNE),
-// clipped at N.
-template <int OUT>
-__device__ __forceinline__ void store_plain_chunk(const uint32_t (&r)[32], void* C, int64_t ldc,
-                                                  int64_t row, int c, int N) {
+// One thread's segment of one row of a plain C: NV fp32 accumulator values
+// for columns c0 .. c0 + NV - 1 (c0 a multiple of 16), stored as fp32 or as
+// bf16 (RNE), clipped at N.  Each thread writes its own row, so the warp's
+// stores hit 32 different rows: 32 bytes per store fill whole L2 sectors,
+// where 16-byte stores left a stream of half-sector writes that slowed the
+// GEMMs' operand loads (measured, 8192^3 with bf16 C: MXFP4 9 %, MXFP8 2 %;
+// 16384 x 8192 x 2048 MXFP8 18 %).
+template <int OUT, int NV>
+__device__ __forceinline__ void store_row_segment(const uint32_t (&r)[NV], void* C, int64_t ldc,
+                                                  int64_t row, int c0, int N) {
   if (OUT == OUT_BF16) {
+    static_assert(NV % 16 == 0, "16 bf16 columns per store");
     uint16_t* crow = reinterpret_cast<uint16_t*>(C) + row * ldc;
+    const bool wide = (reinterpret_cast<uintptr_t>(crow) & 31u) == 0;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int cc = c + 8 * v;
-      uint32_t w[4];
+    for (int v = 0; v < NV / 16; ++v) {
+      const int c = c0 + 16 * v;
+      uint32_t w[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = cvt_bf16x2(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]));
-      if (cc + 7 < N) {
-        *reinterpret_cast<uint4*>(crow + cc) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int e = 0; e < 8; ++e)
+        w[e] = cvt_bf16x2(__uint_as_float(r[16 * v + 2 * e]),
+                          __uint_as_float(r[16 * v + 2 * e + 1]));
+      if (c + 15 < N) {
+        store_32B(crow + c, w, wide);
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (cc + e < N) crow[cc + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+        for (int e = 0; e < 16; ++e)
+          if (c + e < N) crow[c + e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
       }
     }
   } else {
+    static_assert(NV % 8 == 0, "8 fp32 columns per store");
     float* crow = reinterpret_cast<float*>(C) + row * ldc;
+    const bool wide = (reinterpret_cast<uintptr_t>(crow) & 31u) == 0;
 #pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      const int cc = c + 4 * v;
-      if (cc + 3 < N) {
-        *reinterpret_cast<uint4*>(crow + cc) =
-            make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+    for (int v = 0; v < NV / 8; ++v) {
+      const int c = c0 + 8 * v;
+      if (c + 7 < N) {
+        store_32B(crow + c, *reinterpret_cast<const uint32_t(*)[8]>(r + 8 * v), wide);
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (cc + e < N) crow[cc + e] = __uint_as_float(r[4 * v + e]);
+        for (int e = 0; e < 8; ++e)
+          if (c + e < N) crow[c + e] = __uint_as_float(r[8 * v + e]);
       }
     }
   }

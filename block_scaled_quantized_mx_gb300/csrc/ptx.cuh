@@ -267,6 +267,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// One 256-bit global store (sm_100 and later): eight 32-bit words to a
+// 32-byte aligned address, i.e. one whole L2 sector.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Spin (no suspend) until the phase with the given parity completes, within
 // the same bound as mbar_wait; for short waits on the critical path.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,

@@ -226,6 +226,33 @@ def test_host_validation_without_launch(L):
     assert L.mx_selftest_wait_timeout(0, None) == 1
 
 
+def test_binding_checks_planes_before_any_launch(L):
+    """The C ABI receives bare pointers, so the binding checks that an MX
+    tensor's planes hold the bytes its format and shape need, and raises
+    before any compute entry point is called (these tensors live on the
+    host: a call that got through would fail in the library instead)."""
+    import torch
+    good = mx.empty_mx(mx.E4M3, 256, 256, device="cpu")
+    short = mx.MXTensor(good.data[:-1], good.scales, mx.E4M3, 256, 256)
+    few_scales = mx.MXTensor(good.data, good.scales[:-16], mx.E4M3, 256, 256)
+    as_e2m1 = mx.empty_mx(mx.E2M1, 256, 256, device="cpu")
+    as_e4m3 = mx.MXTensor(as_e2m1.data, as_e2m1.scales, mx.E4M3, 256, 256)
+    strided = mx.MXTensor(torch.empty(2 * good.data.numel(), dtype=torch.uint8)[::2],
+                          good.scales, mx.E4M3, 256, 256)
+    for bad in (short, few_scales, as_e4m3, strided):
+        with pytest.raises(ValueError):
+            mx.mx_gemm(bad, good)
+        with pytest.raises(ValueError):
+            mx.mx_gemm(good, bad)
+        with pytest.raises(ValueError):
+            mx.mx_gemm_fused(bad, good)
+        with pytest.raises(ValueError):
+            mx.gemm_dequant(torch.empty(256, 256, dtype=torch.bfloat16), bad)
+    # an output MX tensor of another format than asked for
+    with pytest.raises(ValueError):
+        mx.mx_gemm_fused_quantize(good, good, mx.E2M1, out=good)
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mx, "_lib", None)
     monkeypatch.setattr(mx._build, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -85,6 +85,36 @@ def test_dequant_random_codes(fmt, a, out, M, N, K):
                 f"{a} x fmt{fmt} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("out,ld,off,split", [("bf16", 264, 8, False),
+                                              ("f32", 260, 4, False),
+                                              ("bf16", 264, 8, True)])
+def test_dequant_padded_ldc(out, ld, off, split):
+    """C inside a wider buffer whose row starts are 16- but not always
+    32-byte aligned (see test_padded_ldc in the GEMM tests); nothing outside
+    C is written, with and without the K-split."""
+    fmt = oracle.INT4
+    M, N, K = (64, 256, 4096) if split else (200, 256, 256)
+    g = torch.Generator().manual_seed(ld + off)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    cb, sb = workloads.random_codes((N, K), fmt, seed=ld, scale_lo=116,
+                                    scale_hi=127)
+    b = planes_from_codes(cb, sb, fmt)
+    ws = None
+    if split:
+        nbytes = mx.gemm_dequant_workspace_bytes(M, N, K)
+        assert nbytes > 0, "expected a split for this shape"
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    big = nan_like((M, ld), _odt(out))
+    mx.gemm_dequant(A.cuda(), b, out_dtype=_odt(out), out=big[:, off:off + N],
+                    workspace=ws)
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_a16_bmx(f16_bits(A), oracle.BF16, cb, sb, fmt)
+    check_close(big[:, off:off + N].float().cpu().numpy(), Cr, S, out,
+                f"ldc {ld} offset {off}")
+    assert torch.isnan(big[:, :off].float()).all()
+    assert torch.isnan(big[:, off + N:].float()).all()
+
+
 @pytest.mark.parametrize("fmt", [oracle.INT8, oracle.INT2, oracle.E5M2])
 def test_dequant_wide_scales_bf16(fmt):
     """bf16 A: scales across a wide range are still exact after the

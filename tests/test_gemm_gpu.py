@@ -209,16 +209,62 @@ def test_k_zero_writes_zero():
     assert torch.count_nonzero(Cf).item() == 0
 
 
-def test_padded_ldc():
+@pytest.mark.parametrize("out,ld,off", [("f32", 320, 0), ("bf16", 320, 0),
+                                        ("bf16", 264, 8), ("f32", 260, 4)])
+def test_padded_ldc(out, ld, off):
+    """C inside a wider buffer: rows `ld` elements apart, starting `off`
+    elements in.  With ld * size an odd multiple of 16 bytes, or off * size
+    = 16 bytes, row starts are 16- but not 32-byte aligned, which the
+    epilogue's 32-byte stores must detect; nothing outside C is written."""
     fmt = oracle.E4M3
     ca, sa = workloads.random_codes((256, 256), fmt, 5)
     cb, sb = workloads.random_codes((256, 256), fmt, 6)
-    big = nan_like((256, 320), torch.float32)
+    big = nan_like((256, ld), _out_dtype(out))
     mx.mx_gemm(planes_from_codes(ca, sa, fmt), planes_from_codes(cb, sb, fmt),
-               out_dtype=torch.float32, out=big[:, :256])
+               out_dtype=_out_dtype(out), out=big[:, off:off + 256])
+    assert mx.mx_last_error() == 0
     Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
-    check_close(big[:, :256].cpu().numpy(), Cr, S, "f32", "ldc 320")
-    assert torch.isnan(big[:, 256:]).all()
+    check_close(big[:, off:off + 256].float().cpu().numpy(), Cr, S, out,
+                f"ldc {ld} offset {off}")
+    assert torch.isnan(big[:, :off].float()).all()
+    assert torch.isnan(big[:, off + 256:].float()).all()
+
+
+def test_binding_rejects_bad_outputs():
+    """A caller-supplied output of the wrong dtype, shape, device or inner
+    stride, or an MX output of another format, shape or size, raises before
+    any launch (the library receives only a pointer and a row stride)."""
+    fmt = oracle.E4M3
+    a = mx.empty_mx(fmt, 256, 256)
+    b = mx.empty_mx(fmt, 256, 256)
+    A16 = torch.empty(256, 256, dtype=torch.bfloat16, device="cuda")
+    bf = torch.bfloat16
+    for bad in (torch.empty(256, 256, dtype=torch.float32, device="cuda"),
+                torch.empty(256, 255, dtype=bf, device="cuda"),
+                torch.empty(256, 512, dtype=bf, device="cuda")[:, ::2],
+                torch.empty(256, 256, dtype=bf)):
+        with pytest.raises(ValueError):
+            mx.mx_gemm(a, b, out_dtype=bf, out=bad)
+        with pytest.raises(ValueError):
+            mx.mx_gemm_fused(a, b, out_dtype=bf, out=bad)
+        with pytest.raises(ValueError):
+            mx.gemm_dequant(A16, b, out_dtype=bf, out=bad)
+    with pytest.raises(ValueError):
+        mx.gemm_f16(A16, A16, out=torch.empty(256, 128, device="cuda"))
+    src = torch.empty(256, 256, device="cuda")
+    with pytest.raises(ValueError):
+        mx.mx_quantize(src, oracle.E2M1, out=a)
+    with pytest.raises(ValueError):
+        mx.mx_quantize(torch.empty(256, 128, device="cuda"), fmt, out=a)
+    with pytest.raises(ValueError):
+        mx.mx_quantize(src, fmt, out=mx.MXTensor(a.data[:-1], a.scales, fmt,
+                                                 256, 256))
+    q = torch.empty(2, 128, 64, dtype=bf, device="cuda")
+    with pytest.raises(ValueError):
+        mx.flash_attention(q, q, q, out=torch.empty(2, 128, 32, device="cuda"))
+    with pytest.raises(ValueError):
+        mx.flash_attention(q, q, q, out_dtype=bf,
+                           out=torch.empty(2, 128, 64, device="cuda"))
 
 
 # ---------------------------------------------------------------- 16-bit path
