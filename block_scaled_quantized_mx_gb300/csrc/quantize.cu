@@ -168,9 +168,17 @@ quantize_kstrided(const float* __restrict__ src, int64_t ld, int64_t outer,
         c4[i] = codes4<FMT>(x[4 * i] * s, x[4 * i + 1] * s, x[4 * i + 2] * s, x[4 * i + 3] * s);
       constexpr int BITS = (FMT == FMT_INT2) ? 2 : (FMT == FMT_E2M1 || FMT == FMT_INT4) ? 4 : 8;
       if (BITS == 8) {
-        uint4* dst = reinterpret_cast<uint4*>(data + (n + c) * K + kb);
-        dst[0] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
-        dst[1] = make_uint4(c4[4], c4[5], c4[6], c4[7]);
+        // the lanes write 32 different rows: one 32-byte store per lane
+        // fills a whole L2 sector (the plane is 32-byte aligned unless the
+        // caller placed it otherwise)
+        uint8_t* dst = data + (n + c) * K + kb;
+        if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+          st_global_v8(dst, c4);
+        } else {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+          d4[0] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+          d4[1] = make_uint4(c4[4], c4[5], c4[6], c4[7]);
+        }
       } else if (BITS == 4) {
         *reinterpret_cast<uint4*>(data + ((n + c) * K + kb) / 2) =
             make_uint4(c4[0] | (c4[1] << 16), c4[2] | (c4[3] << 16), c4[4] | (c4[5] << 16),
