@@ -46,7 +46,10 @@ quantize_kcontig(const float* __restrict__ src, int64_t ld, int64_t outer,
                  int64_t K, uint8_t* __restrict__ data, uint8_t* __restrict__ sf) {
   constexpr int EMAX = emax_of<FMT>();
   constexpr int ROWS_PER_WARP = 16;
-  constexpr int BATCH = 8;
+  // Rows whose loads are in flight together.  Fewer registers (40 at 4, 64
+  // at 8, 80 at 16) keep more CTAs resident, which pays more than deeper
+  // batches: 8192 x 8192 E4M3 took 0.054 / 0.056 / 0.061 ms at 4 / 8 / 16.
+  constexpr int BATCH = 4;
   __shared__ __align__(16) uint8_t atom[SF_ATOM_BYTES];
 
   const int lane = threadIdx.x & 31;
