@@ -734,6 +734,48 @@ def oracle_sample(c, budget_s: float):
     return 2.0 * rows * c.N * c.K, dt, rows, oracle.num_threads()
 
 
+def oracle_extras(c, budget_s: float):
+    """Two more figures of the CPU oracle, each on a bounded sample: its
+    quantizer in GB/s of algorithmic bytes on all host cores (rows of the
+    workload's A source), and its MX GEMM in GFLOP/s on one core at
+    1024 x 1024 x 1024 (rows of C from seeded random codes)."""
+    import oracle
+    if not workloads.is_mx(c):
+        return None
+    fa, fb = workloads.formats(c)
+    per_elem = 4.0 + (0.5 if fa == oracle.E2M1 else 1.0) + 1.0 / 32
+    A, _ = workloads.sources(c)
+    An = A.numpy()
+    rows, t0 = 0, time.perf_counter()
+    while rows < c.M and time.perf_counter() - t0 < budget_s / 2:
+        oracle.quantize(An[rows:rows + 256], fa, k_axis=1)
+        rows += min(256, c.M - rows)
+    q_dt = time.perf_counter() - t0
+    q_rows = rows
+    n = 1024
+    ca, sa = workloads.random_codes((n, n), fa, seed=n + 1)
+    cb, sb = workloads.random_codes((n, n), fb, seed=n + 2)
+    oracle.set_num_threads(1)
+    try:
+        rows, t0 = 0, time.perf_counter()
+        while rows < n and time.perf_counter() - t0 < budget_s / 2:
+            oracle.gemm_mx(ca[rows:rows + 8], sa[rows:rows + 8], cb, sb, fa,
+                           fmt_b=fb)
+            rows += 8
+        g_dt = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(0)
+    return {
+        "quantize_gbs": q_rows * c.K * per_elem / q_dt / 1e9,
+        "quantize_cores": oracle.num_threads(),
+        "quantize_sample": "%d rows of the %d x %d A source, %.1f s"
+                           % (q_rows, c.M, c.K, q_dt),
+        "gemm_1core_gflops": 2.0 * rows * n * n / g_dt / 1e9,
+        "gemm_1core_sample": "%d rows of C of a %d^3 product, %.1f s"
+                             % (rows, n, g_dt),
+    }
+
+
 def run_reference(args):
     c = workloads.case(args.workload)
     budget = max(1.0, args.ref_budget / max(1, args.steps))
@@ -831,6 +873,12 @@ def main(argv=None):
             "kind": "oracle",
             "sample": "%d rows of C from the fp32 sources (all of B "
                       "quantized), %.1f s" % (rows, dt)}
+        try:
+            extra = oracle_extras(c, 4.0)
+        except Exception as e:   # a context figure: report, never lose the line
+            extra = {"error": "%s: %s" % (type(e).__name__, e)}
+        if extra is not None:
+            line.setdefault("breakdown", {})["oracle_cpu"] = extra
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()

@@ -121,6 +121,8 @@ def _load():
                                       i64, p, p]
         lib.mxo_num_threads.restype = i32
         lib.mxo_num_threads.argtypes = []
+        lib.mxo_set_num_threads.restype = None
+        lib.mxo_set_num_threads.argtypes = [i32]
         _lib = lib
         return lib
 
@@ -253,6 +255,12 @@ def attention(Q_bits, K_bits, V_bits, dtype: int, scale: float | None = None,
 
 def num_threads() -> int:
     return int(_load().mxo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's parallel loops (n <= 0: one per host core).
+    For timing only: every result is the same for any thread count."""
+    _load().mxo_set_num_threads(int(n))
 
 
 # --------------------------------------------------------------------------

@@ -563,3 +563,16 @@ int mxo_num_threads(void)
     }
     return n;
 }
+
+/* Threads for the following parallel regions (n <= 0: the OpenMP default,
+ * one per host core).  Timing control only: results do not depend on it. */
+void mxo_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    extern int omp_get_num_procs(void);
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}

@@ -766,3 +766,25 @@ def test_attention_permutation_and_rows():
     O2, _ = oracle.attention(_bits16(q), _bits16(k), _bits16(v), oracle.F16,
                              rows=[5, 0])
     assert np.array_equal(O2, O[:, [5, 0]])
+
+
+def test_results_do_not_depend_on_thread_count():
+    """The benchmark times the oracle on one core and on all cores; its
+    parallel loops split rows only, so every result is bit-identical."""
+    g = np.random.default_rng(21)
+    x = (g.standard_normal((96, 256)) * 3).astype(np.float32)
+    y = (g.standard_normal((256, 64)) * 3).astype(np.float32)
+    outs = []
+    for n in (1, 3, 0):
+        oracle.set_num_threads(n)
+        try:
+            ca, sa = oracle.quantize(x, oracle.E4M3, k_axis=1)
+            cb, sb = oracle.quantize(y, oracle.E4M3, k_axis=0)
+            C, S = oracle.gemm_mx(ca, sa, cb, sb, oracle.E4M3)
+        finally:
+            oracle.set_num_threads(0)
+        outs.append((ca, sa, cb, sb, C, S))
+    assert oracle.num_threads() >= 1
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert np.array_equal(a, b)
