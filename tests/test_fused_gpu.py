@@ -140,6 +140,34 @@ def test_fused_quantize_integers_exact(fq):
     assert np.array_equal(codes, cq)
 
 
+@pytest.mark.parametrize("fq", [oracle.E4M3, oracle.E5M2])
+def test_fused_quantize_into_16_byte_aligned_plane(fq):
+    """An output data plane that starts 16 bytes past a 32-byte boundary:
+    the epilogue's 32-byte store of each row's block falls back to two
+    16-byte stores and writes the same bytes (integer operands, so the
+    planes are exact), and nothing outside the plane."""
+    g = np.random.default_rng(37 + fq)
+    M, N, K = 256, 384, 512
+    A = torch.from_numpy(g.integers(-14, 15, (M, K)).astype(np.float32))
+    B = torch.from_numpy(g.integers(-14, 15, (K, N)).astype(np.float32))
+    a, b = mx_quantize_both(A, B, oracle.E4M3, oracle.E4M3)
+    nd, ns = mx.data_bytes(fq, M, N), mx.scale_bytes(M, N)
+    buf = torch.zeros(nd + 32, dtype=torch.uint8, device="cuda")
+    q = mx.MXTensor(buf[16:16 + nd],
+                    torch.zeros(ns, dtype=torch.uint8, device="cuda"), fq,
+                    M, N)
+    assert q.data.data_ptr() % 32 == 16
+    mx.mx_gemm_fused_quantize(a, b, fq, None, mx.ACT_NONE, out=q)
+    assert mx.mx_last_error() == 0
+    Y = A.numpy().astype(np.int64) @ B.numpy().astype(np.int64)
+    assert np.abs(Y).max() < 2 ** 24
+    cq, sq = oracle.quantize(Y.astype(np.float32), fq)
+    codes, scales = lib_quantize_to_oracle_form(q)
+    assert np.array_equal(scales, sq)
+    assert np.array_equal(codes, cq)
+    assert not buf[:16].any() and not buf[16 + nd:].any()
+
+
 @pytest.mark.parametrize("name", ["proj_up", "w4a8_8192"])
 def test_fused_workload_sampled(name):
     """Full-size workload, bias + GELU, quantized to E4M3 for the next
