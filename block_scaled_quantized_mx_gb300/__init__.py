@@ -224,6 +224,15 @@ def _check_out(out: torch.Tensor, rows: int, cols: int, dtype):
         raise ValueError("out must have a unit inner stride")
 
 
+def _out_code(dtype, allowed) -> int:
+    """The C ABI's code for an output dtype among those a call supports."""
+    if dtype not in allowed:
+        raise ValueError("out_dtype must be one of %s, not %s"
+                         % (", ".join(str(a) for a in allowed), dtype))
+    return {torch.float32: DT_F32, torch.bfloat16: DT_BF16,
+            torch.float16: DT_F16}[dtype]
+
+
 def _nbytes(t: torch.Tensor | None) -> int:
     return 0 if t is None else t.numel() * t.element_size()
 
@@ -265,7 +274,7 @@ def mx_gemm(A: MXTensor, B: MXTensor, out_dtype=torch.bfloat16,
     """C = A * B for MX tensors A (M x K) and B (quantized from K x N); the
     two may hold different element formats.  With a workspace (a CUDA tensor of at least mx_gemm_workspace_bytes()
     bytes) the K-split entry point is used."""
-    dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    dt = _out_code(out_dtype, (torch.float32, torch.bfloat16))
     _check_mx(A, "A")
     _check_mx(B, "B")
     if out is None:
@@ -334,7 +343,7 @@ def mx_gemm_fused(A: MXTensor, B: MXTensor, bias: torch.Tensor | None = None,
     """C = act(A * B + bias) with the bias and activation applied to the
     fp32 accumulator inside the GEMM epilogue."""
     _check_bias(bias, B.outer)
-    dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    dt = _out_code(out_dtype, (torch.float32, torch.bfloat16))
     _check_mx(A, "A")
     _check_mx(B, "B")
     if out is None:
@@ -414,7 +423,7 @@ def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
     if K != B.K:
         raise ValueError("inner dimensions differ")
     _check_bias(bias, B.outer)
-    dt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16}[out_dtype]
+    dt = _out_code(out_dtype, (torch.float32, torch.bfloat16))
     _check_mx(B, "B")
     if out is None:
         out = torch.empty((M, B.outer), dtype=out_dtype, device=A.device)
@@ -457,8 +466,7 @@ def flash_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
     BH = Q.numel() // max(1, Lq * d)
     if scale is None:
         scale = 1.0 / float(d) ** 0.5
-    odt = {torch.float32: DT_F32, torch.bfloat16: DT_BF16,
-           torch.float16: DT_F16}[out_dtype]
+    odt = _out_code(out_dtype, (torch.float32, torch.bfloat16, torch.float16))
     if out is None:
         out = torch.empty(Q.shape, dtype=out_dtype, device=Q.device)
     if (out.dtype != out_dtype or not out.is_cuda or out.shape != Q.shape

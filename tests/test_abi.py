@@ -251,6 +251,14 @@ def test_binding_checks_planes_before_any_launch(L):
     # an output MX tensor of another format than asked for
     with pytest.raises(ValueError):
         mx.mx_gemm_fused_quantize(good, good, mx.E2M1, out=good)
+    # an output type the call does not produce
+    for call in (lambda: mx.mx_gemm(good, good, out_dtype=torch.float16),
+                 lambda: mx.mx_gemm_fused(good, good, out_dtype=torch.int8),
+                 lambda: mx.gemm_dequant(
+                     torch.empty(256, 256, dtype=torch.bfloat16), good,
+                     out_dtype=torch.float16)):
+        with pytest.raises(ValueError):
+            call()
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
