@@ -170,6 +170,21 @@ def flops_of(c):
     return 2.0 * c.M * c.N * c.K
 
 
+def metric_name(c):
+    """The metric both arms print for a workload (identical strings, so that
+    the two lines can be divided)."""
+    return "%s GEMM TFLOP/s" % c.kind
+
+
+def step_description(c):
+    """What one step of the workload computes (both arms do this work)."""
+    if workloads.is_mx(c):
+        return ("mx_quantize(A fp32) + mx_quantize(B fp32, K-strided) + "
+                "mx_gemm(A_mx, B_mx) -> %s C; TFLOP/s = 2 M N K / step time"
+                % c.out)
+    return "gemm_f16(A, B) -> %s C; TFLOP/s = 2 M N K / step time" % c.out
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """Largest elapsed time over all ranks (every rank gets the result).
     Ranks are independent replicas of the step, so the job's time is the
@@ -596,8 +611,8 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": "%s bf16 burst x nominal %s/bf16 ratio %g" %
                 (peak_src, c.kind, NOMINAL_RATIO[c.kind])}
     line = {
-        "metric": "%s GEMM TFLOP/s (quantize A + quantize B + GEMM per step)"
-                  % c.kind if is_mx else "%s GEMM TFLOP/s" % c.kind,
+        "metric": metric_name(c),
+        "step": step_description(c),
         "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -780,12 +795,14 @@ def run_reference(args):
     c = workloads.case(args.workload)
     budget = max(1.0, args.ref_budget / max(1, args.steps))
     vals = []
+    secs = []
     last = None
     for _ in range(args.warmup if args.warmup < 1 else 1):
         oracle_sample(c, min(budget, 2.0))
     for _ in range(args.steps):
         fl, dt, rows, thr = oracle_sample(c, budget)
         vals.append(fl / dt / 1e12)
+        secs.append(dt)
         last = (rows, thr, dt)
     v = statistics.median(vals)
     rows, thr, dt = last
@@ -795,8 +812,11 @@ def run_reference(args):
         ("%d rows of C (%.1f s per step)" % (rows, dt))
     return {
         "impl": "reference",
-        "metric": "%s GEMM TFLOP/s" % c.kind, "value": v, "unit": "TFLOP/s",
+        "metric": metric_name(c), "step": step_description(c),
+        "value": v, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        # each step is a bounded sample of the workload (its rows of C)
+        "ms_per_step": statistics.mean(secs) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": c.name, "M": c.M, "N": c.N, "K": c.K,

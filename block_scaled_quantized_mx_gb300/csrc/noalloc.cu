@@ -13,6 +13,8 @@
 // The array lives as long as the process: every GPU on which this module has
 // been loaded (at the latest on the first call there) keeps its 24 MiB until
 // exit.  All calls share it.
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 #include <mutex>
 
@@ -29,23 +31,71 @@ constexpr size_t kScratchBytes = size_t{24} << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_ptr[64] = {};   // device address of g_scratch, per device ordinal
+
+// The cached device address of g_scratch, per device ordinal, with the
+// unique id (cuCtxGetId) of the context it was looked up in.  A device reset
+// or a new primary context reloads the module, possibly at another address,
+// and comes with a new id, so the address is looked up again.
+struct Slot {
+  unsigned long long ctx = 0;
+  void* ptr = nullptr;
+};
+Slot g_slot[64];
+
+// The unique id of the context current on this thread, through the driver
+// entry points; false when there is none yet (or no driver support).
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (!get_current) {
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  }
+  if (!get_id) {
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // The device address of g_scratch on the current device.  The host-side name
 // g_scratch is only a stand-in and must never reach a kernel; the address is
-// looked up once per device, with that device current, and cached.
+// looked up with the device current (cudaGetSymbolAddress) the first time a
+// context of that device calls, and cached for that context.
 mx_status scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
   if (dev < 0 || dev >= 64) return MX_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || p == nullptr) return MX_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+  unsigned long long ctx = 0;
+  const bool have_id = current_context_id(&ctx);
+  Slot& slot = g_slot[dev];
+  if (have_id && slot.ptr != nullptr && slot.ctx == ctx) {
+    *out = slot.ptr;
+    return MX_OK;
   }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess || p == nullptr) return MX_ERR_CUDA;
+  // the lookup initialises the device's context if no call had yet
+  if (have_id || current_context_id(&ctx)) {
+    slot.ctx = ctx;
+    slot.ptr = p;
+  } else {
+    slot = Slot{};   // no id to key the cache on: look up again next time
+  }
+  *out = p;
   return MX_OK;
 }
 

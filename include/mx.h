@@ -385,8 +385,10 @@ mx_status gemm_f16_splitk(const void* A, const void* B, float* C,
  * threads) race on it and give wrong results; serialize them.  Each GPU on
  * which the library's module has been loaded keeps the 24 MiB until the
  * process exits.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture on that device.
+ * address (cudaGetSymbolAddress) and caches it for the device's current
+ * context; make that first call before any stream capture on that device.
+ * After a device reset (cudaDeviceReset) the next call looks the address up
+ * again, so it too must come before any capture.
  */
 mx_status mx_gemm_splitk_noalloc(const mx_tensor* A, const mx_tensor* B, void* C,
                                  int32_t c_dtype, int64_t ldc, void* stream);

@@ -70,3 +70,22 @@ def test_reference_arm_only_on_rank_zero(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "0")
     bench.main(["--impl", "reference"])
     assert called == [1] and '"impl": "reference"' in capsys.readouterr().out
+
+
+def test_both_arms_print_the_same_metric():
+    """The driver divides our line by the reference arm's only when metric,
+    unit and direction agree; the reference line also carries ms_per_step so
+    that its timing can be checked against the run's wall clock."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    args = bench.parse_args(["--impl", "reference", "--workload", "mx256",
+                             "--steps", "2", "--warmup", "0",
+                             "--ref-budget", "2"])
+    ref = bench.run_reference(args)
+    c = workloads.case("mx256")
+    assert ref["metric"] == bench.metric_name(c)
+    assert ref["unit"] == "TFLOP/s" and ref["higher_is_better"] is True
+    assert ref["steps"] == 2 and ref["ms_per_step"] > 0
+    assert ref["step"] == bench.step_description(c)
+    assert ref["cpu_baseline"]["value"] == ref["value"]

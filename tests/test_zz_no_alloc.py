@@ -4,19 +4,21 @@ array inside the library, for callers that cannot allocate device memory
 whose memory is all reserved by a framework allocator).
 
 Called through the C ABI (ctypes), twice in a row on the same problems, its
-output must agree with mx_gemm_splitk given a workspace from the caller,
-within the tolerance the other GEMM tests use: |C - C_ref| <= 1e-4 * S, with
-S = sum_k |a_ik b_kj| from the oracle (plus one bf16 ulp for bf16 output).
+output must
+  * agree with the oracle's C element by element: |C - C_ref| <= 1e-4 * S,
+    S = sum_k |a_ik b_kj| (plus one bf16 ulp of C_ref for bf16 output), the
+    bound every GEMM test uses;
+  * equal, bit for bit, mx_gemm_splitk's output given a caller workspace:
+    the two run the same kernels with the same split and the same fixed
+    reduction order, so any difference is a fault, not rounding.
 This file is collected last on purpose."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import block_scaled_quantized_mx_gb300 as mx
 import oracle
-import workloads
 from tests._parity import check_close, nan_like
 
 pytestmark = pytest.mark.gpu
@@ -38,12 +40,13 @@ def test_noalloc_matches_workspace_entry_point(fmt, M, N, K, out):
 
     ws = torch.empty(mx.mx_gemm_workspace_bytes(fmt, M, N, K),
                      dtype=torch.uint8, device="cuda")
-    C_ref = mx.mx_gemm(a, b, out_dtype=out, workspace=ws)   # mx_gemm_splitk
+    C_ws = mx.mx_gemm(a, b, out_dtype=out, workspace=ws)   # mx_gemm_splitk
+    torch.cuda.synchronize()
     ca, sa = oracle.quantize(A.numpy(), fmt, k_axis=1)
     cb, sb = oracle.quantize(B.numpy(), fmt, k_axis=0)
-    _, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
-    ref = C_ref.float().cpu().numpy().astype(np.float64)
+    ref, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
     kind = "bf16" if out == torch.bfloat16 else "f32"
+    check_close(C_ws.float().cpu().numpy(), ref, S, kind, "workspace entry point")
 
     ta, tb = a.c(), b.c()
     dt = mx.DT_BF16 if out == torch.bfloat16 else mx.DT_F32
@@ -57,6 +60,11 @@ def test_noalloc_matches_workspace_entry_point(fmt, M, N, K, out):
         assert mx.mx_last_error() == 0
         check_close(C.float().cpu().numpy(), ref, S, kind,
                     f"no-alloc call {call}")
+        assert torch.equal(C.view(torch.int16) if out == torch.bfloat16
+                           else C.view(torch.int32),
+                           C_ws.view(torch.int16) if out == torch.bfloat16
+                           else C_ws.view(torch.int32)), \
+            f"no-alloc call {call} differs in bits from mx_gemm_splitk"
 
 
 def test_noalloc_rejects_bad_arguments():
