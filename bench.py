@@ -46,8 +46,9 @@ NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0,
                  # weight-only: B dequantized to bf16, the bf16 tensor rate
                  "w8a16": 1.0, "w4a16": 1.0, "w2a16": 1.0}
 # the per-clock rate of each kind's tcgen05.mma relative to bf16, measured on
-# GB300 with back-to-back MMAs (M = 128, N = 256): fp8 2x, every FP4 form 4x
-# (not the nominal 6x)
+# GB300 with back-to-back MMAs in the forms the kernels issue (cta_group::2,
+# M = 256, N = 256, and the 1-CTA forms): fp8 2x, every FP4 form 4x (not the
+# nominal 6x); profiles/mx_gemm_mxfp4_8192.md
 INSTRUCTION_RATIO = dict(NOMINAL_RATIO, mxfp4=4.0)
 DTYPE_NAME = {"mxfp8": "e4m3", "mxfp4": "e2m1", "mxfp8_e5m2": "e5m2",
               "w4a8": "e4m3 x e2m1"}

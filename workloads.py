@@ -10,7 +10,8 @@ per matrix, so the values do not depend on the device or on its RNG.
 Workloads (sizes and value recipes):
   mx256      MXFP8, M=N=K=256, N(0,1) sources, fp32 output
   f16        FP16 / BF16 dense, M=N=K in {1024, 2048, 4096}, U[-1, 1]
-             sources rounded to the 16-bit type, fp32 output
+             sources rounded to the 16-bit type, fp32 output (also 8192,
+             the size the MX GEMMs are profiled at)
   mxfp8      MXFP8, M=N=K in {2048, 4096, 8192}, N(0,1) with 1 % of the
              entries (Bernoulli(0.01), drawn from the same generator)
              multiplied by 100, bf16 output
@@ -78,7 +79,7 @@ def mx256() -> GemmCase:
 def f16_cases():
     out = []
     for kind in ("f16", "bf16"):
-        for n in (1024, 2048, 4096):
+        for n in (1024, 2048, 4096, 8192):
             sa, sb = _seeds(1, int(math.log2(n)))
             out.append(GemmCase(f"{kind}_{n}", kind, n, n, n, "f32",
                                 "uniform", "uniform", sa, sb))
