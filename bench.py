@@ -52,6 +52,15 @@ NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "mxfp8": 2.0, "mxfp4": 6.0,
 INSTRUCTION_RATIO = dict(NOMINAL_RATIO, mxfp4=4.0)
 DTYPE_NAME = {"mxfp8": "e4m3", "mxfp4": "e2m1", "mxfp8_e5m2": "e5m2",
               "w4a8": "e4m3 x e2m1"}
+# dense flop per clock per SM of each kind's MMA, measured on this machine's
+# GB300 (profiles/mx_gemm_mxfp4_8192.md): the clock-normalised peak is
+# SM count x this x the SM clock the work ran at
+PER_CLOCK = {k: 8192.0 * v for k, v in INSTRUCTION_RATIO.items()}
+# NVIDIA's nominal dense figures for one GB300, TFLOP/s (context)
+NOMINAL_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "mxfp8": 4500.0,
+                  "mxfp8_e5m2": 4500.0, "w4a8": 4500.0, "mxfp4": 13500.0,
+                  "w8a16": 2250.0, "w4a16": 2250.0, "w2a16": 2250.0}
+NOMINAL_HBM_GBS = 7900.0
 
 
 PROFILES = os.path.join(ROOT, "profiles")
@@ -107,19 +116,80 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 
+# NVML clock-event reason bits (nvmlClocksEventReason*)
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlClock:
+    """Query-only NVML readings of one GPU through ctypes (libnvidia-ml): the
+    SM clock, its maximum, the clock-event reasons and the power draw.
+    Nothing is set.  Raises OSError / RuntimeError when NVML is missing."""
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index),
+                                                  ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for GPU %d" % index)
+        reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = reasons or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        v = ctypes.c_uint()
+        self.max_mhz = (float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.h, 1, ctypes.byref(v)) == 0 else None)
+
+    def read(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0   # SM
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return (float(clk.value) if ok else None, pw.value / 1000.0, int(rs.value))
+
+
 class ClockSampler:
+    """SM clock, power and clock-event reasons sampled every 2 ms from a
+    thread while the timed work runs (NVML; nvidia-smi at its 100 ms
+    floor when NVML cannot be loaded)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_s: float = 0.002):
         self.index = index
+        self.period = period_s
+        self.rows = []
+        self.thread = None
         self.proc = None
         self.path = None
+        try:
+            self.nvml = NvmlClock(index)
+        except Exception:
+            self.nvml = None
 
     def start(self):
+        import threading
+        self.rows = []
+        if self.nvml is not None:
+            self.stop_flag = threading.Event()
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    try:
+                        self.rows.append(self.nvml.read())
+                    except Exception:
+                        pass
+                    time.sleep(self.period)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            time.sleep(0.01)
+            return
         try:
             import tempfile
             fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -134,6 +204,23 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            time.sleep(0.01)
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            self.thread = None
+            rows = [r for r in self.rows if r[0] is not None]
+            if not rows:
+                return None
+            sm = [r[0] for r in rows]
+            bits = 0
+            for r in rows:
+                bits |= r[2]
+            return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                    "sm_max_mhz": self.nvml.max_mhz or max(sm),
+                    "power_w_max": max(r[1] for r in rows),
+                    "samples": len(rows), "source": "NVML, 2 ms",
+                    "reasons": sorted(n for b, n in _REASONS.items() if bits & b)}
         if self.proc is None:
             return None
         time.sleep(0.15)
@@ -162,7 +249,8 @@ class ClockSampler:
         loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded),
                 "sm_max_mhz": max(r[1] for r in rows),
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "source": "nvidia-smi, 100 ms",
+                "reasons": reasons}
 
 
 # ------------------------------------------------------------------ our arm
@@ -268,6 +356,95 @@ def time_gemm_only(mx, c, dev, iters=20, flusher=None, splitk=False):
     ms = event_time(f, iters, flusher)
     assert mx.mx_last_error() == 0
     return ms, flops_of(c) / (ms * 1e-3) / 1e12
+
+
+def time_gemm_graph(mx, c, dev, min_bytes=3 * L2_BYTES, replays=5):
+    """Mean time per GEMM of a CUDA graph of back-to-back launches over R
+    distinct operand sets whose bytes together exceed L2 (so every launch
+    finds its operands outside L2), replayed between CUDA events on the
+    current stream: a stream of independent GEMMs, each launch's host cost
+    removed by the graph.  The K-split workspace is used where the library
+    asks for one.  Returns (ms per GEMM, R)."""
+    A, B = workloads.sources(c)
+    dA0, dB0 = A.to(dev), B.to(dev)
+    out_dt = torch.bfloat16 if c.out == "bf16" else torch.float32
+    if workloads.is_dequant(c):
+        fb = workloads.formats(c)[1]
+        q0 = mx.mx_quantize(dB0, fb, k_strided=True)
+        set_bytes = dA0.numel() * 2 + q0.data.numel() + q0.scales.numel()
+        nb = mx.gemm_dequant_workspace_bytes(c.M, c.N, c.K)
+    elif workloads.is_mx(c):
+        fa, fb = workloads.formats(c)
+        qa0 = mx.mx_quantize(dA0, fa)
+        qb0 = mx.mx_quantize(dB0, fb, k_strided=True)
+        set_bytes = (qa0.data.numel() + qa0.scales.numel() + qb0.data.numel() +
+                     qb0.scales.numel())
+        nb = mx.mx_gemm_workspace_bytes(ws_format(fa, fb), c.M, c.N, c.K)
+    else:
+        set_bytes = (dA0.numel() + dB0.numel()) * 2
+        nb = mx.gemm_f16_workspace_bytes(c.M, c.N, c.K)
+    set_bytes += c.M * c.N * (2 if out_dt == torch.bfloat16 else 4)
+    R = max(2, min(64, -(-min_bytes // set_bytes)))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+    calls = []
+    for i in range(R):
+        C = torch.empty((c.M, c.N), dtype=out_dt, device=dev)
+        if workloads.is_dequant(c):
+            a = dA0.clone()
+            qb = mx.MXTensor(q0.data.clone(), q0.scales.clone(), q0.fmt, q0.outer, q0.K)
+            calls.append(lambda s, a=a, qb=qb, C=C: mx.gemm_dequant(
+                a, qb, out_dtype=out_dt, out=C, workspace=ws, stream=s))
+        elif workloads.is_mx(c):
+            qa = mx.MXTensor(qa0.data.clone(), qa0.scales.clone(), qa0.fmt, qa0.outer, qa0.K)
+            qb = mx.MXTensor(qb0.data.clone(), qb0.scales.clone(), qb0.fmt, qb0.outer, qb0.K)
+            calls.append(lambda s, qa=qa, qb=qb, C=C: mx.mx_gemm(
+                qa, qb, out_dtype=out_dt, out=C, workspace=ws, stream=s))
+        else:
+            a, b = dA0.clone(), dB0.clone()
+            calls.append(lambda s, a=a, b=b, C=C: mx.gemm_f16(
+                a, b, out=C, workspace=ws, stream=s))
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for f in calls:
+            f(s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for f in calls:
+            f(s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    assert mx.mx_last_error() == 0
+    ms = e0.elapsed_time(e1) / (replays * R)
+    del g, calls
+    return ms, R
+
+
+def time_quantize_formats(mx, dA, dB, fmts, rows, K):
+    """mx_quantize throughput of other element formats on the step's fp32
+    sources (each larger than L2): GB/s of algorithmic bytes for the A
+    (K-contiguous) and B (K-strided, transposing) layouts."""
+    out = {}
+    for fmt, name in fmts:
+        qa = mx.empty_mx(fmt, rows, K, dA.device)
+        qb = mx.empty_mx(fmt, rows, K, dA.device)
+        ta = event_time(lambda: mx.mx_quantize(dA, fmt, out=qa))
+        tb = event_time(lambda: mx.mx_quantize(dB, fmt, k_strided=True, out=qb))
+        gb = quant_bytes(fmt, rows, K)
+        out[name] = {"a_ms": ta, "b_ms": tb, "a_gbs": gb / ta / 1e6,
+                     "b_gbs": gb / tb / 1e6}
+    assert mx.mx_last_error() == 0
+    return out
 
 
 def time_fused(mx, c, dev, flusher):
@@ -499,6 +676,21 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0 and fa == fb == 1:
             extra["library_reference"] = cublaslt_mx_reference(c, qa, qb, out_dt, C, mx)
 
+    window = None
+
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def clock_peak(kind, mhz):
+        return nsm * PER_CLOCK[kind] * mhz * 1e6 / 1e12 if mhz else None
+
+    clk_mhz = (clk or {}).get("sm_mhz")
+    if is_mx and rank == 0 and not args.no_quant_formats:
+        others_q = [(1, "e4m3"), (2, "e2m1"), (3, "e5m2")]
+        extra["quantize_formats"] = time_quantize_formats(mx, dA, dB, others_q, c.M, c.K)
+        for v in extra["quantize_formats"].values():
+            v["a_frac_hbm"] = v["a_gbs"] / hbm
+            v["b_frac_hbm"] = v["b_gbs"] / hbm
+
     # ---- end to end through the C ABI with host buffers
     # Every step copies its fp32 inputs from pinned host memory and its
     # result back, inside the timed region.  Steps are pipelined on three
@@ -575,9 +767,17 @@ def run_ours(args, rank, world, local_rank):
                 continue
             oc = workloads.case(name)
             ms_o, tf_o = time_gemm_only(mx, oc, dev, flusher=fl,
-                                        splitk=args.splitk)
+                                        splitk=not args.no_splitk_others)
             others[name] = {"gemm_ms": ms_o, "tflops": tf_o,
-                            "frac_of_peak": tf_o / (bf16 * NOMINAL_RATIO[oc.kind])}
+                            "frac_of_peak": tf_o / (bf16 * NOMINAL_RATIO[oc.kind]),
+                            "frac_of_nominal": tf_o / NOMINAL_TFLOPS[oc.kind]}
+            if not args.no_graph_others:
+                gms, nsets = time_gemm_graph(mx, oc, dev)
+                gtf = flops_of(oc) / (gms * 1e-3) / 1e12
+                others[name].update({
+                    "graph_ms": gms, "graph_tflops": gtf,
+                    "graph_frac_of_peak": gtf / (bf16 * NOMINAL_RATIO[oc.kind]),
+                    "graph_operand_sets": nsets})
             if INSTRUCTION_RATIO[oc.kind] != NOMINAL_RATIO[oc.kind]:
                 others[name]["frac_of_instruction_rate"] = \
                     tf_o / (bf16 * INSTRUCTION_RATIO[oc.kind])
@@ -602,6 +802,29 @@ def run_ours(args, rank, world, local_rank):
                 fused[name] = time_fused(mx, workloads.case(name), dev, fl)
         del fl
 
+    # ---- the SM clock under this load: the same step back to back for
+    # about a second with the 2 ms sampler running (the timed region itself
+    # lasts only steps x ms_per_step, a few samples)
+    if not args.no_clock_window:
+        n_win = int(min(5000, max(20, args.clock_window_s * 1e3 / ms_step)))
+        cs = ClockSampler(clocks.index)
+        w0 = torch.cuda.Event(enable_timing=True)
+        w1 = torch.cuda.Event(enable_timing=True)
+        cs.start()
+        w0.record(stream)
+        for _ in range(n_win):
+            if flusher is not None:
+                flusher()
+            step()
+        w1.record(stream)
+        w1.synchronize()
+        cw = cs.stop()
+        assert mx.mx_last_error() == 0
+        w_ms = w0.elapsed_time(w1) / n_win
+        window = {"steps": n_win, "ms_per_step": w_ms, "clocks": cw,
+                  "note": "ms_per_step includes the L2 flush" if flusher is not None
+                  else "back-to-back steps"}
+
     roofline = {"bound": "tensor", "kernel": "mx_gemm" if is_mx else "gemm_f16",
                 "achieved": gemm_tf, "peak": peak, "unit": "TFLOP/s",
                 "frac": gemm_tf / peak,
@@ -610,7 +833,20 @@ def run_ours(args, rank, world, local_rank):
                                   "per launch, ncu capture summarised in "
                                   "profiles/ (null once the kernel changed)",
                 "peak_source": "%s bf16 burst x nominal %s/bf16 ratio %g" %
-                (peak_src, c.kind, NOMINAL_RATIO[c.kind])}
+                (peak_src, c.kind, NOMINAL_RATIO[c.kind]),
+                "frac_of_nominal": gemm_tf / NOMINAL_TFLOPS[c.kind],
+                "nominal_peak": NOMINAL_TFLOPS[c.kind]}
+    if clk_mhz:
+        cp = clock_peak(c.kind, clk_mhz)
+        roofline["clock_normalised"] = {
+            "sm_mhz": clk_mhz, "peak": cp, "frac": gemm_tf / cp,
+            "peak_source": "%d SMs x %d flop/clk/SM (measured %s MMA rate) x "
+                           "median SM clock sampled in the timed region"
+                           % (nsm, PER_CLOCK[c.kind], c.kind)}
+    if window and window.get("clocks") and window["clocks"].get("sm_mhz"):
+        wm = window["clocks"]["sm_mhz"]
+        window["step_tflops"] = flops_of(c) / (window["ms_per_step"] * 1e-3) / 1e12
+        window["clock_normalised_peak"] = clock_peak(c.kind, wm)
     line = {
         "metric": metric_name(c),
         "step": step_description(c),
@@ -634,6 +870,7 @@ def run_ours(args, rank, world, local_rank):
         "attention": attention,
         "e2e": e2e,
         "clocks": clk,
+        "clock_window": window,
     }
     return line
 
@@ -862,7 +1099,18 @@ def parse_args(argv=None):
                     help="append one provenance record per measured operation "
                          "(code hash, shapes, seeds, times, clocks, environment)")
     ap.add_argument("--splitk", action="store_true",
-                    help="use the K-split GEMM entry points (with a workspace)")
+                    help="use the K-split GEMM entry points (with a workspace) "
+                         "in the step")
+    ap.add_argument("--no-splitk-others", action="store_true",
+                    help="time the other workloads without the K-split "
+                         "workspace the library asks for")
+    ap.add_argument("--no-graph-others", action="store_true",
+                    help="skip the CUDA-graph timing of the other workloads")
+    ap.add_argument("--no-clock-window", action="store_true")
+    ap.add_argument("--clock-window-s", type=float, default=1.0,
+                    help="seconds of back-to-back steps sampled for the SM clock")
+    ap.add_argument("--no-quant-formats", action="store_true",
+                    help="skip the E2M1 / E5M2 quantizer timings")
     return ap.parse_args(argv)
 
 

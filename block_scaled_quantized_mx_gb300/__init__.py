@@ -45,7 +45,7 @@ EXPORTS = ("mx_data_bytes", "mx_scale_bytes", "mx_quantize", "mx_gemm",
            "gemm_f16_workspace_bytes", "gemm_f16_splitk",
            "mx_gemm_splitk_noalloc", "mx_last_error",
            "mx_selftest_wait_timeout", "mx_scales_to_rowmajor",
-           "mx_status_string", "mx_version")
+           "mx_status_string", "mx_version", "mx_set_tile_width")
 
 
 class MXError(RuntimeError):
@@ -145,6 +145,8 @@ def lib() -> ctypes.CDLL:
     L.mx_status_string.argtypes = [i32]
     L.mx_version.restype = i32
     L.mx_version.argtypes = []
+    L.mx_set_tile_width.restype = i32
+    L.mx_set_tile_width.argtypes = [i32]
     _lib = L
     return L
 
@@ -510,3 +512,9 @@ def scales_to_rowmajor(tiled, outer: int, K: int):
     _check(lib().mx_scales_to_rowmajor(t.ctypes.data, out.ctypes.data, outer,
                                        K), "mx_scales_to_rowmajor")
     return out
+
+
+def set_tile_width(tbn: int) -> None:
+    """Fix the GEMMs' output-tile width (128 or 256) for later calls, or let
+    the library pick it per shape (0, the default)."""
+    _check(lib().mx_set_tile_width(int(tbn)), "mx_set_tile_width")

@@ -373,7 +373,13 @@ const char* mx_status_string(int32_t status) {
   }
 }
 
-int32_t mx_version(void) { return 100; }
+int32_t mx_version(void) { return 200; }
+
+mx_status mx_set_tile_width(int32_t tbn) {
+  if (tbn != 0 && tbn != 128 && tbn != 256) return MX_ERR_INVALID_ARG;
+  mxk::gemm_force_tile_width(tbn);
+  return MX_OK;
+}
 
 }  // extern "C"
 #pragma GCC visibility pop

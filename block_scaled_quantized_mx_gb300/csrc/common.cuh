@@ -105,6 +105,10 @@ size_t attention_workspace_bytes(int64_t BH, int64_t Lq, int64_t Lk, int64_t d);
 // FMT_E2M1 (both operands E2M1), or 0 for the 16-bit GEMM.
 size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K);
 
+// Tile width of the GEMMs' configuration: 0 picks it per shape, 128 or 256
+// fixes it (128 only for plain or bias/activation outputs).
+void gemm_force_tile_width(int tbn);
+
 cudaError_t launch_zero_fill(void* C, int64_t rows, int64_t cols, int64_t ldc,
                              int elem_bytes, cudaStream_t st);
 

@@ -19,15 +19,18 @@ constexpr int GROUP_M = 8;           // raster group height in M tiles
 // the form in which the epilogue stores C
 enum Out : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_MX8 = 2, OUT_MX4 = 3 };
 
-// Tiles of (BM*CG) x BN walked in groups of GROUP_M tile rows, so that the
-// clusters running at the same time share A and B tiles in L2.
+// Tiles walked in groups of `group` tile rows, column by column inside a
+// group, so that the clusters running at the same time share A and B tiles
+// in L2, and a group's rows of A stay in L2 while all of B streams past them
+// once: B is read from DRAM once per group.
 struct TileSched {
-  int num_m, num_n, total;   // in tiles of (BM*CG) x BN
+  int num_m, num_n, total;   // in tiles
+  int group = GROUP_M;       // tile rows per raster group
   __host__ __device__ __forceinline__ void tile(int t, int& mb, int& nb) const {
-    const int per_group = GROUP_M * num_n;
+    const int per_group = group * num_n;
     const int g = t / per_group;
-    const int first_m = g * GROUP_M;
-    const int gsz = min(num_m - first_m, GROUP_M);
+    const int first_m = g * group;
+    const int gsz = min(num_m - first_m, group);
     const int r = t - g * per_group;
     mb = first_m + r % gsz;
     nb = r / gsz;

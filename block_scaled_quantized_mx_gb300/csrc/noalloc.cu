@@ -118,7 +118,9 @@ mx_status mx_gemm_splitk_noalloc(const mx_tensor* A, const mx_tensor* B, void* C
   const mx_status s = scratch_on_current_device(&scratch);
   if (s != MX_OK) return s;
   // The partial tiles are written in full before they are read, within this
-  // call, so nothing in the scratch has to start at zero.
+  // call, and the split's counters count only this launch's tagged arrivals
+  // (and are left at zero by every completed launch), so nothing in the
+  // scratch has to start at zero.
   return mx_gemm_splitk(A, B, C, c_dtype, ldc, scratch, kScratchBytes, stream);
 }
 

@@ -337,15 +337,24 @@ mx_status flash_attention_splitkv(const void* Q, const void* K, const void* V, v
 /*
  * K-split variants.  When a problem's tiles leave clusters of SMs idle (a last,
  * partial wave of tiles, or fewer tiles than cluster slots), these calls
- * split the affected tiles along K across the idle clusters: each part writes
- * its fp32 partial tile into the workspace and a second kernel adds the parts
- * in a fixed order (so results do not depend on timing) and writes C.  The
+ * split the affected tiles along K across the idle clusters, inside the one
+ * GEMM launch: each part writes its fp32 partial tile into the workspace and
+ * counts itself on the tile's counter there; the part that completes the
+ * count adds all the tile's parts in part order (the same order whichever
+ * part finishes last, so results do not depend on timing) and writes C.  The
  * sum is grouped differently from the unsplit call, so the two can differ in
  * the last bits; both are within the same accumulation bound.
  *
  *   workspace        device, 16-byte aligned, caller-owned scratch of at
- *                    least *_workspace_bytes() bytes for the problem; its
- *                    contents on entry do not matter and are garbage after.
+ *                    least *_workspace_bytes() bytes for the problem: the
+ *                    partial tiles, then one 8-byte counter per split tile
+ *                    and CTA.  Its contents on entry do not matter: a counter
+ *                    word counts only arrivals tagged with this launch's
+ *                    48-bit tag (a stale word matches it with probability
+ *                    2^-48), and the completing arrival sets it to zero, so a
+ *                    call replayed from a CUDA graph (same tag) starts from
+ *                    zero too.  Two calls that share a workspace must not
+ *                    run at the same time.
  *                    NULL or a smaller size: the call runs unsplit.
  *   other arguments  as for mx_gemm / gemm_f16.
  * *_workspace_bytes returns 0 when the problem is not split (or on bad
@@ -416,6 +425,21 @@ const char* mx_status_string(int32_t status);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t mx_version(void);
+
+/* Tuning and testing knob (the pages have no counterpart): the width of the
+ * GEMMs' output tiles.  0 (the default) picks, per shape, the plan with the
+ * smallest estimated time among 256-wide tiles, 128-wide tiles and -- for the
+ * *_splitk calls -- 128-wide tiles with the K-split.  128 or 256 fixes the
+ * width for every later mx_gemm / gemm_f16 call of the process (128 only
+ * applies to fp32 / bf16 outputs: an MX-quantized C always uses 256).  The
+ * K-split runs on 128-wide tiles: with 128 fixed, the *_splitk calls split
+ * whenever the tiles leave part of a wave idle (and *_workspace_bytes sizes
+ * the workspace for that); with 256 fixed they never split.
+ * Results do not depend on the width (each element of C is summed in the
+ * same order); they depend on the K-split only in the last bits.
+ * Process-wide: set it while no other thread launches GEMMs.  Returns
+ * MX_ERR_INVALID_ARG for any other value. */
+mx_status mx_set_tile_width(int32_t tbn);
 
 #ifdef __cplusplus
 }

@@ -1,8 +1,13 @@
 """K-split GEMM entry points (mx_gemm_splitk, gemm_f16_splitk) vs the oracle.
 
+Most tests fix the tile width at 128 (the split's tiles), which makes every
+shape with a partial wave split; test_auto_plan_splits_long_k leaves the
+choice to the library.
+
 The split path applies to problems whose last wave of tiles would leave
 clusters idle: those tiles are cut along K, partials go to the workspace and
-a second kernel adds them in a fixed order.  Checked: the workspace size
+the last part of each tile to finish adds them in part order, inside the same
+launch.  Checked: the workspace size
 query, parity against the float64 oracle within the usual tolerance for
 shapes that split 2-way and 4-way (ragged edges included), run-to-run bitwise
 determinism, and that a missing or too small workspace falls back to the
@@ -24,6 +29,16 @@ pytestmark = pytest.mark.gpu
 def _built():
     mx.build()
     mx.lib()
+
+
+@pytest.fixture(autouse=True)
+def _split_tiles():
+    """The K-split runs on 128-wide tiles; fixing that width makes the split
+    calls split whenever the tiles leave part of a wave idle, so these
+    shapes exercise it whatever the library's cost model would pick."""
+    mx.set_tile_width(128)
+    yield
+    mx.set_tile_width(0)
 
 
 def _ws(nbytes):
@@ -70,7 +85,7 @@ def test_mx_splitk_small_workspace_falls_back():
 
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (4096, 4096, 1024),
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (2304, 2304, 1024),
                                    (520, 776, 2048)])
 def test_f16_splitk(dt, M, N, K):
     nbytes = mx.gemm_f16_workspace_bytes(M, N, K)
@@ -114,3 +129,54 @@ def test_workloads_splitk_sampled(name):
         Cr, S = oracle_mx_product(A, B, fa, fb, rows=rows)
     assert mx.mx_last_error() == 0
     check_close(C.float().cpu().numpy()[rows], Cr, S, c.out, name)
+
+
+def test_mx_splitk_graph_replay():
+    """A split call captured in a CUDA graph replays with the same counter
+    tag; the completing arrival of each tile returns its counter to zero, so
+    every replay reduces correctly and gives the eager call's bits."""
+    fmt, M, N, K = oracle.E4M3, 1024, 1024, 2048
+    nbytes = mx.mx_gemm_workspace_bytes(fmt, M, N, K)
+    assert nbytes > 0
+    ca, sa = workloads.random_codes((M, K), fmt, 21)
+    cb, sb = workloads.random_codes((N, K), fmt, 22)
+    a, b = planes_from_codes(ca, sa, fmt), planes_from_codes(cb, sb, fmt)
+    ws = _ws(nbytes)
+    ws.fill_(0x5A)
+    C_eager = mx.mx_gemm(a, b, out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    C = nan_like((M, N), torch.float32)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mx.mx_gemm(a, b, out_dtype=torch.float32, out=C, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.mx_gemm(a, b, out_dtype=torch.float32, out=C, workspace=ws, stream=s)
+    for _ in range(3):
+        C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert mx.mx_last_error() == 0
+        assert torch.equal(C, C_eager)
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
+    check_close(C.cpu().numpy(), Cr, S, "f32", "graph replay")
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 4096), (128, 1024, 8192)])
+def test_auto_plan_splits_long_k(fmt, M, N, K):
+    """Few tiles and a long K: the library's own plan splits."""
+    mx.set_tile_width(0)
+    nbytes = mx.mx_gemm_workspace_bytes(fmt, M, N, K)
+    assert nbytes > 0
+    ca, sa = workloads.random_codes((M, K), fmt, 31)
+    cb, sb = workloads.random_codes((N, K), fmt, 32)
+    a, b = planes_from_codes(ca, sa, fmt), planes_from_codes(cb, sb, fmt)
+    C = nan_like((M, N), torch.float32)
+    mx.mx_gemm(a, b, out_dtype=torch.float32, out=C, workspace=_ws(nbytes))
+    assert mx.mx_last_error() == 0
+    Cr, S = oracle.gemm_mx(ca, sa, cb, sb, fmt)
+    check_close(C.cpu().numpy(), Cr, S, "f32", "auto split")

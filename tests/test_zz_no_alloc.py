@@ -31,6 +31,15 @@ pytestmark = pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point(fmt, M, N, K, out):
     mx.build()
     L = mx.lib()
+    # 128-wide tiles: the split applies to every shape with a partial wave
+    mx.set_tile_width(128)
+    try:
+        _check(L, fmt, M, N, K, out)
+    finally:
+        mx.set_tile_width(0)
+
+
+def _check(L, fmt, M, N, K, out):
     assert mx.mx_gemm_workspace_bytes(fmt, M, N, K) > 0   # the split applies
     g = torch.Generator().manual_seed(M + N + K)
     A = torch.randn(M, K, generator=g)
