@@ -211,7 +211,9 @@ __device__ __forceinline__ void record_timeout(volatile int* abort, unsigned sit
 // a CUDA graph, which reuses its tag, counts from zero again.
 __device__ __forceinline__ int tagged_arrive(unsigned long long* ctr, unsigned long long tag,
                                              int target) {
-  unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  // first guess zero, what a completed launch leaves: the first arrival then
+  // takes one atomic round trip instead of a read and an atomic
+  unsigned long long v = 0ull;
   for (int i = 0; i < (1 << 16); ++i) {
     const unsigned long long cnt = ((v >> 16) == tag) ? (v & 0xFFFFull) : 0ull;
     const unsigned long long nv =
@@ -553,7 +555,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // counter.  The CTA that completes the count sums the ranges in range
         // order -- the same order whichever CTA that is, so the result does
         // not depend on timing -- and stores the tile.
-        const int part = unit % args.split;
         const int tile = unit / args.split;
         constexpr int CHUNKS = EPI_COLS / 4;
         const size_t slice = static_cast<size_t>(BM) * TBN;   // floats per partial
@@ -594,31 +595,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         __threadfence();
         const float* tile_ws = args.ws + (static_cast<size_t>(tile) * args.split * CG + rank) *
                                              slice + mine;
-        // fully unrolled: r is indexed by constants only (a runtime index
-        // would move the whole row to local memory)
+        // Every range's partial, this CTA's own included, is in the
+        // workspace: reload them in range order, each range's CHUNKS loads
+        // issued together (one L2 round trip per range), and add them in
+        // that order into r (indexed by constants only).
+        for (int p = 0; p < args.split; ++p) {
+          const float* src = tile_ws + static_cast<size_t>(p) * CG * slice;
+          float4 x[CHUNKS];
 #pragma unroll
-        for (int v = 0; v < CHUNKS; ++v) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int p = 0; p < args.split; ++p) {
-            float4 x;
-            if (p == part)
-              x = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-            else
-              x = ld_global_cg_f4(tile_ws + static_cast<size_t>(p) * CG * slice + v * 128);
+          for (int v = 0; v < CHUNKS; ++v) x[v] = ld_global_cg_f4(src + v * 128);
+#pragma unroll
+          for (int v = 0; v < CHUNKS; ++v) {
             if (p == 0) {
-              acc = x;
+              r[4 * v] = __float_as_uint(x[v].x);
+              r[4 * v + 1] = __float_as_uint(x[v].y);
+              r[4 * v + 2] = __float_as_uint(x[v].z);
+              r[4 * v + 3] = __float_as_uint(x[v].w);
             } else {
-              acc.x += x.x;
-              acc.y += x.y;
-              acc.z += x.z;
-              acc.w += x.w;
+              r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) + x[v].x);
+              r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + x[v].y);
+              r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + x[v].z);
+              r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + x[v].w);
             }
           }
-          r[4 * v] = __float_as_uint(acc.x);
-          r[4 * v + 1] = __float_as_uint(acc.y);
-          r[4 * v + 2] = __float_as_uint(acc.z);
-          r[4 * v + 3] = __float_as_uint(acc.w);
         }
       }
       const int64_t row0 = static_cast<int64_t>(mb) * BM * CG + rank * BM + 32 * q;

@@ -166,7 +166,7 @@ def test_mx_splitk_graph_replay():
 
 
 @pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E2M1])
-@pytest.mark.parametrize("M,N,K", [(256, 256, 4096), (128, 1024, 8192)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 16384), (128, 1024, 16384)])
 def test_auto_plan_splits_long_k(fmt, M, N, K):
     """Few tiles and a long K: the library's own plan splits."""
     mx.set_tile_width(0)
