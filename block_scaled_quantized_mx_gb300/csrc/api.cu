@@ -336,9 +336,12 @@ mx_status mx_last_error(void* stream) {
   cudaError_t e3 = cudaSuccess, e4 = cudaSuccess;
   const unsigned c = mxk::fetch_and_clear_status_dq(&e3);
   const unsigned d = mxk::fetch_and_clear_status_attn(&e4);
-  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess)
+  cudaError_t e5 = cudaSuccess;
+  const unsigned f = mxk::fetch_and_clear_status_dqd(&e5);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess ||
+      e5 != cudaSuccess)
     return MX_ERR_CUDA;
-  if ((a | b | c | d) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
+  if ((a | b | c | d | f) & mxk::STATUS_TIMEOUT) return MX_ERR_TIMEOUT;
   return MX_OK;
 }
 

@@ -582,6 +582,10 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
                                 void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0 || K % DQ_KPS) return cudaErrorInvalidValue;
+  // a few tokens: the weights-as-M decode kernel (dqdec.cu)
+  if (dequant_decode_applies(M, epi))
+    return launch_gemm_dequant_decode(a_dtype, A, lda, fmt_b, b_data, b_sf, C, c_dtype, ldc, M,
+                                      N, K, epi, ws, ws_bytes, st);
   DqPlan plan = dq_plan(M, N, K, ws != nullptr && epi.q_fmt == 0);
   if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = DqPlan{1, 0};
   float* w = static_cast<float*>(ws);
@@ -628,6 +632,7 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
 
 size_t dequant_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || K % DQ_KPS) return 0;
+  if (dequant_decode_applies(M, Epilogue{})) return dequant_decode_workspace_bytes(M, N, K);
   return dq_plan(M, N, K, true).ws_bytes;
 }
 
