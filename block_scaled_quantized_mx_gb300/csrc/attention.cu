@@ -485,6 +485,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   }
 
+  __syncwarp();   // reconverge before the aligned barrier (one-lane roles)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

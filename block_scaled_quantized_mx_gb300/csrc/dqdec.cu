@@ -22,16 +22,17 @@
 //     64 K, raw bytes), its scale atom and the tokens' 64-K slice (NT rows,
 //     128-byte swizzle) into a ring as deep as shared memory allows (up to 16
 //     stages: 64 KB of int4 codes in flight per SM);
-//   * warps 2..5: dequantizers, one per TMEM lane quarter, one weight row per
-//     thread, both 32-element blocks of it per chunk: codes x scale -> 16-bit
-//     values written straight into tensor memory (tcgen05.st) in one of four
-//     slots, never through shared memory;
+//   * warps 2..: dequantizers, in groups of four (one warp per TMEM lane
+//     quarter) that take the chunks in turn, one weight row per thread, both
+//     32-element blocks of it per chunk: codes x scale -> 16-bit values
+//     written straight into tensor memory (tcgen05.st) in one of four slots
+//     per group, never through shared memory;
 //   * warp 1: tensor-memory allocation and the MMA loop (one elected lane
 //     issues): per chunk four kind::f16 MMAs, M = 128 weight rows, N = NT
 //     tokens, K = 16, A read from the tensor-memory slot, B (the tokens) from
 //     shared memory; per range of a weight block, a commit of the accumulator
 //     (two buffers, alternating) to the epilogue;
-//   * warps 6..9: epilogue, one weight row per thread and 32 tokens at a
+//   * the last four warps: epilogue, one weight row per thread and 32 tokens at a
 //     time: bias and activation, C[m][n] stored for every token m (a warp's
 //     32 rows are 32 consecutive columns of C), or the range's fp32 partial
 //     to the workspace.
@@ -59,23 +60,35 @@ __device__ unsigned int g_status_dqd = 0;
 
 constexpr int WR = 128;                  // weight rows per block (MMA M)
 constexpr int KC = 64;                   // K per chunk (one ring stage)
-constexpr int A_SLOTS = 4;               // tensor-memory slots of dequantized weights
-constexpr int A_COL0 = 256;              // first slot column
+constexpr int A_COL0 = 256;              // first tensor-memory slot column
 constexpr int MAX_STAGES = 16;
-// warps 2..5: dequantizers, warps 6..9: epilogue, one per TMEM lane quarter
-// each (a warp reaches the quarter warp % 4).  Ten warps leave 3 per SM
-// sub-partition: 170 registers a thread, where 14 warps (4 on some
-// sub-partitions) capped them at 128 and spilled.
-constexpr int DQ_W0 = 2;
-constexpr int NUM_DQ = 4;
-constexpr int EPI_W0 = DQ_W0 + NUM_DQ;
+constexpr int MAX_SLOTS = 8;
+constexpr int DQ_W0 = 2;                 // first dequantizer warp
 constexpr int NUM_EPI = 4;
-constexpr int THREADS = 32 * (EPI_W0 + NUM_EPI);   // 320
 constexpr int SMEM_BUDGET = 200 * 1024;  // ring bytes
 
-// barriers: full[16], empty[16], a_ready[4], a_free[4], acc_full[2],
+// Warp layout per token width NT.  Dequantizers come in groups of four
+// warps, one per TMEM lane quarter (a warp reaches the quarter warp % 4);
+// with two groups they take the chunks in turn, which hides one chunk's
+// conversion and tensor-memory store behind the other's (the chain of one
+// group set the pace: one chunk per ~0.45 us).  Then four epilogue warps.
+// Two groups make 14 warps, so 128 registers a thread (a sub-partition
+// holds 4 warps): enough for NT = 64; NT = 128, whose epilogue needs more,
+// keeps one group (10 warps, 3 per sub-partition, 170 registers).
+template <int NT>
+struct Lay {
+  static constexpr int DQG = (NT == 64) ? 2 : 1;
+  static constexpr int NUM_DQ = 4 * DQG;
+  static constexpr int A_SLOTS = 4 * DQG;   // tensor-memory slots of dequantized weights
+  static constexpr int EPI_W0 = DQ_W0 + NUM_DQ;
+  static constexpr int THREADS = 32 * (EPI_W0 + NUM_EPI);
+  static_assert(A_SLOTS <= MAX_SLOTS, "slot barriers");
+  static_assert(2 * NT <= A_COL0 && A_COL0 + 32 * A_SLOTS <= 512, "tensor-memory columns");
+};
+
+// barriers: full[16], empty[16], a_ready[8], a_free[8], acc_full[2],
 // acc_empty[2], part_written, decided
-constexpr int NBAR = 2 * MAX_STAGES + 2 * A_SLOTS + 4 + 2;
+constexpr int NBAR = 2 * MAX_STAGES + 2 * MAX_SLOTS + 4 + 2;
 
 struct DecArgs {
   void* C;
@@ -148,12 +161,13 @@ __device__ __forceinline__ uint32_t idesc_dec(bool bf16) {
 
 // One dequantizer warp's part of every chunk of this CTA: weight row
 // 32 q + lane, both 32-element blocks of the chunk.
-template <int FMT>
+template <int FMT, int DQG>
 __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Ranges& rg, int c,
                                              uint32_t base, uint32_t tmem_base, uint32_t bar_full,
                                              uint32_t bar_empty, uint32_t bar_a_ready,
-                                             uint32_t bar_a_free, int q, int lane,
+                                             uint32_t bar_a_free, int q, int g, int lane,
                                              volatile int* abort) {
+  constexpr int A_SLOTS = 4 * DQG;
   const int row = 32 * q + lane;
   const bool bf16 = a.a_bf16 != 0;
   constexpr int BB = block_code_bytes<FMT>();
@@ -163,9 +177,18 @@ __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Ranges& rg,
   int kc = u0 % rg.kch, s = 0;
   uint32_t ph = 0, ci = 0;
   for (int u = u0; u < u1; ++u, ++ci) {
+    // this group's chunks only (the counters advance over every chunk)
+    if (DQG > 1 && static_cast<int>(ci % DQG) != g) {
+      if (++kc == rg.kch) kc = 0;
+      if (++s == a.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+      continue;
+    }
     const int slot = static_cast<int>(ci & (A_SLOTS - 1));
     const uint32_t sph = (ci / A_SLOTS) & 1u;
-    if (!mbar_wait(bar_full + 8 * s, ph, abort)) {
+    if (!mbar_wait_short(bar_full + 8 * s, ph, abort)) {
       dqd_timeout(abort, 21);
       return;
     }
@@ -184,7 +207,7 @@ __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Ranges& rg,
     dq_block_regs<FMT>(w1, sc1, bf16, o1);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);   // codes and scales consumed
-    if (!mbar_wait(bar_a_free + 8 * slot, sph ^ 1u, abort)) {
+    if (!mbar_wait_short(bar_a_free + 8 * slot, sph ^ 1u, abort)) {
       dqd_timeout(abort, 22);
       return;
     }
@@ -239,7 +262,7 @@ __device__ __forceinline__ void dec_store(const float (&v)[32], void* C, int64_t
 }
 
 template <int NT, int OUT>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Lay<NT>::THREADS, 1)
 dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
              const __grid_constant__ CUtensorMap tmSF, const DecArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -250,8 +273,11 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
   const uint32_t bar_full = bars;
   const uint32_t bar_empty = bar_full + 8 * MAX_STAGES;
   const uint32_t bar_a_ready = bar_empty + 8 * MAX_STAGES;
-  const uint32_t bar_a_free = bar_a_ready + 8 * A_SLOTS;
-  const uint32_t bar_acc_full = bar_a_free + 8 * A_SLOTS;
+  using LY = Lay<NT>;
+  constexpr int A_SLOTS = LY::A_SLOTS;
+  constexpr int EPI_W0 = LY::EPI_W0;
+  const uint32_t bar_a_free = bar_a_ready + 8 * MAX_SLOTS;
+  const uint32_t bar_acc_full = bar_a_free + 8 * MAX_SLOTS;
   const uint32_t bar_acc_empty = bar_acc_full + 16;
   const uint32_t bar_written = bar_acc_empty + 16;
   const uint32_t bar_decided = bar_written + 8;
@@ -274,11 +300,12 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
   if (warp == 0) {
     for (int i = lane; i < NBAR; i += 32) {
       uint32_t count = 1;
-      if (i >= MAX_STAGES && i < 2 * MAX_STAGES) count = 1 + NUM_DQ;          // empty
-      else if (i >= 2 * MAX_STAGES && i < 2 * MAX_STAGES + A_SLOTS) count = NUM_DQ;   // a_ready
-      else if (i >= 2 * MAX_STAGES + 2 * A_SLOTS + 2 &&
-               i < 2 * MAX_STAGES + 2 * A_SLOTS + 4) count = NUM_EPI;         // acc_empty
-      else if (i == 2 * MAX_STAGES + 2 * A_SLOTS + 4) count = NUM_EPI;        // written
+      // one group of four dequantizer warps handles each chunk
+      if (i >= MAX_STAGES && i < 2 * MAX_STAGES) count = 1 + 4;               // empty
+      else if (i >= 2 * MAX_STAGES && i < 2 * MAX_STAGES + MAX_SLOTS) count = 4;  // a_ready
+      else if (i >= 2 * MAX_STAGES + 2 * MAX_SLOTS + 2 &&
+               i < 2 * MAX_STAGES + 2 * MAX_SLOTS + 4) count = NUM_EPI;       // acc_empty
+      else if (i == 2 * MAX_STAGES + 2 * MAX_SLOTS + 4) count = NUM_EPI;      // written
       mbar_init(bar_full + 8 * i, count);
     }
     fence_mbar_init();
@@ -345,8 +372,10 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
       for (; u < seg_end; ++u, ++ci) {
         const int slot = static_cast<int>(ci & (A_SLOTS - 1));
         const uint32_t sph = (ci / A_SLOTS) & 1u;
-        if (!mbar_wait(bar_a_ready + 8 * slot, sph, abort) ||
-            !mbar_wait(bar_full + 8 * s, ph, abort)) {
+        // the MMA warp's waits are on the critical path and usually find
+        // the slot not yet written: spin rather than sleep through a wake-up
+        if (!mbar_wait_spin(bar_a_ready + 8 * slot, sph, abort) ||
+            !mbar_wait_spin(bar_full + 8 * s, ph, abort)) {
           dqd_timeout(abort, 24);
           ok = false;
           break;
@@ -374,31 +403,31 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     }
   } else if (warp >= DQ_W0 && warp < EPI_W0) {
     // ------------------------------------------------------------ dequantizers
-    const int q = warp & 3;
+    const int q = warp & 3, g = (warp - DQ_W0) >> 2;
     switch (a.fmt) {
       case FMT_INT4:
-        dequant_loop<FMT_INT4>(a, rg, c, base, tmem_base, bar_full, bar_empty, bar_a_ready,
-                               bar_a_free, q, lane, abort);
+        dequant_loop<FMT_INT4, LY::DQG>(a, rg, c, base, tmem_base, bar_full, bar_empty,
+                               bar_a_ready, bar_a_free, q, g, lane, abort);
         break;
       case FMT_INT8:
-        dequant_loop<FMT_INT8>(a, rg, c, base, tmem_base, bar_full, bar_empty, bar_a_ready,
-                               bar_a_free, q, lane, abort);
+        dequant_loop<FMT_INT8, LY::DQG>(a, rg, c, base, tmem_base, bar_full, bar_empty,
+                               bar_a_ready, bar_a_free, q, g, lane, abort);
         break;
       case FMT_INT2:
-        dequant_loop<FMT_INT2>(a, rg, c, base, tmem_base, bar_full, bar_empty, bar_a_ready,
-                               bar_a_free, q, lane, abort);
+        dequant_loop<FMT_INT2, LY::DQG>(a, rg, c, base, tmem_base, bar_full, bar_empty,
+                               bar_a_ready, bar_a_free, q, g, lane, abort);
         break;
       case FMT_E2M1:
-        dequant_loop<FMT_E2M1>(a, rg, c, base, tmem_base, bar_full, bar_empty, bar_a_ready,
-                               bar_a_free, q, lane, abort);
+        dequant_loop<FMT_E2M1, LY::DQG>(a, rg, c, base, tmem_base, bar_full, bar_empty,
+                               bar_a_ready, bar_a_free, q, g, lane, abort);
         break;
       case FMT_E5M2:
-        dequant_loop<FMT_E5M2>(a, rg, c, base, tmem_base, bar_full, bar_empty, bar_a_ready,
-                               bar_a_free, q, lane, abort);
+        dequant_loop<FMT_E5M2, LY::DQG>(a, rg, c, base, tmem_base, bar_full, bar_empty,
+                               bar_a_ready, bar_a_free, q, g, lane, abort);
         break;
       default:
-        dequant_loop<FMT_E4M3>(a, rg, c, base, tmem_base, bar_full, bar_empty, bar_a_ready,
-                               bar_a_free, q, lane, abort);
+        dequant_loop<FMT_E4M3, LY::DQG>(a, rg, c, base, tmem_base, bar_full, bar_empty,
+                               bar_a_ready, bar_a_free, q, g, lane, abort);
         break;
     }
   } else if (warp >= EPI_W0) {
@@ -520,6 +549,7 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     }
   }
 
+  __syncwarp();   // reconverge before the aligned barrier (one-lane roles)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -582,7 +612,7 @@ cudaError_t dqd_run(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensor
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_smem[dev] = smem;
   }
-  kern<<<grid, THREADS, smem, st>>>(tx, tw, tsf, a);
+  kern<<<grid, Lay<NT>::THREADS, smem, st>>>(tx, tw, tsf, a);
   return cudaGetLastError();
 }
 

@@ -434,6 +434,7 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
   }
 
+  __syncwarp();   // reconverge before the aligned barrier (one-lane roles)
   tc_fence_before();
   if (CG == 2)
     cluster_sync();

@@ -682,6 +682,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   }
 
+  // Reconverge the warp first: some roles ran on one lane (the producer),
+  // and an aligned block or cluster barrier reached by a diverged warp is
+  // undefined -- it was seen to release before the other warps arrived.
+  __syncwarp();
   tc_fence_before();
   if (CG == 2)
     cluster_sync();   // no CTA of the pair retires while the other may use it

@@ -23,9 +23,10 @@
 
 namespace {
 
-// 24 MiB.  The split never needs more than one fp32 tile of 256 x 256 per
-// cluster of two SMs (76 x 256 KiB ~ 19 MiB on a 152-SM GB300); a problem
-// that would need more is rejected with MX_ERR_SHAPE.
+// 24 MiB.  The split never needs more than one fp32 partial of 256 x 128
+// per cluster of two SMs, plus its counters (76 x 128 KiB ~ 10 MiB on a
+// 152-SM GB300); a problem that would need more is rejected with
+// MX_ERR_SHAPE.
 constexpr size_t kScratchBytes = size_t{24} << 20;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];

@@ -104,6 +104,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Wait like mbar_wait, but suspended at most `hint_ns` at a time: for waits
+// that often find the phase incomplete and sit on a critical path, where a
+// long suspension would add its wake-up delay to every step.
+__device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity,
+                                                volatile int* abort, uint32_t hint_ns = 256u) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > MXK_WAIT_LIMIT_CYCLES) return false;
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {

@@ -387,7 +387,7 @@ mx_status gemm_f16_splitk(const void* A, const void* B, float* C,
  *   A, B, C, c_dtype, ldc, stream   as for mx_gemm.
  * Returns MX_ERR_SHAPE when the problem's split would need more than the
  * 24 MiB (mx_gemm_workspace_bytes() > 24 MiB; not reachable on a 152-SM
- * GB300, where the split needs at most about 19 MiB).
+ * GB300, where the split needs at most about 10 MiB).
  *
  * The array is shared by every call in the process: two calls whose
  * executions overlap on the GPU (different streams, or different host
