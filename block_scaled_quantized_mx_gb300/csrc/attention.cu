@@ -197,6 +197,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     prefetch_tmap(&tmV);
   }
   if (warp == 1) tmem_alloc_cg<1>(smem_u32(tmem_slot), AT_TMEM_COLS);
+  __syncwarp();   // reconverge before the aligned barrier (one-lane setup)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -92,16 +92,14 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
 size_t dequant_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 // The decode-shaped dequantizing GEMM (dqdec.cu): M <= 128 tokens, a plain or
-// bias / activation output; K a multiple of 64.  With a workspace of at
-// least dequant_decode_workspace_bytes the weight blocks' K ranges are
-// spread over every SM, else each CTA takes whole 128-row weight blocks.
+// bias / activation output; K a multiple of 64.  Its K split stays inside
+// thread-block clusters: no workspace (dequant_decode_workspace_bytes is 0).
 bool dequant_decode_applies(int64_t M, const Epilogue& epi);
 size_t dequant_decode_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_dequant_decode(int a_dtype, const void* A, int64_t lda, int fmt_b,
                                        const void* b_data, const uint8_t* b_sf, void* C,
                                        int c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K,
-                                       const Epilogue& epi, void* ws, size_t ws_bytes,
-                                       cudaStream_t st);
+                                       const Epilogue& epi, cudaStream_t st);
 unsigned fetch_and_clear_status_dqd(cudaError_t* err);
 
 // O = softmax(Q K^T * scale) V for BH heads: Q BH x Lq x d, K and V

@@ -190,6 +190,7 @@ dqgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     prefetch_tmap(&tmSF);
   }
   if (warp == 1) tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS_DQ);
+  __syncwarp();   // reconverge before the aligned barrier (one-lane setup)
   tc_fence_before();
   if (CG == 2)
     cluster_sync();
@@ -586,7 +587,7 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
   // a few tokens: the weights-as-M decode kernel (dqdec.cu)
   if (dequant_decode_applies(M, epi))
     return launch_gemm_dequant_decode(a_dtype, A, lda, fmt_b, b_data, b_sf, C, c_dtype, ldc, M,
-                                      N, K, epi, ws, ws_bytes, st);
+                                      N, K, epi, st);
   DqPlan plan = dq_plan(M, N, K, ws != nullptr && epi.q_fmt == 0);
   if (plan.split > 1 && ws_bytes < plan.ws_bytes) plan = DqPlan{1, 0};
   float* w = static_cast<float*>(ws);

@@ -344,6 +344,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (T::MX && lane == 4) prefetch_tmap(&tmSFB);
   }
   if (warp == 1) tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
+  __syncwarp();   // reconverge before the aligned barrier (lane-dependent setup)
   tc_fence_before();
   if (CG == 2)
     cluster_sync();   // peers' barriers are initialised before any remote use

@@ -253,7 +253,12 @@ mx_status gemm_f16_fused(const void* A, const void* B, const mx_epilogue* epi,
  * threadgroup memory and multiplied.  Here the CTA pair dequantizes B's codes
  * and scales into shared memory as a_dtype values and runs the 16-bit tensor
  * cores; weight-only quantization (int4 / int2 / E2M1 weights, 16-bit
- * activations) is the intended use.
+ * activations) is the intended use.  Up to 128 rows of A (decoding a few
+ * tokens) a second kernel takes the product: B's 128-row blocks are the MMA's
+ * rows, dequantized into tensor memory 256 K at a time, A's rows its columns;
+ * when the blocks are fewer than the SMs, each block's K range is split over
+ * a thread-block cluster of up to 8 CTAs whose partial sums are added in a
+ * fixed order on chip (no workspace, same bits every run).
  *
  *   A        device, M x K, row-major, element type a_dtype (MX_DT_F16 or
  *            MX_DT_BF16); lda >= K, a multiple of 8; 16-byte aligned
@@ -269,13 +274,14 @@ mx_status gemm_dequant(const void* A, int32_t a_dtype, int64_t M, int64_t lda,
                        const mx_tensor* B, const mx_epilogue* epi, void* C,
                        int32_t c_dtype, int64_t ldc, void* stream);
 
-/* gemm_dequant with a K-split: when the output tiles leave SMs idle (a few
- * rows of A, as in decoding one token at a time), each tile's K range is
- * split into parts that run on those SMs, each writing an fp32 partial tile
- * to the workspace; a second kernel adds the parts in a fixed order, applies
- * the epilogue and writes C.  workspace: device, 16-byte aligned, at least
- * gemm_dequant_workspace_bytes(M, N, K) bytes (0: the problem is not split;
- * NULL or smaller: the call runs unsplit). */
+/* gemm_dequant with a K-split: when the output tiles leave SMs idle (more
+ * than 128 rows of A but few tiles), each tile's K range is split into parts
+ * that run on those SMs, each writing an fp32 partial tile to the
+ * workspace; a second kernel adds the parts in a fixed order, applies the
+ * epilogue and writes C.  workspace: device, 16-byte aligned, at least
+ * gemm_dequant_workspace_bytes(M, N, K) bytes (0: the problem is not split
+ * this way -- always so for M <= 128, whose kernel splits K inside clusters
+ * and ignores the workspace; NULL or smaller: the call runs unsplit). */
 size_t gemm_dequant_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mx_status gemm_dequant_splitk(const void* A, int32_t a_dtype, int64_t M,
                               int64_t lda, const mx_tensor* B,

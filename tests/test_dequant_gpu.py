@@ -93,7 +93,7 @@ def test_dequant_padded_ldc(out, ld, off, split):
     32-byte aligned (see test_padded_ldc in the GEMM tests); nothing outside
     C is written, with and without the K-split."""
     fmt = oracle.INT4
-    M, N, K = (64, 256, 4096) if split else (200, 256, 256)
+    M, N, K = (200, 256, 4096) if split else (200, 256, 256)
     g = torch.Generator().manual_seed(ld + off)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     cb, sb = workloads.random_codes((N, K), fmt, seed=ld, scale_lo=116,
@@ -207,16 +207,22 @@ def test_dequant_deterministic():
                                    (64, 2048, 2048), (128, 512, 4096),
                                    (200, 768, 4096)])
 def test_dequant_splitk(fmt, out, M, N, K):
-    """Decode-like shapes: few output tiles, K split over the idle SMs; the
-    parts are summed in a fixed order by the reduction kernel."""
+    """Decode-like shapes: few output tiles, K split over the idle SMs.  Over
+    128 tokens the parts go to the workspace and are summed in a fixed order
+    by the reduction kernel; up to 128 tokens the decode kernel splits each
+    weight block's K range inside a thread-block cluster and needs no
+    workspace.  Either way a repeat gives the same bits."""
     g = torch.Generator().manual_seed(M + N + K + fmt)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     cb, sb = workloads.random_codes((N, K), fmt, seed=N + fmt, scale_lo=116,
                                     scale_hi=127)
     b = planes_from_codes(cb, sb, fmt)
     nbytes = mx.gemm_dequant_workspace_bytes(M, N, K)
-    assert nbytes > 0, "expected a split for this shape"
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if M > 128:
+        assert nbytes > 0, "expected a split for this shape"
+    else:
+        assert nbytes == 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
     C = nan_like((M, N), _odt(out))
     mx.gemm_dequant(A.cuda(), b, out_dtype=_odt(out), out=C, workspace=ws)
     assert mx.mx_last_error() == 0
@@ -227,7 +233,7 @@ def test_dequant_splitk(fmt, out, M, N, K):
 
 
 def test_dequant_splitk_fused_epilogue():
-    M, N, K = 32, 1024, 4096
+    M, N, K = 200, 1024, 4096
     g = torch.Generator().manual_seed(44)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     W = torch.randn(K, N, generator=g) * 0.02
@@ -245,5 +251,7 @@ def test_dequant_splitk_fused_epilogue():
 
 def test_dequant_workspace_only_for_idle_sms():
     assert mx.gemm_dequant_workspace_bytes(8192, 8192, 8192) == 0
-    assert mx.gemm_dequant_workspace_bytes(64, 8192, 8192) > 0
-    assert mx.gemm_dequant_workspace_bytes(64, 8192, 100) == 0      # K % 64
+    assert mx.gemm_dequant_workspace_bytes(200, 768, 4096) > 0
+    assert mx.gemm_dequant_workspace_bytes(200, 768, 100) == 0      # K % 64
+    # up to 128 tokens: the decode kernel splits K inside clusters
+    assert mx.gemm_dequant_workspace_bytes(64, 8192, 8192) == 0
