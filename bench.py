@@ -65,8 +65,8 @@ NOMINAL_HBM_GBS = 7900.0
 
 PROFILES = os.path.join(ROOT, "profiles")
 GEMM_SOURCES = [os.path.join(ROOT, "block_scaled_quantized_mx_gb300", "csrc", f)
-                for f in ("gemm.cu", "gemm_common.cuh", "mx_rule.cuh", "ptx.cuh",
-                          "common.cuh")]
+                for f in ("gemm.cu", "gemm_kernel.cuh", "gemm_mxf8.cu", "gemm_common.cuh",
+                          "mx_rule.cuh", "ptx.cuh", "common.cuh")]
 
 
 def gemm_source_hash() -> str:
