@@ -684,8 +684,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   }
 
   // Reconverge the warp first: some roles ran on one lane (the producer),
-  // and an aligned block or cluster barrier reached by a diverged warp is
-  // undefined -- it was seen to release before the other warps arrived.
+  // and an aligned block or cluster barrier must be reached by every lane of
+  // a warp together.
   __syncwarp();
   tc_fence_before();
   if (CG == 2)
