@@ -124,6 +124,40 @@ __device__ __forceinline__ void commit_elect(uint32_t bar) {
       : "memory");
 }
 
+// Packed fp32 pairs (sm_100 and later): one instruction does two fp32
+// operations, each rounded as the scalar one is, so results are the same
+// per element and the softmax issues half as many instructions for them.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// three-input maximum / minimum (sm_100 and later): two comparisons in one
+// instruction, NaN inputs ignored as fmaxf / fminf ignore them
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two probabilities -> a packed pair of the operand type.
 __device__ __forceinline__ uint32_t pack_p(float a, float b, bool bf16) {
   return bf16 ? cvt_bf16x2(a, b) : cvt_f16x2(a, b);
@@ -360,12 +394,16 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         s_eff = scale_log2e;
         if (scale_log2e >= 0.0f) {
 #pragma unroll
-          for (int e = 0; e < AT_BK; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e]));
+          for (int e = 0; e < AT_BK; e += 2)
+            mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], __uint_as_float(sv[e]),
+                                      __uint_as_float(sv[e + 1]));
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx8[i] = INFINITY;
 #pragma unroll
-          for (int e = 0; e < AT_BK; ++e) mx8[e & 7] = fminf(mx8[e & 7], __uint_as_float(sv[e]));
+          for (int e = 0; e < AT_BK; e += 2)
+            mx8[(e >> 1) & 7] = min3f(mx8[(e >> 1) & 7], __uint_as_float(sv[e]),
+                                      __uint_as_float(sv[e + 1]));
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] *= scale_log2e;
@@ -402,23 +440,31 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // p = 2^(x - m), rounded to the operand type, written back as packed P
       // over the scores (already in registers): chunk c of P is columns
       // 16 c .. 16 c + 15; keys beyond Lk have x = -inf, p = 0
-      float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // pairs of scores: x = s s_eff - m and the running sums as packed fp32
+      const uint64_t se2 = f2_pack(s_eff, s_eff), nm2 = f2_pack(-m_new, -m_new);
+      uint64_t sum2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
       for (int c = 0; c < AT_BK / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float x0 = fmaf(__uint_as_float(sv[32 * c + 2 * e]), s_eff, -m_new);
-          const float x1 = fmaf(__uint_as_float(sv[32 * c + 2 * e + 1]), s_eff, -m_new);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[32 * c + 2 * e]),
+                                   __uint_as_float(sv[32 * c + 2 * e + 1])),
+                           se2, nm2),
+                    x0, x1);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
           pk[e] = pack_p(p0, p1, BF);
-          sum4[e & 3] += p0 + p1;
+          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
         }
         tmem_st_32x32b_x16(lane_addr + 16 * c, pk);
       }
       tmem_wait_st();
-      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      float s0, s1, s2, s3;
+      f2_unpack(sum2[0], s0, s1);
+      f2_unpack(sum2[1], s2, s3);
+      l = l * alpha + ((s0 + s2) + (s1 + s3));
       m = m_new;
       tc_fence_before();
       __syncwarp();
