@@ -78,8 +78,9 @@ struct AtSmem {
   static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr int V_OFF = K_OFF + 2 * K_BYTES;
   static constexpr int BAR_OFF = V_OFF + 2 * V_BYTES;
-  // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full[2], o_done[2]
-  static constexpr int MISC_OFF = BAR_OFF + 15 * 8;
+  // q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2],
+  // p_full[2 tiles][2 halves], o_done[2]
+  static constexpr int MISC_OFF = BAR_OFF + 17 * 8;
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -192,8 +193,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t bar_k_empty = bar_v + 16;     // [2] ring stage
   const uint32_t bar_v_empty = bar_k_empty + 16;   // [2] ring stage
   const uint32_t bar_s_full = bar_v_empty + 16;    // [2] tile
-  const uint32_t bar_p_full = bar_s_full + 16;     // [2] tile
-  const uint32_t bar_o_done = bar_p_full + 16;     // [2] tile
+  const uint32_t bar_p_full = bar_s_full + 16;     // [2] tile x [2] half of the keys
+  const uint32_t bar_o_done = bar_p_full + 32;     // [2] tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::MISC_OFF);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 4);
 
@@ -221,7 +222,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(bar_k_empty + 8 * i, 1);
       mbar_init(bar_v_empty + 8 * i, 1);
       mbar_init(bar_s_full + 8 * i, 1);
-      mbar_init(bar_p_full + 8 * i, 4);
+      mbar_init(bar_p_full + 16 * i, 4);
+      mbar_init(bar_p_full + 16 * i + 8, 4);
       mbar_init(bar_o_done + 8 * i, 1);
     }
     *abort = 0;
@@ -313,7 +315,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if (j >= 1) {
             // O_t += P_t,{j-1} V_{j-1}, P read from tensor memory
             const int jj = j - 1, st = jj & 1;
-            if (!mbar_wait(bar_p_full + 8 * t, jj & 1, abort) ||
+            // P arrives in two halves of 64 keys: the product with the first
+            // half runs while the softmax warps compute the second
+            if (!mbar_wait(bar_p_full + 16 * t, jj & 1, abort) ||
                 !mbar_wait(bar_v + 8 * st, (jj >> 1) & 1u, abort)) {
               at_timeout(abort, 0x34);
               ok = false;
@@ -322,11 +326,20 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < AT_BK / 16; ++kk) {
+              if (kk == AT_BK / 32) {
+                if (!mbar_wait(bar_p_full + 16 * t + 8, jj & 1, abort)) {
+                  at_timeout(abort, 0x36);
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
               const uint32_t boff = (kk >> 2) * (D / 64) * 8192 + (kk & 3) * 2048;
               mma_ts_elect(o_t, s_t + 8 * kk,
                            dv0 + static_cast<uint64_t>((st * L::V_BYTES + boff) >> 4),
                            id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
             }
+            if (!ok) break;
             // both tiles' products with V_{j-1} issued: its slot frees when they end
             if (t == 1) commit_elect(bar_v_empty + 8 * st);
           }
@@ -459,16 +472,19 @@ attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
         }
         tmem_st_32x32b_x16(lane_addr + 16 * c, pk);
+        if (c == AT_BK / 64 - 1 || c == AT_BK / 32 - 1) {
+          // half of P (64 keys) written: the product with it may start
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_p_full + 16 * t + (c == AT_BK / 32 - 1 ? 8 : 0));
+        }
       }
-      tmem_wait_st();
       float s0, s1, s2, s3;
       f2_unpack(sum2[0], s0, s1);
       f2_unpack(sum2[1], s2, s3);
       l = l * alpha + ((s0 + s2) + (s1 + s3));
       m = m_new;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full + 8 * t);
     }
     if (ok) {
       if (!mbar_wait(bar_o_done + 8 * t, 0, abort)) {
