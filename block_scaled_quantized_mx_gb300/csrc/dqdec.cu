@@ -184,7 +184,7 @@ __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Work& wk,
                                              uint32_t code_base, uint32_t tmem_base,
                                              uint32_t bar_code_full, uint32_t bar_code_empty,
                                              uint32_t bar_slot_free, uint32_t bar_a_ready, int q,
-                                             int g, int lane, volatile int* abort) {
+                                             int g, int ngroups, int lane, volatile int* abort) {
   using LY = Lay<NT>;
   const int row = 32 * q + lane;
   const bool bf16 = a.a_bf16 != 0;
@@ -192,7 +192,7 @@ __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Work& wk,
   // the scale word of this row in a scale atom: blocks 0..3 of the atom
   const uint32_t sf_word = 16 * (row & 31) + 4 * ((row >> 5) & 3);
   const int nq = wk.nq();
-  for (int i = g; i < nq; i += LY::DQG) {
+  for (int i = g; i < nq; i += ngroups) {
     const int qi = wk.qa + i % wk.jq;
     const int nu = min(QU, wk.kch - QU * qi);
     const int s = i % a.cs;
@@ -258,6 +258,27 @@ __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Work& wk,
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_a_ready + 8 * slot);
   }
+}
+
+// dequant_loop for B's element format.
+template <int NT>
+__device__ __forceinline__ void dequant_any(const DecArgs& a, const Work& wk, uint32_t code_base,
+                                            uint32_t tmem_base, uint32_t bar_code_full,
+                                            uint32_t bar_code_empty, uint32_t bar_slot_free,
+                                            uint32_t bar_a_ready, int q, int g, int ngroups,
+                                            int lane, volatile int* abort) {
+#define MXK_DQD_LOOP(F)                                                                   \
+  dequant_loop<F, NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty,         \
+                      bar_slot_free, bar_a_ready, q, g, ngroups, lane, abort)
+  switch (a.fmt) {
+    case FMT_INT4: MXK_DQD_LOOP(FMT_INT4); break;
+    case FMT_INT8: MXK_DQD_LOOP(FMT_INT8); break;
+    case FMT_INT2: MXK_DQD_LOOP(FMT_INT2); break;
+    case FMT_E2M1: MXK_DQD_LOOP(FMT_E2M1); break;
+    case FMT_E5M2: MXK_DQD_LOOP(FMT_E5M2); break;
+    default: MXK_DQD_LOOP(FMT_E4M3); break;
+  }
+#undef MXK_DQD_LOOP
 }
 
 // bias + activation on 32 values of weight row n (one column of C)
@@ -344,6 +365,9 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     }
   }
   const int nq = wk.nq();
+  // dequantizer groups: the epilogue warps join as one more when this CTA
+  // has a single block (every slot then has its own group)
+  const int ngroups = (wk.n_jobs == 1) ? LY::DQG + 1 : LY::DQG;
 
   if (warp == 0) {
     constexpr int N0 = 2 * MAX_CS, N1 = N0 + 3 * MAX_SLOTS;
@@ -463,22 +487,16 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     }
   } else if (warp < EPI_W0) {
     // ------------------------------------------------------------ dequantizers
-    const int q = warp & 3, g = (warp - LY::DQ_W0) >> 2;
-#define MXK_DQD_LOOP(F)                                                                   \
-  dequant_loop<F, NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty,         \
-                      bar_slot_free, bar_a_ready, q, g, lane, abort)
-    switch (a.fmt) {
-      case FMT_INT4: MXK_DQD_LOOP(FMT_INT4); break;
-      case FMT_INT8: MXK_DQD_LOOP(FMT_INT8); break;
-      case FMT_INT2: MXK_DQD_LOOP(FMT_INT2); break;
-      case FMT_E2M1: MXK_DQD_LOOP(FMT_E2M1); break;
-      case FMT_E5M2: MXK_DQD_LOOP(FMT_E5M2); break;
-      default: MXK_DQD_LOOP(FMT_E4M3); break;
-    }
-#undef MXK_DQD_LOOP
+    dequant_any<NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty, bar_slot_free,
+                    bar_a_ready, warp & 3, (warp - LY::DQ_W0) >> 2, ngroups, lane, abort);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    // with a single block the epilogue has nothing to do until the last
+    // MMA: these four warps convert quads meanwhile, as one more group
+    if (ngroups > LY::DQG)
+      dequant_any<NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty, bar_slot_free,
+                      bar_a_ready, q, LY::DQG, ngroups, lane, abort);
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     for (int job = 0; job < wk.n_jobs; ++job) {
       const uint32_t buf = job & 1, use = job >> 1;
