@@ -803,6 +803,19 @@ def run_ours(args, rank, world, local_rank):
             if workloads.is_dequant(oc):
                 gbs = dequant_bytes(oc) / ms_o / 1e6
                 others[name].update({"gbs": gbs, "frac_of_hbm": gbs / hbm})
+        # the four projections of one transformer layer (QKV, out, up, down):
+        # their summed flops over their summed times
+        projs = [n for n in ("proj_qkv", "proj_out", "proj_up", "proj_down") if n in others]
+        if len(projs) == 4:
+            flop = sum(flops_of(workloads.case(n)) for n in projs)
+            ms = sum(others[n]["gemm_ms"] for n in projs)
+            agg = {"gemms": projs, "gemm_ms": ms, "tflops": flop / (ms * 1e-3) / 1e12}
+            agg["frac_of_peak"] = agg["tflops"] / (bf16 * NOMINAL_RATIO["mxfp8"])
+            if all("graph_ms" in others[n] for n in projs):
+                gms = sum(others[n]["graph_ms"] for n in projs)
+                agg.update({"graph_ms": gms, "graph_tflops": flop / (gms * 1e-3) / 1e12})
+                agg["graph_frac_of_peak"] = agg["graph_tflops"] / (bf16 * NOMINAL_RATIO["mxfp8"])
+            others["proj_layer_aggregate"] = agg
         del fl
     attention = {}
     if not args.no_attention and rank == 0:
@@ -945,6 +958,11 @@ def provenance_rows(line):
                  frac_of_peak=(line.get("roofline") or {}).get("frac"),
                  breakdown=line.get("breakdown"))]
     for name, r in (line.get("gemm_only_other_workloads") or {}).items():
+        if name == "proj_layer_aggregate":
+            rows.append(dict(env, op="gemm_aggregate", workload=name, gemms=r["gemms"],
+                             ms=r["gemm_ms"], tflops=r["tflops"],
+                             frac_of_peak=r["frac_of_peak"]))
+            continue
         rows.append(dict(env, op="gemm", workload=name, **case_fields(name),
                          ms=r["gemm_ms"], tflops=r["tflops"],
                          frac_of_peak=r["frac_of_peak"],
