@@ -26,8 +26,7 @@
 //   * warp 0: code producer -- per quad one copy of the block's codes (128
 //     rows x 256 K: 128-byte rows in the 128-byte swizzle; 8-bit codes as two
 //     such boxes, 2-bit codes as 64-byte rows in the 64-byte swizzle) and
-//     one of its two scale atoms, into a ring as deep as shared memory
-//     allows;
+//     its two scale atoms, into a ring as deep as shared memory allows;
 //   * the last warp: token producer -- per quad one three-dimensional copy of
 //     the tokens' 256-K slice (NT rows x 4 x 64 K, 128-byte swizzle), into
 //     the quad's slot;
@@ -35,7 +34,9 @@
 //     lane quarter) that take the quads in turn, one weight row per thread:
 //     codes x scale -> 16-bit values written straight into the quad's
 //     tensor-memory slot (tcgen05.st, 32 columns per 64 K), never through
-//     shared memory; one arrival per quad;
+//     shared memory; one arrival per quad.  With a single weight block per
+//     CTA (as in every cluster) the four epilogue warps, idle until the
+//     last MMA, join as one more group;
 //   * warp 1: tensor-memory allocation and the MMA loop (one elected lane
 //     issues): per quad up to 16 kind::f16 MMAs, M = 128 weight rows, N = NT
 //     tokens, A read from the slot, B (the tokens) from shared memory, then
@@ -82,7 +83,9 @@ constexpr int SMEM_BUDGET = 200 * 1024;  // token slots + code ring
 // quarter warp % 4), four epilogue warps, token producer.  Two groups take
 // the quads in turn for NT = 64 (one quad's conversion and stores overlap
 // the other's); NT = 128, whose accumulators leave room for two slots and
-// whose epilogue needs more registers, keeps one group.
+// whose epilogue needs more registers, keeps one group.  The epilogue warps
+// add a group when the CTA has one block (3 for NT = 64, 2 for NT = 128:
+// one per slot).
 template <int NT>
 struct Lay {
   static constexpr int DQG = (NT == 64) ? 2 : 1;
