@@ -137,6 +137,8 @@ def _cluster_size(N, K, sms):
                                      (64, 128 * 64, 1216, 2),    # 64 blocks, last quad 3 steps
                                      (128, 128 * 50, 768, 2),    # NT = 128
                                      (5, 128 * 200, 512, 1),     # 200 blocks: some CTAs take two
+                                     (100, 128 * 200, 256, 1),   # the same with NT = 128
+                                     (128, 128 * 100, 512, 1),   # NT = 128, one block per CTA
                                      (64, 128 * 20, 256, 1)])    # one quad: no split
 def test_decode_cluster_sizes(M, N, K, S):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
