@@ -633,9 +633,9 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None:
                 ev[1].record(stream)
 
-    # our kernels per step: 2 quantizes (MX) + the GEMM (+ the partials'
-    # reduction when the K-split is active)
-    launches_per_step = (3 if is_mx else 1) + (1 if ws is not None else 0)
+    # our kernels per step: 2 quantizes (MX) + the GEMM (the K-split, when
+    # active, sums its partials inside the same GEMM launch)
+    launches_per_step = 3 if is_mx else 1
     # operands smaller than L2: flush it between timed steps, and take the
     # step time from the kernels' own events (the flush is not timed)
     src_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
