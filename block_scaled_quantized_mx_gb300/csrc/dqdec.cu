@@ -106,6 +106,8 @@ constexpr int MAX_CLUSTER = 8;
 // a_ready[3], acc_full[2], acc_empty[2]
 constexpr int NBAR = 2 * MAX_CS + 3 * MAX_SLOTS + 4;
 constexpr int MISC_BYTES = 16;   // tensor-memory address, abort flag
+// everything, with the 1024-byte alignment slack, within a CTA's 227 KB
+static_assert(SMEM_BUDGET + 8 * NBAR + MISC_BYTES + 1024 <= 227 * 1024, "shared memory");
 
 struct DecArgs {
   void* C;
@@ -119,6 +121,11 @@ struct DecArgs {
   int S;                // cluster size: the ranks that split one block's quads
   EpiArgs epi;
 };
+
+// One outcome of a wait for a whole warp: the tensor-memory instructions
+// after the warp-wide waits are warp-collective, so no lane may go on while
+// another gives up.
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
 
 __device__ __forceinline__ void dqd_timeout(volatile int* abort, unsigned site) {
   *abort = 1;
@@ -199,12 +206,12 @@ __device__ __forceinline__ void dequant_loop(const DecArgs& a, const Work& wk,
     const int qi = wk.qa + i % wk.jq;
     const int nu = min(QU, wk.kch - QU * qi);
     const int s = i % a.cs;
-    if (!mbar_wait_short(bar_code_full + 8 * s, (i / a.cs) & 1, abort)) {
+    if (!warp_all(mbar_wait_short(bar_code_full + 8 * s, (i / a.cs) & 1, abort))) {
       dqd_timeout(abort, 21);
       return;
     }
     const int slot = i % LY::SLOTS;
-    if (!mbar_wait_short(bar_slot_free + 8 * slot, ((i / LY::SLOTS) & 1) ^ 1, abort)) {
+    if (!warp_all(mbar_wait_short(bar_slot_free + 8 * slot, ((i / LY::SLOTS) & 1) ^ 1, abort))) {
       dqd_timeout(abort, 22);
       return;
     }
@@ -451,7 +458,7 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     bool ok = true;
     for (int job = 0; job < wk.n_jobs && ok; ++job) {
       const uint32_t buf = job & 1, use = job >> 1;
-      if (!mbar_wait_spin(bar_acc_empty + 8 * buf, (use & 1u) ^ 1u, abort)) {
+      if (!warp_all(mbar_wait_spin(bar_acc_empty + 8 * buf, (use & 1u) ^ 1u, abort))) {
         dqd_timeout(abort, 23);
         break;
       }
@@ -462,8 +469,8 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
         const uint32_t sph = (i / SLOTS) & 1u;
         // the MMA warp's waits are on the critical path: spin rather than
         // sleep through a wake-up
-        if (!mbar_wait_spin(bar_a_ready + 8 * slot, sph, abort) ||
-            !mbar_wait_spin(bar_x_full + 8 * slot, sph, abort)) {
+        if (!warp_all(mbar_wait_spin(bar_a_ready + 8 * slot, sph, abort) &&
+                      mbar_wait_spin(bar_x_full + 8 * slot, sph, abort))) {
           dqd_timeout(abort, 24);
           ok = false;
           break;
@@ -503,7 +510,7 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     for (int job = 0; job < wk.n_jobs; ++job) {
       const uint32_t buf = job & 1, use = job >> 1;
-      if (!mbar_wait(bar_acc_full + 8 * buf, use & 1u, abort)) {
+      if (!warp_all(mbar_wait(bar_acc_full + 8 * buf, use & 1u, abort))) {
         dqd_timeout(abort, 25);
         break;
       }

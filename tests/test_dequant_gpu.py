@@ -115,11 +115,14 @@ def test_dequant_padded_ldc(out, ld, off, split):
     assert torch.isnan(big[:, off + N:].float()).all()
 
 
-@pytest.mark.parametrize("fmt", [oracle.INT8, oracle.INT2, oracle.E5M2])
-def test_dequant_wide_scales_bf16(fmt):
+@pytest.mark.parametrize("M", [256, 64])
+@pytest.mark.parametrize("fmt", [oracle.INT8, oracle.INT4, oracle.INT2, oracle.E5M2])
+def test_dequant_wide_scales_bf16(fmt, M):
     """bf16 A: scales across a wide range are still exact after the
-    dequantization to bf16."""
-    M, N, K = 256, 256, 256
+    dequantization to bf16 (M = 64: the decode kernel, whose quads take a
+    shorter conversion loop when every scale code is at most 231, or 247 for
+    4- and 2-bit codes, and the general one otherwise)."""
+    N, K = 256, 256
     g = torch.Generator().manual_seed(90 + fmt)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     cb, sb = workloads.random_codes((N, K), fmt, seed=91 + fmt, scale_lo=40,
