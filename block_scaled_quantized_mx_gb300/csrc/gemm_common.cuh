@@ -22,7 +22,9 @@ enum Out : int { OUT_F32 = 0, OUT_BF16 = 1, OUT_MX8 = 2, OUT_MX4 = 3 };
 // Tiles walked in groups of `group` tile rows, column by column inside a
 // group, so that the clusters running at the same time share A and B tiles
 // in L2, and a group's rows of A stay in L2 while all of B streams past them
-// once: B is read from DRAM once per group.
+// once: B is read from DRAM once per group.  Odd groups walk the columns
+// backwards, so a group starts on the columns of B its predecessor read last
+// (still in L2).
 struct TileSched {
   int num_m, num_n, total;   // in tiles
   int group = GROUP_M;       // tile rows per raster group
@@ -33,7 +35,7 @@ struct TileSched {
     const int gsz = min(num_m - first_m, group);
     const int r = t - g * per_group;
     mb = first_m + r % gsz;
-    nb = r / gsz;
+    nb = (g & 1) ? num_n - 1 - r / gsz : r / gsz;
   }
 };
 
