@@ -495,18 +495,21 @@ dqdec_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
       if (issuer) tc_commit(bar_acc_full + 8 * buf);
       __syncwarp();
     }
-  } else if (warp < EPI_W0) {
-    // ------------------------------------------------------------ dequantizers
-    dequant_any<NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty, bar_slot_free,
-                    bar_a_ready, warp & 3, (warp - LY::DQ_W0) >> 2, ngroups, lane, abort);
   } else {
+    // ------------------------------------------------------------ dequantizers
+    // One call site for every group, so the conversion loop exists once in
+    // the code and in the instruction cache.  With a single block the
+    // epilogue warps have nothing to do until the last MMA: they convert
+    // quads meanwhile, as one more group.
+    const bool epi_warp = warp >= EPI_W0;
+    if (!epi_warp || ngroups > LY::DQG)
+      dequant_any<NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty, bar_slot_free,
+                      bar_a_ready, warp & 3, epi_warp ? LY::DQG : (warp - LY::DQ_W0) >> 2,
+                      ngroups, lane, abort);
+  }
+  if (warp >= EPI_W0 && warp < EPI_W0 + NUM_EPI) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    // with a single block the epilogue has nothing to do until the last
-    // MMA: these four warps convert quads meanwhile, as one more group
-    if (ngroups > LY::DQG)
-      dequant_any<NT>(a, wk, code_base, tmem_base, bar_code_full, bar_code_empty, bar_slot_free,
-                      bar_a_ready, q, LY::DQG, ngroups, lane, abort);
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     for (int job = 0; job < wk.n_jobs; ++job) {
       const uint32_t buf = job & 1, use = job >> 1;
