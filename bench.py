@@ -1119,7 +1119,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--others", default="mxfp8_4096,mxfp4_8192,mxfp4_4096,"
                     "mxfp8_e5m2_8192,w4a8_8192,w4a16_8192,w2a16_8192,"
-                    "w4a16_decode,"
+                    "w4a16_decode,w4a16_decode_m1,"
                     "bf16_4096,f16_4096,bf16_2048,bf16_1024,proj_qkv,proj_out,"
                     "proj_up,proj_down,mx256",
                     help="workloads whose GEMM alone is also timed (L2 "

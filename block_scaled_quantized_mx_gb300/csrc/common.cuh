@@ -102,6 +102,14 @@ cudaError_t launch_gemm_dequant_decode(int a_dtype, const void* A, int64_t lda, 
                                        const Epilogue& epi, cudaStream_t st);
 unsigned fetch_and_clear_status_dqd(cudaError_t* err);
 
+// A single row of a bf16 A and 4- or 2-bit weights (dqgemv.cu): CUDA-core
+// dot products streaming B once, for a plain or bias / activation output; K
+// a multiple of 64.  No workspace, no waits.
+bool dequant_gemv_applies(int64_t M, int a_dtype, int fmt_b, const Epilogue& epi);
+cudaError_t launch_gemm_dequant_gemv(const void* A, int fmt_b, const void* b_data,
+                                     const uint8_t* b_sf, void* C, int c_dtype, int64_t N,
+                                     int64_t K, const Epilogue& epi, cudaStream_t st);
+
 // O = softmax(Q K^T * scale) V for BH heads: Q BH x Lq x d, K and V
 // BH x Lk x d, row-major, dtype DT_F16 / DT_BF16; d 64 or 128; O BH x Lq x d
 // of o_dtype (DT_F32, DT_BF16 or DT_F16).

@@ -584,6 +584,10 @@ cudaError_t launch_gemm_dequant(int a_dtype, const void* A, int64_t lda, int fmt
                                 void* ws, size_t ws_bytes, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (K == 0 || K % DQ_KPS) return cudaErrorInvalidValue;
+  // one token of a bf16 A, 4- or 2-bit weights: CUDA-core dot products
+  // streaming B (dqgemv.cu)
+  if (dequant_gemv_applies(M, a_dtype, fmt_b, epi))
+    return launch_gemm_dequant_gemv(A, fmt_b, b_data, b_sf, C, c_dtype, N, K, epi, st);
   // a few tokens: the weights-as-M decode kernel (dqdec.cu)
   if (dequant_decode_applies(M, epi))
     return launch_gemm_dequant_decode(a_dtype, A, lda, fmt_b, b_data, b_sf, C, c_dtype, ldc, M,

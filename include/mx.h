@@ -258,7 +258,11 @@ mx_status gemm_f16_fused(const void* A, const void* B, const mx_epilogue* epi,
  * rows, dequantized into tensor memory 256 K at a time, A's rows its columns;
  * when the blocks are fewer than the SMs, each block's K range is split over
  * a thread-block cluster of up to 8 CTAs whose partial sums are added in a
- * fixed order on chip (no workspace, same bits every run).
+ * fixed order on chip (no workspace, same bits every run).  A single row of
+ * a bf16 A with 4- or 2-bit codes (int4, int2, E2M1: decoding one token)
+ * takes a third kernel that streams B once on the CUDA cores: each lane
+ * dequantizes whole 32-element blocks to the same bf16 values and sums
+ * their products with A in fp32 (no workspace, same bits every run).
  *
  *   A        device, M x K, row-major, element type a_dtype (MX_DT_F16 or
  *            MX_DT_BF16); lda >= K, a multiple of 8; 16-byte aligned

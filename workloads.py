@@ -22,7 +22,8 @@ Workloads (sizes and value recipes):
              E2M1 weights (B, N(0, 0.02)), M=N=K in {2048, 8192}, bf16 output
   w4a16      weight-only quantization: bf16 activations (A, N(0,1)) times
              int4 weights (B, N(0, 0.02), quantized by the MX rule),
-             M=N=K=8192, and a decode-shaped M=64, N=K=8192; bf16 output
+             M=N=K=8192, a decode-shaped M=64, N=K=8192, and a single
+             token M=1, N=K=8192; bf16 output
   w2a16      the same with int2 weights, M=N=K=8192
   attn       fused attention over image tokens: 2 images x 16 heads, 4096
              tokens each (a 64 x 64 patch grid, the image-segmentation model
@@ -119,7 +120,8 @@ def dequant_cases():
     out = []
     for i, (name, kind, M) in enumerate((("w4a16_8192", "w4a16", 8192),
                                          ("w2a16_8192", "w2a16", 8192),
-                                         ("w4a16_decode", "w4a16", 64))):
+                                         ("w4a16_decode", "w4a16", 64),
+                                         ("w4a16_decode_m1", "w4a16", 1))):
         sa, sb = _seeds(7, i)
         out.append(GemmCase(name, kind, M, 8192, 8192, "bf16", "normal",
                             "weight", sa, sb))
