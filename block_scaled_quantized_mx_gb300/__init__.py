@@ -415,8 +415,8 @@ def gemm_dequant(A: torch.Tensor, B: MXTensor, bias: torch.Tensor | None = None,
                  workspace: torch.Tensor | None = None) -> torch.Tensor:
     """C = act(A * dequant(B)^T + bias) for a row-major fp16 / bf16 A
     (M x K) and an MX tensor B of any format (N x K, quantized from a K x N
-    matrix): B is dequantized to A's type in shared or tensor memory (for
-    one to four rows of a bf16 A, exactly, in fp32 registers).  With a
+    matrix): B is dequantized to A's type in shared or tensor memory, or in
+    registers for a single bf16 row with 4- or 2-bit codes.  With a
     workspace (gemm_dequant_workspace_bytes) the K-split entry point runs."""
     if A.dtype not in (torch.float16, torch.bfloat16) or A.dim() != 2:
         raise ValueError("A must be a 2-D fp16 or bf16 tensor")

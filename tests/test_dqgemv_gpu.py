@@ -165,9 +165,9 @@ def test_gemv_deterministic():
 
 
 def test_f16_tokens_take_the_decode_kernel():
-    """An f16 A of one to four rows is not the GEMV's case (its B
-    dequantization to f16 may round or overflow where fp32 would not); the
-    tensor-core decode kernel takes it, and still matches the oracle."""
+    """An f16 A is not the single-token kernel's case (it dequantizes to
+    bf16); the tensor-core decode kernel takes it, and still matches the
+    oracle."""
     M, N, K, fmt = 2, 384, 1024, oracle.INT4
     g = torch.Generator().manual_seed(9)
     A = torch.randn(M, K, generator=g).to(torch.float16)
